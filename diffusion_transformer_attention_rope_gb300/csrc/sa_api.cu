@@ -1,0 +1,285 @@
+// sa_api.cu -- the C ABI declared in include/sa_attn.h: host-side argument checks, the
+// per-device handle, TMA descriptor encoding and the two launches (RoPE pre-pass, attention).
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "sa_attn.h"
+#include "sa_kernels.h"
+
+struct sa_attn_s {
+  int device;
+  int num_sms;
+  float rope_base;
+  float inv_freq[sa::kHeadDim / 2];
+  int* d_err;  // 4-byte device error word
+  PFN_cuTensorMapEncodeTiled_v12000 encode;
+  unsigned long long timeout_ns;
+};
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+sa_status fail(sa_status st, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return st;
+}
+
+sa_status ok() {
+  g_msg[0] = '\0';
+  return SA_OK;
+}
+
+// Switches to `dev` for the lifetime of the object and restores the caller's device.
+struct DeviceGuard {
+  int prev = -1;
+  bool ok = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) != cudaSuccess) return;
+    ok = prev == dev || cudaSetDevice(dev) == cudaSuccess;
+  }
+  ~DeviceGuard() {
+    int cur = -1;
+    if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+  }
+};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+// 3-D tiled map over a [planes][rows][cols] array of 2-byte elements: box = 64 cols x 128 rows x
+// 1 plane, 128-byte swizzle (the layout the tcgen05 descriptors expect).  Rows past the end
+// of a plane read as zeros.
+bool encode_map(const sa_attn_s* h, CUtensorMap* m, const void* base, bool bf16, uint64_t cols,
+                uint64_t rows, uint64_t planes) {
+  const cuuint64_t dims[3] = {cols, rows, planes};
+  const cuuint64_t strides[2] = {cols * 2, cols * 2 * rows};
+  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(sa::kBlockN), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = h->encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                         3, const_cast<void*>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool qk_elems(int B, int H, int L, int nmaps, size_t* out) {
+  if (B <= 0 || H <= 0 || L <= 0) return false;
+  const unsigned long long n = static_cast<unsigned long long>(B) * H * nmaps * L * sa::kHeadDim;
+  if (n >= (1ull << 40)) return false;
+  *out = static_cast<size_t>(n);
+  return true;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* sa_last_error(void) { return g_msg; }
+
+const char* sa_status_string(sa_status s) {
+  switch (s) {
+    case SA_OK: return "SA_OK";
+    case SA_ERR_INVALID_ARG: return "SA_ERR_INVALID_ARG";
+    case SA_ERR_UNSUPPORTED: return "SA_ERR_UNSUPPORTED";
+    case SA_ERR_CUDA: return "SA_ERR_CUDA";
+    case SA_ERR_DEVICE_TIMEOUT: return "SA_ERR_DEVICE_TIMEOUT";
+    case SA_ERR_NO_DEVICE: return "SA_ERR_NO_DEVICE";
+    case SA_ERR_WORKSPACE: return "SA_ERR_WORKSPACE";
+  }
+  return "SA_ERR_UNKNOWN";
+}
+
+sa_status sa_attn_create(sa_attn_t* handle, int device, float rope_base) {
+  if (!handle) return fail(SA_ERR_INVALID_ARG, "sa_attn_create: handle pointer is NULL");
+  *handle = nullptr;
+  if (!(rope_base > 1.0f) || !std::isfinite(rope_base))
+    return fail(SA_ERR_INVALID_ARG, "sa_attn_create: rope_base must be finite and > 1 (got %g)",
+                static_cast<double>(rope_base));
+  int count = 0;
+  cudaError_t e = cudaGetDeviceCount(&count);
+  if (e != cudaSuccess || count == 0)
+    return fail(SA_ERR_NO_DEVICE, "sa_attn_create: no CUDA device (%s)", cudaGetErrorString(e));
+  if (device < 0 || device >= count)
+    return fail(SA_ERR_NO_DEVICE, "sa_attn_create: device %d out of range [0, %d)", device, count);
+  DeviceGuard guard(device);
+  if (!guard.ok) return fail(SA_ERR_CUDA, "sa_attn_create: cannot select device %d", device);
+  cudaDeviceProp prop;
+  if ((e = cudaGetDeviceProperties(&prop, device)) != cudaSuccess)
+    return fail(SA_ERR_CUDA, "sa_attn_create: %s", cudaGetErrorString(e));
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(SA_ERR_UNSUPPORTED,
+                "sa_attn_create: device %d is sm_%d%d; this library is built for sm_103a (GB300)",
+                device, prop.major, prop.minor);
+
+  sa_attn_s* h = new (std::nothrow) sa_attn_s();
+  if (!h) return fail(SA_ERR_CUDA, "sa_attn_create: out of host memory");
+  h->device = device;
+  h->num_sms = prop.multiProcessorCount;
+  h->rope_base = rope_base;
+  h->timeout_ns = 1000000000ull;  // 1 s per pipeline wait
+  for (int i = 0; i < sa::kHeadDim / 2; ++i)
+    h->inv_freq[i] = static_cast<float>(
+        std::pow(static_cast<double>(rope_base), -2.0 * i / static_cast<double>(sa::kHeadDim)));
+
+  cudaDriverEntryPointQueryResult q;
+  void* fn = nullptr;
+  e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+    delete h;
+    return fail(SA_ERR_CUDA, "sa_attn_create: cuTensorMapEncodeTiled unavailable (%s)",
+                cudaGetErrorString(e));
+  }
+  h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  if ((e = cudaMalloc(&h->d_err, sizeof(int))) != cudaSuccess) {
+    delete h;
+    return fail(SA_ERR_CUDA, "sa_attn_create: cudaMalloc: %s", cudaGetErrorString(e));
+  }
+  if ((e = cudaMemset(h->d_err, 0, sizeof(int))) != cudaSuccess ||
+      (e = sa::fmha_set_attributes()) != cudaSuccess) {
+    cudaFree(h->d_err);
+    delete h;
+    return fail(SA_ERR_CUDA, "sa_attn_create: %s", cudaGetErrorString(e));
+  }
+  *handle = h;
+  return ok();
+}
+
+sa_status sa_attn_destroy(sa_attn_t h) {
+  if (!h) return ok();
+  {
+    DeviceGuard guard(h->device);
+    cudaDeviceSynchronize();
+    cudaFree(h->d_err);
+  }
+  delete h;
+  return ok();
+}
+
+size_t sa_rope_attn_workspace_size(int B, int H, int L, int d, int differential) {
+  size_t n = 0;
+  if (d != sa::kHeadDim || !qk_elems(B, H, L, differential ? 2 : 1, &n)) return 0;
+  return 2 * align256(n * 2);
+}
+
+sa_status sa_rope_attn(sa_attn_t h, const void* q, const void* k, const void* v,
+                       const int32_t* positions, void* out, int B, int H, int L, int d, int window,
+                       const float* lambda, sa_dtype dtype, void* workspace,
+                       size_t workspace_bytes, sa_stream_t stream) {
+  if (!h) return fail(SA_ERR_INVALID_ARG, "sa_rope_attn: handle is NULL");
+  if (!q || !k || !v || !out)
+    return fail(SA_ERR_INVALID_ARG, "sa_rope_attn: q, k, v and out must be non-NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      (workspace && !aligned16(workspace)))
+    return fail(SA_ERR_INVALID_ARG, "sa_rope_attn: q, k, v, out and workspace must be 16-byte aligned");
+  if (B <= 0 || H <= 0 || L <= 0)
+    return fail(SA_ERR_INVALID_ARG, "sa_rope_attn: B, H, L must be >= 1 (got %d, %d, %d)", B, H, L);
+  if (L >= sa::kMaxL)
+    return fail(SA_ERR_UNSUPPORTED, "sa_rope_attn: L = %d exceeds the supported maximum %d", L,
+                sa::kMaxL - 1);
+  if (d != sa::kHeadDim)
+    return fail(SA_ERR_UNSUPPORTED, "sa_rope_attn: head dim d = %d; only d = 64 is supported", d);
+  if (dtype != SA_FP16 && dtype != SA_BF16)
+    return fail(SA_ERR_INVALID_ARG, "sa_rope_attn: unknown dtype %d", static_cast<int>(dtype));
+  const bool diff = lambda != nullptr;
+  const int nmaps = diff ? 2 : 1;
+  const int dv = diff ? 2 * d : d;
+  if (diff && H > sa::kMaxDiffHeads)
+    return fail(SA_ERR_UNSUPPORTED, "sa_rope_attn: differential attention supports H <= %d (got %d)",
+                sa::kMaxDiffHeads, H);
+  size_t nqk = 0;
+  if (!qk_elems(B, H, L, nmaps, &nqk) ||
+      static_cast<unsigned long long>(B) * H * L * dv >= (1ull << 40))
+    return fail(SA_ERR_INVALID_ARG, "sa_rope_attn: tensor sizes overflow");
+  if (static_cast<long long>(B) * H * ((L + sa::fmha_rows_per_cta(diff) - 1) /
+                                       sa::fmha_rows_per_cta(diff)) >= (1ll << 31))
+    return fail(SA_ERR_UNSUPPORTED, "sa_rope_attn: too many query tiles for one launch");
+  if (diff) {
+    for (int i = 0; i < H; ++i)
+      if (!std::isfinite(lambda[i]))
+        return fail(SA_ERR_INVALID_ARG, "sa_rope_attn: lambda[%d] is not finite", i);
+  }
+  const size_t need = sa_rope_attn_workspace_size(B, H, L, d, diff);
+  if (!workspace || workspace_bytes < need)
+    return fail(SA_ERR_WORKSPACE, "sa_rope_attn: workspace of %zu bytes needed, %zu given%s", need,
+                workspace_bytes, workspace ? "" : " (NULL)");
+
+  const bool bf16 = dtype == SA_BF16;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint16_t* q_rot = reinterpret_cast<uint16_t*>(ws);
+  uint16_t* k_rot = reinterpret_cast<uint16_t*>(ws + align256(nqk * 2));
+
+  const unsigned long long planes_qk = static_cast<unsigned long long>(B) * H * nmaps;
+  const unsigned long long planes_v = static_cast<unsigned long long>(B) * H;
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (!encode_map(h, &tm_q, q_rot, bf16, d, L, planes_qk) ||
+      !encode_map(h, &tm_k, k_rot, bf16, d, L, planes_qk) ||
+      !encode_map(h, &tm_v, v, bf16, dv, L, planes_v))
+    return fail(SA_ERR_CUDA, "sa_rope_attn: cuTensorMapEncodeTiled rejected a tensor map");
+
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return fail(SA_ERR_CUDA, "sa_rope_attn: cannot select device %d", h->device);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+
+  sa::RopeArgs ra;
+  ra.q = static_cast<const uint16_t*>(q);
+  ra.k = static_cast<const uint16_t*>(k);
+  ra.q_out = q_rot;
+  ra.k_out = k_rot;
+  ra.positions = positions;
+  ra.planes = static_cast<long long>(planes_qk);
+  ra.L = L;
+  ra.planes_per_block = 1;
+  std::memcpy(ra.inv_freq, h->inv_freq, sizeof(ra.inv_freq));
+  cudaError_t e = sa::rope_launch(ra, bf16, h->num_sms, st);
+  if (e != cudaSuccess) return fail(SA_ERR_CUDA, "sa_rope_attn: RoPE launch: %s", cudaGetErrorString(e));
+
+  sa::FmhaArgs fa;
+  std::memset(&fa, 0, sizeof(fa));
+  fa.out = out;
+  fa.err = h->d_err;
+  fa.L = L;
+  fa.H = H;
+  const int rows = sa::fmha_rows_per_cta(diff);
+  fa.n_qblocks = (L + rows - 1) / rows;
+  fa.window = (window < 0 || window >= L - 1) ? -1 : window;
+  fa.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  fa.timeout_ns = h->timeout_ns;
+  if (diff)
+    for (int i = 0; i < H; ++i) fa.lambda[i] = lambda[i];
+  const long long ctas = static_cast<long long>(B) * H * fa.n_qblocks;
+  e = sa::fmha_launch(diff, bf16, tm_q, tm_k, tm_v, fa, ctas, st);
+  if (e != cudaSuccess)
+    return fail(SA_ERR_CUDA, "sa_rope_attn: attention launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+sa_status sa_attn_check(sa_attn_t h) {
+  if (!h) return fail(SA_ERR_INVALID_ARG, "sa_attn_check: handle is NULL");
+  DeviceGuard guard(h->device);
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return fail(SA_ERR_CUDA, "sa_attn_check: %s", cudaGetErrorString(e));
+  int word = 0;
+  if ((e = cudaMemcpy(&word, h->d_err, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess ||
+      (e = cudaMemset(h->d_err, 0, sizeof(int))) != cudaSuccess)
+    return fail(SA_ERR_CUDA, "sa_attn_check: %s", cudaGetErrorString(e));
+  if (word != 0)
+    return fail(SA_ERR_DEVICE_TIMEOUT,
+                "sa_attn_check: a kernel gave up on a pipeline wait (error bits 0x%x: 1 = TMA, "
+                "2 = MMA, 4 = softmax)",
+                word);
+  return ok();
+}
+
+}  // extern "C"

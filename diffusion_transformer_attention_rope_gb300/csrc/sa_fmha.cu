@@ -1,0 +1,494 @@
+// sa_fmha.cu -- fused attention on rotated q', k' for sm_103a (GB300).
+//
+// Computes out = softmax(q' k'^T / sqrt(d)) v with the softmax accumulated in FP32
+// (HF discussion #3 "fp16mixed attention-core fix", section "The bug": SDPA on fp16 inputs,
+// FMHA accumulating the softmax in FP32), its differential form
+// out = O(Q1,K1) - lambda_h * O(Q2,K2) with the subtraction done in FP32 on the FP32
+// accumulators (HF discussion #6 "sm_120 SAME-L", section "How the kernels differ"), and the
+// symmetric sliding window |i - j| <= w (same page, "Three gotchas").
+//
+// One CTA (320 threads, 1 per SM) owns 256 query rows of one (batch, head) as two 128-row
+// tiles (standard), or 128 rows with both maps (differential).  Warp roles:
+//   warps 0-3, 4-7  softmax warpgroups, one per tile / map: thread = query row = TMEM lane.
+//   warp 8          TMA producer: Q tiles once, then a ring of K/V stages (128 keys each).
+//   warp 9          TMEM allocator and the single-thread tcgen05.mma issuer.
+// Per K/V tile and warpgroup s:
+//   S_s = Q_s K^T      tcgen05.mma, A and B from 128B-swizzled smem, fp32 into TMEM
+//   P_s = exp2(S_s*c - m)   softmax warps: tcgen05.ld S, row max, lazy rescale of O_s
+//                      (only when the running max grows by more than 2^8), fp16/bf16 P
+//                      written back to TMEM with tcgen05.st
+//   O_s += P_s V       tcgen05.mma, A = P from TMEM, B = V (MN-major) from smem
+// TMEM (512 columns): standard S0|S1|P0|P1|O0|O1 = 128|128|64|64|64|64;
+// differential S0|S1|O0|O1 = 128|128|128|128 with P_s written over the first 64 columns of
+// S_s (the issuer waits for P_s V to finish before it writes the next S_s there).
+// The sliding window visits only the K/V tiles that intersect [q0 - w, q_last + w]; element
+// masks are applied only on tiles that are not entirely inside every row's window.
+// Every wait is bounded: on timeout a warp sets the device error word and a CTA-wide abort
+// flag, waits (bounded) for its own copies / MMAs in flight, and the CTA frees TMEM and exits.
+#include "sa_kernels.h"
+#include "sa_ptx.cuh"
+
+namespace sa {
+namespace {
+
+constexpr int kTile = kBlockM * kHeadDim * 2;  // bytes of one 128 x 64 fp16/bf16 tile (16 KB)
+constexpr int kTmaWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr uint32_t kTmemCols = 512;
+
+template <bool DIFF>
+struct Cfg {
+  static constexpr int NS = DIFF ? 2 : 3;                       // K/V ring stages
+  static constexpr int DV = DIFF ? 128 : 64;                    // value / output width
+  static constexpr int ROWS = fmha_rows_per_cta(DIFF);          // query rows per CTA
+  static constexpr int Q_BYTES = 2 * kTile;                     // two Q tiles (or maps)
+  static constexpr int K_STAGE = DIFF ? 2 * kTile : kTile;      // K (both maps for DIFF)
+  static constexpr int V_STAGE = DIFF ? 2 * kTile : kTile;      // V: 128 keys x DV
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_V = OFF_K + NS * K_STAGE;
+  static constexpr int OFF_BAR = OFF_V + NS * V_STAGE;
+  // barriers: q_full, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full[2],
+  //           pv_done[2], o_full, drain
+  static constexpr int NBAR = 1 + 3 * NS + 2 + 2 + 2 + 1 + 1;
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;           // tmem base, abort flag
+  static constexpr int OFF_LSUM = OFF_MISC + 16;                // float [2][128]
+  static constexpr int SMEM_USED = OFF_LSUM + 2 * kBlockM * 4;
+  static constexpr int SMEM_ALLOC = SMEM_USED + 1024;           // slack for 1 KB alignment
+  __device__ static uint32_t s_col(int s) { return s * 128; }
+  __device__ static uint32_t p_col(int s) { return DIFF ? s * 128 : 256 + s * 64; }
+  __device__ static uint32_t o_col(int s) { return DIFF ? 256 + s * 128 : 384 + s * 64; }
+};
+
+static_assert(Cfg<false>::SMEM_ALLOC <= 227 * 1024, "smem budget");
+static_assert(Cfg<true>::SMEM_ALLOC <= 227 * 1024, "smem budget");
+static_assert(Cfg<false>::SMEM_USED > 114 * 1024, "one CTA per SM keeps TMEM allocation uncontended");
+
+struct Barriers {
+  uint32_t q_full, k_full0, v_full0, kv_empty0, s_full0, p_full0, pv_done0, o_full, drain;
+  int ns;
+  __device__ uint32_t k_full(int i) const { return k_full0 + 8 * i; }
+  __device__ uint32_t v_full(int i) const { return v_full0 + 8 * i; }
+  __device__ uint32_t kv_empty(int i) const { return kv_empty0 + 8 * i; }
+  __device__ uint32_t s_full(int s) const { return s_full0 + 8 * s; }
+  __device__ uint32_t p_full(int s) const { return p_full0 + 8 * s; }
+  __device__ uint32_t pv_done(int s) const { return pv_done0 + 8 * s; }
+};
+
+// Pipeline wait: bounded by the wall clock and by the CTA abort flag.
+__device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                      int* err, int err_bit, uint64_t timeout_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (globaltimer_ns() - t0 > timeout_ns) {
+      *abort_flag = 1;
+      atomicOr(err, err_bit);
+      return false;
+    }
+  }
+}
+
+template <bool DIFF, bool BF16>
+__global__ void __launch_bounds__(kFmhaThreads, 1)
+    fmha_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FmhaArgs a) {
+  using C = Cfg<DIFF>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t sQ = sb + C::OFF_Q, sK = sb + C::OFF_K, sV = sb + C::OFF_V;
+
+  Barriers bar;
+  bar.ns = C::NS;
+  bar.q_full = sb + C::OFF_BAR;
+  bar.k_full0 = bar.q_full + 8;
+  bar.v_full0 = bar.k_full0 + 8 * C::NS;
+  bar.kv_empty0 = bar.v_full0 + 8 * C::NS;
+  bar.s_full0 = bar.kv_empty0 + 8 * C::NS;
+  bar.p_full0 = bar.s_full0 + 16;
+  bar.pv_done0 = bar.p_full0 + 16;
+  bar.o_full = bar.pv_done0 + 16;
+  bar.drain = bar.o_full + 8;
+
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  float* lsum = reinterpret_cast<float*>(smem + C::OFF_LSUM);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int L = a.L;
+  const int bh = blockIdx.x / a.n_qblocks;
+  const int q0 = (blockIdx.x % a.n_qblocks) * C::ROWS;
+  const int q_last = min(L, q0 + C::ROWS) - 1;
+  const int w = a.window;
+
+  // K/V tiles this CTA visits.
+  int t_lo = 0, t_hi = (L - 1) / kBlockN;
+  if (w >= 0) {
+    t_lo = max(0, q0 - w) / kBlockN;
+    t_hi = min(L - 1, q_last + w) / kBlockN;
+  }
+  const int n_tiles = t_hi - t_lo + 1;
+  const uint64_t tmo = a.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar.q_full, 1);
+    for (int i = 0; i < C::NS; ++i) {
+      mbar_init(bar.k_full(i), 1);
+      mbar_init(bar.v_full(i), 1);
+      mbar_init(bar.kv_empty(i), 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar.s_full(s), 1);
+      mbar_init(bar.p_full(s), kBlockM);
+      mbar_init(bar.pv_done(s), 1);
+    }
+    mbar_init(bar.o_full, 1);
+    mbar_init(bar.drain, 1);
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const int plane_q = DIFF ? 2 * bh : bh;
+      mbar_arrive_expect_tx(bar.q_full, C::Q_BYTES);
+      if (DIFF) {
+        tma_load_3d(sQ, &tm_q, bar.q_full, 0, q0, plane_q);
+        tma_load_3d(sQ + kTile, &tm_q, bar.q_full, 0, q0, plane_q + 1);
+      } else {
+        tma_load_3d(sQ, &tm_q, bar.q_full, 0, q0, plane_q);
+        tma_load_3d(sQ + kTile, &tm_q, bar.q_full, 0, q0 + kBlockM, plane_q);
+      }
+      int issued = 0;
+      for (int it = 0; it < n_tiles; ++it) {
+        const int st = it % C::NS;
+        const uint32_t ph = (it / C::NS) & 1;
+        if (!pwait(bar.kv_empty(st), ph ^ 1, abort_flag, a.err, kErrProducer, tmo)) break;
+        const int key0 = (t_lo + it) * kBlockN;
+        const uint32_t k_dst = sK + st * C::K_STAGE;
+        const uint32_t v_dst = sV + st * C::V_STAGE;
+        mbar_arrive_expect_tx(bar.k_full(st), C::K_STAGE);
+        if (DIFF) {
+          tma_load_3d(k_dst, &tm_k, bar.k_full(st), 0, key0, 2 * bh);
+          tma_load_3d(k_dst + kTile, &tm_k, bar.k_full(st), 0, key0, 2 * bh + 1);
+        } else {
+          tma_load_3d(k_dst, &tm_k, bar.k_full(st), 0, key0, bh);
+        }
+        mbar_arrive_expect_tx(bar.v_full(st), C::V_STAGE);
+        tma_load_3d(v_dst, &tm_v, bar.v_full(st), 0, key0, bh);
+        if (DIFF) tma_load_3d(v_dst + kTile, &tm_v, bar.v_full(st), 64, key0, bh);
+        issued = it + 1;
+      }
+      if (*abort_flag) {
+        // Let the copies already issued land before the CTA's shared memory goes away.
+        mbar_wait_limit(bar.q_full, 0, tmo);
+        const int first = issued > C::NS ? issued - C::NS : 0;
+        for (int it = first; it < issued; ++it) {
+          const int st = it % C::NS;
+          const uint32_t ph = (it / C::NS) & 1;
+          mbar_wait_limit(bar.k_full(st), ph, tmo);
+          mbar_wait_limit(bar.v_full(st), ph, tmo);
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == kMmaWarp) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t idesc_s = make_idesc_f16(kBlockM, kBlockN, BF16, false);
+      constexpr uint32_t idesc_o = make_idesc_f16(kBlockM, C::DV, BF16, true);
+      auto issue_s = [&](int s, int st) {
+        const uint32_t qa = sQ + s * kTile;
+        const uint32_t kb = sK + st * C::K_STAGE + (DIFF ? s * kTile : 0);
+#pragma unroll
+        for (int kk = 0; kk < kHeadDim / 16; ++kk)
+          umma_ss(tmem + C::s_col(s), smem_desc_sw128(qa + 32 * kk, 16, 1024),
+                  smem_desc_sw128(kb + 32 * kk, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+      };
+      auto issue_pv = [&](int s, int st, bool accumulate) {
+        const uint32_t vb = sV + st * C::V_STAGE;
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk)
+          umma_ts(tmem + C::o_col(s), tmem + C::p_col(s) + 8 * kk,
+                  smem_desc_sw128(vb + 2048 * kk, kTile, 1024), idesc_o,
+                  (accumulate || kk > 0) ? 1u : 0u);
+      };
+      bool ok = pwait(bar.q_full, 0, abort_flag, a.err, kErrMma, tmo) &&
+                pwait(bar.k_full(0), 0, abort_flag, a.err, kErrMma, tmo);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        umma_commit(bar.s_full(0));
+        issue_s(1, 0);
+        umma_commit(bar.s_full(1));
+      }
+      for (int it = 0; ok && it < n_tiles; ++it) {
+        const int st = it % C::NS;
+        const uint32_t ph = (it / C::NS) & 1;
+        const bool last = it + 1 == n_tiles;
+        const int st2 = (it + 1) % C::NS;
+        const uint32_t ph2 = ((it + 1) / C::NS) & 1;
+        if (!DIFF) {
+          for (int s = 0; s < 2 && ok; ++s) {
+            ok = pwait(bar.p_full(s), it & 1, abort_flag, a.err, kErrMma, tmo);
+            if (ok && s == 0) ok = pwait(bar.v_full(st), ph, abort_flag, a.err, kErrMma, tmo);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(s, st, it > 0);
+            if (s == 1) umma_commit(bar.kv_empty(st));
+            if (!last) {
+              if (s == 0) ok = pwait(bar.k_full(st2), ph2, abort_flag, a.err, kErrMma, tmo);
+              if (!ok) break;
+              tc_fence_after();
+              issue_s(s, st2);
+              umma_commit(bar.s_full(s));
+            }
+          }
+        } else {
+          ok = pwait(bar.v_full(st), ph, abort_flag, a.err, kErrMma, tmo);
+          for (int s = 0; s < 2 && ok; ++s) {
+            ok = pwait(bar.p_full(s), it & 1, abort_flag, a.err, kErrMma, tmo);
+            if (!ok) break;
+            tc_fence_after();
+            issue_pv(s, st, it > 0);
+            umma_commit(bar.pv_done(s));
+          }
+          if (ok) umma_commit(bar.kv_empty(st));
+          if (ok && !last) {
+            ok = pwait(bar.k_full(st2), ph2, abort_flag, a.err, kErrMma, tmo);
+            for (int s = 0; s < 2 && ok; ++s) {
+              // P_s lives in the S_s columns: the next S_s may only be written once P_s V is done.
+              ok = pwait(bar.pv_done(s), it & 1, abort_flag, a.err, kErrMma, tmo);
+              if (!ok) break;
+              tc_fence_after();
+              issue_s(s, st2);
+              umma_commit(bar.s_full(s));
+            }
+          }
+        }
+        if (ok && last) umma_commit(bar.o_full);
+      }
+      // No MMA may still be running when TMEM is released.
+      umma_commit(bar.drain);
+      mbar_wait_limit(bar.drain, 0, tmo);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ softmax warpgroups
+    const int s = warp >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;                     // TMEM lane = tile row
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const int grow = DIFF ? q0 + r : q0 + s * kBlockM + r;  // query row in the sequence
+    const float c = a.scale_log2;
+    const float tau = 8.0f / c;                            // lazy-rescale threshold (raw units)
+    const int rows_lo = q0, rows_hi = q0 + C::ROWS - 1;
+    float m_use = -INFINITY;
+    float l_sum = 0.0f;
+    bool ok = true;
+
+    for (int it = 0; it < n_tiles; ++it) {
+      ok = pwait(bar.s_full(s), it & 1, abort_flag, a.err, kErrSoftmax, tmo);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      uint32_t sr[kBlockN];
+#pragma unroll
+      for (int cc = 0; cc < kBlockN / 32; ++cc)
+        tmem_ld32_nowait(tmem + C::s_col(s) + lane_off + 32 * cc, sr + 32 * cc);
+      tmem_wait_ld_128(sr);
+
+      const int key0 = (t_lo + it) * kBlockN;
+      const bool need_mask =
+          (key0 + kBlockN > L) ||
+          (w >= 0 && !(key0 >= rows_hi - w && key0 + kBlockN - 1 <= rows_lo + w));
+      if (need_mask) {
+#pragma unroll
+        for (int j = 0; j < kBlockN; ++j) {
+          const int key = key0 + j;
+          bool valid = key < L;
+          if (w >= 0) valid = valid && key >= grow - w && key <= grow + w;
+          if (!valid) sr[j] = __float_as_uint(-INFINITY);
+        }
+      }
+      float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
+      float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+#pragma unroll
+      for (int j = 4; j < kBlockN; j += 4) {
+        mx0 = fmaxf(mx0, __uint_as_float(sr[j]));
+        mx1 = fmaxf(mx1, __uint_as_float(sr[j + 1]));
+        mx2 = fmaxf(mx2, __uint_as_float(sr[j + 2]));
+        mx3 = fmaxf(mx3, __uint_as_float(sr[j + 3]));
+      }
+      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+
+      // Lazy rescale: keep the old running max unless this tile raises it by more than tau
+      // (P then stays <= 2^8).  The decision is warp-uniform because tcgen05.ld/st are.
+      float f = 1.0f;
+      bool rescale = false;
+      if (it == 0) {
+        m_use = mt;
+      } else if (__any_sync(0xffffffffu, mt > m_use + tau)) {
+        const float m_new = fmaxf(m_use, mt);
+        f = (m_new == m_use) ? 1.0f : ex2_approx((m_use - m_new) * c);
+        m_use = m_new;
+        rescale = true;
+      }
+      const float mb = (m_use == -INFINITY) ? 0.0f : m_use * c;
+      float sum0 = 0.0f, sum1 = 0.0f;
+      uint32_t pk[kBlockN / 2];
+#pragma unroll
+      for (int j = 0; j < kBlockN / 2; ++j) {
+        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * j]), c, -mb));
+        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * j + 1]), c, -mb));
+        sum0 += p0;
+        sum1 += p1;
+        pk[j] = pack2<BF16>(p0, p1);
+      }
+      l_sum = fmaf(l_sum, f, sum0 + sum1);
+      tmem_st32(tmem + C::p_col(s) + lane_off, pk);
+      tmem_st32(tmem + C::p_col(s) + lane_off + 32, pk + 32);
+      if (rescale) {
+        // O_s is stable here: P_s V of the previous tile finished before S_s of this tile
+        // was committed, and P_s V of this tile waits for the arrive below.
+#pragma unroll
+        for (int cc = 0; cc < C::DV / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32_nowait(tmem + C::o_col(s) + lane_off + 32 * cc, o);
+          tmem_wait_ld_32(o);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+          tmem_st32(tmem + C::o_col(s) + lane_off + 32 * cc, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar.p_full(s));
+    }
+
+    // ---------------------------------------------------------------- epilogue
+    if (ok) ok = pwait(bar.o_full, 0, abort_flag, a.err, kErrSoftmax, tmo);
+    ok = __all_sync(0xffffffffu, ok);
+    tc_fence_after();
+    if (!DIFF) {
+      const float inv = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
+      uint16_t* dst = static_cast<uint16_t*>(a.out) +
+                      (static_cast<size_t>(bh) * L + grow) * static_cast<size_t>(C::DV);
+      if (ok) {
+#pragma unroll
+        for (int cc = 0; cc < C::DV / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32_nowait(tmem + C::o_col(s) + lane_off + 32 * cc, o);
+          tmem_wait_ld_32(o);
+          uint32_t pkd[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j)
+            pkd[j] = pack2<BF16>(__uint_as_float(o[2 * j]) * inv, __uint_as_float(o[2 * j + 1]) * inv);
+          if (grow < L) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * cc);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              d4[j] = make_uint4(pkd[4 * j], pkd[4 * j + 1], pkd[4 * j + 2], pkd[4 * j + 3]);
+          }
+        }
+      }
+    } else {
+      lsum[s * kBlockM + r] = l_sum;
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      const float l0 = lsum[r], l1 = lsum[kBlockM + r];
+      const float inv0 = l0 > 0.0f ? 1.0f / l0 : 0.0f;
+      const float inv1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;
+      const float lam = a.lambda[bh % a.H];
+      uint16_t* dst = static_cast<uint16_t*>(a.out) +
+                      (static_cast<size_t>(bh) * L + grow) * static_cast<size_t>(C::DV) + 64 * s;
+      if (ok) {
+        // warpgroup s writes output columns [64 s, 64 s + 64)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const uint32_t col = 64 * s + 32 * cc;
+          uint32_t o0[32], o1[32];
+          tmem_ld32_nowait(tmem + C::o_col(0) + lane_off + col, o0);
+          tmem_ld32_nowait(tmem + C::o_col(1) + lane_off + col, o1);
+          tmem_wait_ld_32(o0);
+          tmem_wait_ld_32(o1);
+          uint32_t pkd[16];
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const float y0 = fmaf(-lam, __uint_as_float(o1[2 * j]) * inv1, __uint_as_float(o0[2 * j]) * inv0);
+            const float y1 =
+                fmaf(-lam, __uint_as_float(o1[2 * j + 1]) * inv1, __uint_as_float(o0[2 * j + 1]) * inv0);
+            pkd[j] = pack2<BF16>(y0, y1);
+          }
+          if (grow < L) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * cc);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              d4[j] = make_uint4(pkd[4 * j], pkd[4 * j + 1], pkd[4 * j + 2], pkd[4 * j + 3]);
+          }
+        }
+      }
+    }
+  }
+
+  // ------------------------------------------------------------------ teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <bool DIFF, bool BF16>
+cudaError_t set_attr() {
+  return cudaFuncSetAttribute(fmha_kernel<DIFF, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Cfg<DIFF>::SMEM_ALLOC);
+}
+
+template <bool DIFF, bool BF16>
+cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                   const FmhaArgs& a, long long num_ctas, cudaStream_t stream) {
+  fmha_kernel<DIFF, BF16><<<static_cast<unsigned>(num_ctas), kFmhaThreads, Cfg<DIFF>::SMEM_ALLOC,
+                            stream>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t fmha_set_attributes() {
+  cudaError_t e;
+  if ((e = set_attr<false, false>()) != cudaSuccess) return e;
+  if ((e = set_attr<false, true>()) != cudaSuccess) return e;
+  if ((e = set_attr<true, false>()) != cudaSuccess) return e;
+  return set_attr<true, true>();
+}
+
+cudaError_t fmha_launch(bool diff, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk,
+                        const CUtensorMap& tv, const FmhaArgs& a, long long num_ctas,
+                        cudaStream_t stream) {
+  if (diff) return bf16 ? launch<true, true>(tq, tk, tv, a, num_ctas, stream)
+                        : launch<true, false>(tq, tk, tv, a, num_ctas, stream);
+  return bf16 ? launch<false, true>(tq, tk, tv, a, num_ctas, stream)
+              : launch<false, false>(tq, tk, tv, a, num_ctas, stream);
+}
+
+}  // namespace sa

@@ -1,0 +1,60 @@
+// sa_kernels.h -- host-side view of the two kernels of the RoPE + attention core:
+// argument structs, tile constants and launchers.  No torch types anywhere.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace sa {
+
+constexpr int kHeadDim = 64;          // d of q and k (the only supported value)
+constexpr int kBlockM = 128;          // query rows per tile = TMEM lanes
+constexpr int kBlockN = 128;          // keys per K/V tile
+constexpr int kMaxDiffHeads = 128;    // lambda is carried by value in the kernel arguments
+constexpr int kFmhaThreads = 320;     // 8 softmax warps + 1 TMA warp + 1 MMA warp
+constexpr int kMaxL = 1 << 24;        // positions and row indices stay exact in FP32 / int32
+
+// Bits of the device error word.
+constexpr int kErrProducer = 1;       // TMA warp gave up on a wait
+constexpr int kErrMma = 2;            // MMA warp gave up on a wait
+constexpr int kErrSoftmax = 4;        // softmax / epilogue warps gave up on a wait
+
+// RoPE pre-pass: rotate q and k (all planes) in FP32 and cast back to the storage dtype.
+struct RopeArgs {
+  const uint16_t* q;
+  const uint16_t* k;
+  uint16_t* q_out;
+  uint16_t* k_out;
+  const int32_t* positions;   // [L] or nullptr for 0..L-1
+  long long planes;           // B * H * nmaps rows-of-L planes in q (and in k)
+  int L;
+  int planes_per_block;
+  float inv_freq[kHeadDim / 2];
+};
+
+// Attention kernel arguments (tensor maps are passed separately as __grid_constant__).
+struct FmhaArgs {
+  void* out;                  // [B, H, L, d_v]
+  int* err;                   // device error word (bits above), atomically OR-ed
+  int L;
+  int H;
+  int n_qblocks;              // CTAs per (b, h)
+  int window;                 // < 0: full attention, else |i - j| <= window (< L - 1)
+  float scale_log2;           // log2(e) / sqrt(d)
+  unsigned long long timeout_ns;
+  float lambda[kMaxDiffHeads];
+};
+
+// Rows of queries one CTA owns: two 128-row tiles (standard) or one tile with two maps.
+constexpr int fmha_rows_per_cta(bool diff) { return diff ? kBlockM : 2 * kBlockM; }
+
+cudaError_t rope_launch(const RopeArgs& a, bool bf16, int num_sms, cudaStream_t stream);
+
+cudaError_t fmha_set_attributes();
+cudaError_t fmha_launch(bool diff, bool bf16, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
+                        const CUtensorMap& tm_v, const FmhaArgs& a, long long num_ctas,
+                        cudaStream_t stream);
+
+}  // namespace sa

@@ -1,0 +1,114 @@
+// sa_rope.cu -- RoPE pre-pass: q' = RoPE(q), k' = RoPE(k) in FP32, cast back to fp16/bf16.
+//
+// HF discussion #3 "fp16mixed attention-core fix", section "The bug": apply_rotary_pos_emb
+// computes in FP32 and ends with t.to(out_dtype), so attention then runs on fp16/bf16 q, k.
+// Rotate-half over the full head dim (d = 64): pair (i, i + 32) at position p turns by
+// theta = p * inv_freq[i], inv_freq[i] = base^(-2i/64) held as FP32.  The angle itself is an
+// FP32 product and sin/cos are the full-precision single-precision functions: the sa3_trt
+// README ("Retired: bf16") shows what a low-precision angle does at long sequence lengths.
+//
+// One block rotates 32 positions of every plane in its slice of planes (a plane is one
+// (batch, head, map) sequence).  sin/cos are computed once per (position, pair) and reused
+// across all planes of the slice and across q and k.  The pass is HBM-bound: it reads q and k
+// once and writes q', k' once, with 16-byte accesses.
+#include "sa_kernels.h"
+#include "sa_ptx.cuh"
+
+namespace sa {
+namespace {
+
+constexpr int kRopeRows = 32;      // positions per block
+constexpr int kRopeThreads = 128;  // 32 positions x 4 groups of 8 rotation pairs
+
+__device__ __forceinline__ uint4 ld_stream(const uint16_t* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void st_v4(uint16_t* p, uint4 v) {
+  asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+
+// Rotate elements [8g, 8g+8) together with their partners [32+8g, 32+8g+8) of one row.
+template <bool BF16>
+__device__ __forceinline__ void rotate_chunk(const uint16_t* __restrict__ src,
+                                             uint16_t* __restrict__ dst, const float (&c)[8],
+                                             const float (&s)[8]) {
+  const uint4 lo = ld_stream(src);
+  const uint4 hi = ld_stream(src + 32);
+  const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w};
+  const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w};
+  uint32_t ol[4], oh[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 a = unpack2<BF16>(lw[j]);  // x_i, x_{i+1}
+    const float2 b = unpack2<BF16>(hw[j]);  // x_{i+32}, x_{i+33}
+    const int i0 = 2 * j, i1 = 2 * j + 1;
+    const float ya0 = fmaf(a.x, c[i0], -(b.x * s[i0]));
+    const float ya1 = fmaf(a.y, c[i1], -(b.y * s[i1]));
+    const float yb0 = fmaf(b.x, c[i0], a.x * s[i0]);
+    const float yb1 = fmaf(b.y, c[i1], a.y * s[i1]);
+    ol[j] = pack2<BF16>(ya0, ya1);
+    oh[j] = pack2<BF16>(yb0, yb1);
+  }
+  st_v4(dst, make_uint4(ol[0], ol[1], ol[2], ol[3]));
+  st_v4(dst + 32, make_uint4(oh[0], oh[1], oh[2], oh[3]));
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constant__ RopeArgs a) {
+  const int r = threadIdx.x >> 2;  // position within the block
+  const int g = threadIdx.x & 3;   // group of 8 pairs: pairs [8g, 8g + 8)
+  const int l = blockIdx.x * kRopeRows + r;
+  if (l >= a.L) return;
+  const int p = a.positions ? a.positions[l] : l;
+  const float pf = static_cast<float>(p);
+  float c[8], s[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const float theta = __fmul_rn(pf, a.inv_freq[8 * g + i]);
+    sincosf(theta, &s[i], &c[i]);
+  }
+  const long long first = static_cast<long long>(blockIdx.y) * a.planes_per_block;
+  long long last = first + a.planes_per_block;
+  if (last > a.planes) last = a.planes;
+  const size_t row_stride = static_cast<size_t>(a.L) * kHeadDim;
+  size_t off = static_cast<size_t>(first) * row_stride + static_cast<size_t>(l) * kHeadDim + 8 * g;
+#pragma unroll 2
+  for (long long pl = first; pl < last; ++pl, off += row_stride) {
+    rotate_chunk<BF16>(a.q + off, a.q_out + off, c, s);
+    rotate_chunk<BF16>(a.k + off, a.k_out + off, c, s);
+  }
+}
+
+}  // namespace
+
+cudaError_t rope_launch(const RopeArgs& a_in, bool bf16, int num_sms, cudaStream_t stream) {
+  RopeArgs a = a_in;
+  const long long bx = (a.L + kRopeRows - 1) / kRopeRows;
+  const long long want = 8LL * (num_sms > 0 ? num_sms : 148);
+  long long by = (want + bx - 1) / bx;
+  if (by > a.planes) by = a.planes;
+  if (by < 1) by = 1;
+  long long ppb = (a.planes + by - 1) / by;
+  by = (a.planes + ppb - 1) / ppb;
+  if (by > 65535) {
+    by = 65535;
+    ppb = (a.planes + by - 1) / by;
+    by = (a.planes + ppb - 1) / ppb;
+  }
+  a.planes_per_block = static_cast<int>(ppb);
+  const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(by));
+  if (bf16)
+    rope_kernel<true><<<grid, kRopeThreads, 0, stream>>>(a);
+  else
+    rope_kernel<false><<<grid, kRopeThreads, 0, stream>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace sa

@@ -1,0 +1,149 @@
+/*
+ * sa_attn.h -- C ABI of the GB300 (sm_103a) RoPE + attention core of the
+ * Stable Audio 3 DiT and SAME autoencoder.
+ *
+ * What one call computes, per (batch b, head h, query row i):
+ *
+ *   RoPE on q and k, rotate-half over the full head dim, in FP32, then cast
+ *   back to the storage dtype (HF discussion #3 "fp16mixed attention-core fix",
+ *   section "The bug": apply_rotary_pos_emb computes in FP32 and ends with
+ *   t.to(out_dtype); section "The fix": Mul(fp32) -> Cast(fp16)x2):
+ *       theta_{p,i} = p * rope_base^(-2i/d),  i < d/2
+ *       x'_i       = x_i cos(theta) - x_{i+d/2} sin(theta)
+ *       x'_{i+d/2} = x_{i+d/2} cos(theta) + x_i sin(theta)
+ *   then fused scaled-dot-product attention, non-causal, scale 1/sqrt(d), the
+ *   softmax accumulated in FP32 (same page, "The bug": TensorRT's FMHA
+ *   accumulates softmax in FP32):
+ *       out_i = sum_j softmax_j(q'_i . k'_j / sqrt(d)) v_j
+ *   Differential attention (lambda != NULL; HF discussion #6 "sm_120 SAME-L",
+ *   section "How the kernels differ": two softmax maps sharing V, the
+ *   subtraction kept in FP32 on FP32 accumulators):
+ *       out_i = o(Q1,K1)_i - lambda_h * o(Q2,K2)_i
+ *   Sliding window (window >= 0; the SAME-L diff_attn_swa window of the same
+ *   page's "Three gotchas" is symmetric): key j is used for query i iff
+ *   |i - j| <= window.  window < 0, or window >= L-1, is full attention.
+ *
+ * Conventions shared by every entry point:
+ *   - Every function returns an sa_status; SA_OK is 0.  On any other status
+ *     sa_last_error() returns a thread-local message that says what was wrong.
+ *   - Device pointers must be CUDA device memory of the handle's device; all
+ *     tensors are dense, C-contiguous, and 16-byte aligned.
+ *   - Nothing is allocated and nothing is copied host<->device inside
+ *     sa_rope_attn: it only encodes kernel arguments and enqueues two kernels
+ *     on `stream`, so it can be captured into a CUDA graph.  When a host-side
+ *     check fails, nothing is enqueued and `out` is not written.
+ */
+#ifndef SA_ATTN_H
+#define SA_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SA_API __attribute__((visibility("default")))
+#else
+#define SA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque handle: per-device state (FP32 RoPE frequency table, kernel
+ * attributes, a 4-byte device error word).  Owned by the caller, freed by
+ * sa_attn_destroy. */
+typedef struct sa_attn_s* sa_attn_t;
+
+/* The same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* sa_stream_t;
+
+typedef enum { SA_FP16 = 0, SA_BF16 = 1 } sa_dtype;
+
+typedef enum {
+    SA_OK = 0,
+    SA_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, bad size, bad value */
+    SA_ERR_UNSUPPORTED = 2,     /* head dim other than 64, too many heads, wrong GPU */
+    SA_ERR_CUDA = 3,            /* a CUDA runtime call or a launch failed */
+    SA_ERR_DEVICE_TIMEOUT = 4,  /* a kernel gave up on a pipeline wait (see sa_attn_check) */
+    SA_ERR_NO_DEVICE = 5,       /* no CUDA device, or the device index is out of range */
+    SA_ERR_WORKSPACE = 6        /* workspace missing or smaller than sa_rope_attn_workspace_size */
+} sa_status;
+
+/* Largest H accepted by the differential path (lambda is passed by value). */
+#define SA_MAX_DIFF_HEADS 128
+
+/*
+ * Create a handle on CUDA device `device`.  rope_base is the RoPE base
+ * (10000 for Stable Audio 3); the FP32 frequency table rope_base^(-2i/64) is
+ * computed here in double and rounded once.  Fails with SA_ERR_NO_DEVICE when
+ * there is no such device and SA_ERR_UNSUPPORTED when it is not an sm_103
+ * (GB300) part.  Restores the caller's current device before returning.
+ */
+SA_API sa_status sa_attn_create(sa_attn_t* handle, int device, float rope_base);
+
+/* Free the handle.  NULL is accepted.  Synchronizes the handle's device. */
+SA_API sa_status sa_attn_destroy(sa_attn_t handle);
+
+/*
+ * Bytes of device workspace sa_rope_attn needs for this shape: the rotated
+ * and cast-back q and k (two buffers of B*H*nmaps*L*d elements of 2 bytes,
+ * each rounded up to 256 bytes).  differential != 0 selects nmaps = 2.
+ * Returns 0 for invalid sizes.
+ */
+SA_API size_t sa_rope_attn_workspace_size(int B, int H, int L, int d, int differential);
+
+/*
+ * Enqueue RoPE + attention on `stream`.
+ *
+ *   q, k      device, dtype.  Standard (lambda == NULL): [B, H, L, d].
+ *             Differential (lambda != NULL): [B, H, 2, L, d]; map 0 is
+ *             (Q1, K1), map 1 is (Q2, K2).
+ *   v         device, dtype.  Standard: [B, H, L, d].  Differential:
+ *             [B, H, L, 2d] (d_v = 128).
+ *   positions device int32 [L] (shared by all batches and heads), or NULL for
+ *             0..L-1.  Each is converted to FP32 before the angle product, which
+ *             is exact for |p| < 2^24.
+ *   out       device, dtype, [B, H, L, d_v].  Must not overlap any input.
+ *   B, H, L   >= 1, L < 2^24, with B*H*L*d_v < 2^40.  d must be 64.
+ *   window    < 0: full attention; >= 0: |i - j| <= window.
+ *   lambda    host float[H] (H <= SA_MAX_DIFF_HEADS) or NULL.  Read during the
+ *             call only (copied into the kernel arguments).
+ *   dtype     SA_FP16 or SA_BF16 for q, k, v and out alike.
+ *   workspace device scratch of at least sa_rope_attn_workspace_size bytes,
+ *             16-byte aligned; contents on entry are ignored.  Calls that use
+ *             the same workspace must be ordered on the GPU (same stream).
+ *   stream    CUDA stream; the call is asynchronous with respect to the host.
+ *
+ * Errors: SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_WORKSPACE from host
+ * checks (nothing enqueued); SA_ERR_CUDA when a launch is rejected.  Device
+ * side pipeline timeouts are reported later by sa_attn_check.
+ */
+SA_API sa_status sa_rope_attn(sa_attn_t handle,
+                       const void* q, const void* k, const void* v,
+                       const int32_t* positions,
+                       void* out,
+                       int B, int H, int L, int d,
+                       int window,
+                       const float* lambda,
+                       sa_dtype dtype,
+                       void* workspace, size_t workspace_bytes,
+                       sa_stream_t stream);
+
+/*
+ * Synchronize the handle's device, then read and clear its device error
+ * word.  SA_OK if no kernel since the last check gave up on a wait;
+ * SA_ERR_DEVICE_TIMEOUT otherwise (its output is then unspecified).
+ */
+SA_API sa_status sa_attn_check(sa_attn_t handle);
+
+/* Thread-local description of the last failure on this thread ("" if none). */
+SA_API const char* sa_last_error(void);
+
+/* Static name of a status code. */
+SA_API const char* sa_status_string(sa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SA_ATTN_H */
