@@ -1,0 +1,420 @@
+"""Benchmark of the RoPE + attention core on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = one pass of the whole hot path over one batch of synthetic input:
+the RoPE stage (q, k rotated in FP32, cast back) and the attention stage
+(QK^T/sqrt(d), FP32 softmax, P.V; differential / windowed per workload).
+Default workload: the DiT standard attention at L=1292 (B=1, H=16, d=64, fp16).
+
+Prints ONE JSON line (rank 0).  ``value`` is attention TFLOP/s of the whole job
+(algorithmic FLOPs, inputs resident in HBM, L2 flushed between steps, CUDA
+events on the launching stream, max over ranks).  ``e2e`` is the same metric
+through the public C-ABI call with pinned host buffers and the host<->device
+copies inside the timed region.  ``roofline`` is for the attention kernel,
+timed live between events recorded around its own launch.  ``cpu_baseline``
+times the FP64 oracle on the host cores on a bounded sample.
+
+``--impl reference`` times the FP64 CPU oracle (the reference arm of this
+repository) on the same workload; each step is a bounded sample of it.
+Multi-GPU (torchrun): every rank runs an independent replica of the workload
+(the path shards by (batch, head) with no exchange), so scaling is weak.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "attention TFLOP/s and % of GB300 FP16/BF16 tensor peak at L=1292/4096"
+DEFAULT_WORKLOAD = "dit_l1292"
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ----------------------------------------------------------------------------- accounting
+
+def allowed_pairs_per_head(w) -> int:
+    """(query, key) pairs the mask admits per head: all L^2, or |i - j| <= window."""
+    L, win = w.L, w.window
+    if win < 0 or win >= L - 1:
+        return L * L
+    i = np.arange(L, dtype=np.int64)
+    return int((np.minimum(L - 1, i + win) - np.maximum(0, i - win) + 1).sum())
+
+
+def flops(w) -> int:
+    """Algorithmic FLOPs: per softmax map and allowed pair, 2*d (QK^T) + 2*d_v (P.V)."""
+    return w.B * w.H * w.nmaps * allowed_pairs_per_head(w) * (2 * w.d + 2 * w.dv)
+
+
+def io_bytes(w) -> int:
+    n = w.B * w.H * w.L
+    return 2 * (n * w.nmaps * w.d * 2 + n * w.dv + n * w.dv)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "tflops": float(p["bf16_tflops"]),
+                "tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except Exception:
+        return {"hbm_gbs": 6800.0, "tflops": 1900.0, "tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def load_traffic(workload: str):
+    """DRAM bytes per attention launch from the committed ncu summary, if one exists."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            t = json.load(f)
+        return t.get(workload)
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", f"sa_clocks_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(world, backend):
+    if world > 1:
+        import torch.distributed as dist
+
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+        return dist
+    return None
+
+
+def reduce_max(dist, value: float, device) -> float:
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+# ----------------------------------------------------------------------------- CPU baseline (oracle)
+
+def row_flops(w, rows: np.ndarray) -> int:
+    i = rows % w.L
+    if w.window < 0 or w.window >= w.L - 1:
+        keys = np.full(i.shape, w.L, dtype=np.int64)
+    else:
+        keys = np.minimum(w.L - 1, i + w.window) - np.maximum(0, i - w.window) + 1
+    return int(keys.sum()) * w.nmaps * (2 * w.d + 2 * w.dv)
+
+
+def oracle_sample(w, x, budget_s: float, rng, threads=None):
+    """Time the FP64 oracle on a random row sample sized to ~budget_s of work.
+    Returns (tflops, seconds, rows_done, threads)."""
+    import oracle
+
+    oracle.build()
+    threads = threads or oracle.default_threads()
+    total = w.B * w.H * w.L
+    probe = rng.choice(total, size=min(total, max(64, total // 200)), replace=False)
+    t0 = time.perf_counter()
+    oracle.rope_attn_workload(x, rows=probe, threads=threads)
+    dt = max(time.perf_counter() - t0, 1e-3)
+    n = int(min(total, max(len(probe), len(probe) * budget_s / dt)))
+    rows = rng.choice(total, size=n, replace=False)
+    t0 = time.perf_counter()
+    oracle.rope_attn_workload(x, rows=rows, threads=threads)
+    dt = time.perf_counter() - t0
+    return row_flops(w, rows) / dt / 1e12, dt, n, threads
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+
+    import diffusion_transformer_attention_rope_gb300 as sa
+
+    world, rank, local = dist_env()
+    dist = dist_init(world, "nccl")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    w = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(w, seed=w.seed + rank)
+    tdt = torch.float16 if w.dtype == "fp16" else torch.bfloat16
+    dtype = sa.SA_FP16 if w.dtype == "fp16" else sa.SA_BF16
+
+    def to_dev(bits):
+        return torch.from_numpy(bits.view(np.int16)).to(device).view(tdt)
+
+    q, k, v = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"])
+    out = torch.empty((w.B, w.H, w.L, w.dv), dtype=tdt, device=device)
+    lam = None if x["lam"] is None else [float(t) for t in x["lam"]]
+    ws_bytes = sa.sa_rope_attn_workspace_size(w.B, w.H, w.L, w.d, w.differential)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+    nqk = q.numel()
+    q_rot = ws[: nqk * 2]
+    k_rot = ws[(nqk * 2 + 255) // 256 * 256:][: nqk * 2]
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
+    h = sa.sa_attn_create(local)
+    stream = torch.cuda.current_stream(device)
+    s = stream.cuda_stream
+
+    def rope():
+        sa.sa_rope_qk(h, q.data_ptr(), k.data_ptr(), None, q_rot.data_ptr(), k_rot.data_ptr(),
+                      w.B, w.H, w.L, w.d, w.nmaps, dtype, s)
+
+    def attn():
+        sa.sa_attn_fwd(h, q_rot.data_ptr(), k_rot.data_ptr(), v.data_ptr(), out.data_ptr(),
+                       w.B, w.H, w.L, w.d, w.window, lam, dtype, s)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        rope()
+        attn()
+    torch.cuda.synchronize(device)
+    sa.sa_attn_check(h)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    barrier(dist)
+    torch.cuda.synchronize(device)
+    clocks.start()
+    for i in range(args.steps):
+        flush.zero_()                      # L2 flush outside the timed events
+        ev[i][0].record(stream)
+        rope()
+        ev[i][1].record(stream)
+        attn()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(device)
+    barrier(dist)
+    clk = clocks.stop()
+    sa.sa_attn_check(h)
+    step_ms = [e[0].elapsed_time(e[2]) for e in ev]
+    attn_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    rope_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    total_ms = reduce_max(dist, float(sum(step_ms)), device)
+
+    # e2e: the public call with pinned host buffers, copies inside the timed region
+    qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
+    oh = torch.empty(out.shape, dtype=tdt).pin_memory()
+    ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
+
+    def e2e_step(e=None):
+        if e is not None:
+            e[0].record(stream)
+        q.copy_(qh, non_blocking=True)
+        k.copy_(kh, non_blocking=True)
+        v.copy_(vh, non_blocking=True)
+        sa.sa_rope_attn(h, q.data_ptr(), k.data_ptr(), v.data_ptr(), None, out.data_ptr(), w.B, w.H,
+                        w.L, w.d, w.window, lam, dtype, ws.data_ptr(), ws_bytes, s)
+        oh.copy_(out, non_blocking=True)
+        if e is not None:
+            e[1].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        e2e_step()
+    barrier(dist)
+    torch.cuda.synchronize(device)
+    for i in range(args.steps):
+        flush.zero_()
+        e2e_step(ev2[i])
+    torch.cuda.synchronize(device)
+    barrier(dist)
+    sa.sa_attn_check(h)
+    e2e_total = reduce_max(dist, float(sum(e[0].elapsed_time(e[1]) for e in ev2)), device)
+    h2d = sum(t.numel() * t.element_size() for t in (q, k, v))
+    d2h = out.numel() * out.element_size()
+    sa.sa_attn_destroy(h)
+
+    if rank != 0:
+        return None
+    fl = flops(w)
+    peaks = load_peaks()
+    value = world * fl * args.steps / (total_ms * 1e-3) / 1e12
+    attn_avg_s = statistics.mean(attn_ms) * 1e-3
+    achieved = fl / attn_avg_s / 1e12
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        tfl, dt, n, th = oracle_sample(w, x, args.cpu_budget, np.random.default_rng(0))
+        cpu = {"value": tfl, "unit": "TFLOP/s", "cores": th, "kind": "oracle",
+               "sample": f"{n} of {w.B * w.H * w.L} query rows (random, all heads), {dt:.1f} s, FP64 C oracle"}
+    return {
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "d_v": w.dv,
+                   "maps": w.nmaps, "window": w.window, "flops_per_step_per_gpu": fl,
+                   "l2": "flushed before every step (256 MiB write, outside the events)",
+                   "parallelism": f"replicas x{world}"},
+        "frac_of_peak": value / world / peaks["tflops"],
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["tflops"], "traffic": load_traffic(w.name),
+                     "kernel": "attention (sa_attn_fwd)", "peak_source": peaks["source"] + " bf16 burst",
+                     "avg_ms": attn_avg_s * 1e3},
+        "stages_ms": {"rope": statistics.mean(rope_ms), "attention": statistics.mean(attn_ms)},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * fl * args.steps / (e2e_total * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk,
+    }
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The FP64 CPU oracle, timed on the host cores; each step is a bounded row sample."""
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return None
+    w = synth.WORKLOADS[args.workload]
+    x = synth.make_inputs(w)
+    rng = np.random.default_rng(1)
+    per_step = max(0.2, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_sample(w, x, per_step / 4, rng)
+    vals, secs, rows = [], [], 0
+    th = None
+    for _ in range(args.steps):
+        tfl, dt, n, th = oracle_sample(w, x, per_step, rng)
+        vals.append(tfl)
+        secs.append(dt)
+        rows += n
+    value = statistics.mean(vals)
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": statistics.mean(secs) * 1e3,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "d_v": w.dv,
+                   "maps": w.nmaps, "window": w.window},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": th, "kind": "oracle",
+                         "sample": f"{rows} query rows over {args.steps} steps (random rows of "
+                                   f"{w.B * w.H * w.L}), FP64 C oracle"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        ap.error("--warmup must be >= 3")
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    world, _, _ = dist_env()
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -19,7 +19,7 @@ from typing import Optional, Sequence
 __all__ = [
     "SA_FP16", "SA_BF16", "SaAttnError", "library_path", "load_library",
     "sa_attn_create", "sa_attn_destroy", "sa_rope_attn_workspace_size", "sa_rope_attn",
-    "sa_attn_check", "sa_last_error", "sa_status_string", "RopeAttention",
+    "sa_rope_qk", "sa_attn_fwd", "sa_attn_check", "sa_last_error", "sa_status_string", "RopeAttention",
 ]
 
 SA_FP16 = 0
@@ -64,6 +64,10 @@ def load_library():
         lib.sa_rope_attn.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i,
                                      ctypes.POINTER(f), i, vp, sz, vp]
         lib.sa_rope_attn.restype = i
+        lib.sa_rope_qk.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+        lib.sa_rope_qk.restype = i
+        lib.sa_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(f), i, vp]
+        lib.sa_attn_fwd.restype = i
         lib.sa_attn_check.argtypes = [vp]
         lib.sa_attn_check.restype = i
         lib.sa_last_error.argtypes = []
@@ -106,14 +110,37 @@ def sa_rope_attn(handle: int, q: int, k: int, v: int, positions: Optional[int], 
                  dtype: int, workspace: Optional[int], workspace_bytes: int,
                  stream: Optional[int]) -> None:
     """Enqueue RoPE + attention.  Pointer arguments are device addresses (ints) or None."""
-    lam_arr = None
-    if lam is not None:
-        vals = [float(x) for x in lam]
-        lam_arr = (ctypes.c_float * len(vals))(*vals)
+    lam_arr = _lam(lam)
     _check(load_library().sa_rope_attn(
         ctypes.c_void_p(handle), ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v),
         ctypes.c_void_p(positions), ctypes.c_void_p(out), int(B), int(H), int(L), int(d),
         int(window), lam_arr, int(dtype), ctypes.c_void_p(workspace), int(workspace_bytes),
+        ctypes.c_void_p(stream)))
+
+
+def _lam(lam):
+    if lam is None:
+        return None
+    vals = [float(x) for x in lam]
+    return (ctypes.c_float * len(vals))(*vals)
+
+
+def sa_rope_qk(handle: int, q: int, k: int, positions: Optional[int], q_rot: int, k_rot: int,
+               B: int, H: int, L: int, d: int, nmaps: int, dtype: int, stream: Optional[int]) -> None:
+    """Enqueue the RoPE stage alone (q_rot/k_rot get the rotated, cast-back q/k)."""
+    _check(load_library().sa_rope_qk(
+        ctypes.c_void_p(handle), ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(positions),
+        ctypes.c_void_p(q_rot), ctypes.c_void_p(k_rot), int(B), int(H), int(L), int(d), int(nmaps),
+        int(dtype), ctypes.c_void_p(stream)))
+
+
+def sa_attn_fwd(handle: int, q_rot: int, k_rot: int, v: int, out: int, B: int, H: int, L: int,
+                d: int, window: int, lam: Optional[Sequence[float]], dtype: int,
+                stream: Optional[int]) -> None:
+    """Enqueue the attention stage alone on already-rotated q/k."""
+    _check(load_library().sa_attn_fwd(
+        ctypes.c_void_p(handle), ctypes.c_void_p(q_rot), ctypes.c_void_p(k_rot), ctypes.c_void_p(v),
+        ctypes.c_void_p(out), int(B), int(H), int(L), int(d), int(window), _lam(lam), int(dtype),
         ctypes.c_void_p(stream)))
 
 

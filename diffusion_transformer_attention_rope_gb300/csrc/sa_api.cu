@@ -82,6 +82,94 @@ bool qk_elems(int B, int H, int L, int nmaps, size_t* out) {
   return true;
 }
 
+
+// Shape / dtype checks shared by the entry points.
+sa_status check_shape(const char* fn, int B, int H, int L, int d, sa_dtype dtype, bool diff) {
+  if (B <= 0 || H <= 0 || L <= 0)
+    return fail(SA_ERR_INVALID_ARG, "%s: B, H, L must be >= 1 (got %d, %d, %d)", fn, B, H, L);
+  if (L >= sa::kMaxL)
+    return fail(SA_ERR_UNSUPPORTED, "%s: L = %d exceeds the supported maximum %d", fn, L, sa::kMaxL - 1);
+  if (d != sa::kHeadDim)
+    return fail(SA_ERR_UNSUPPORTED, "%s: head dim d = %d; only d = 64 is supported", fn, d);
+  if (dtype != SA_FP16 && dtype != SA_BF16)
+    return fail(SA_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, static_cast<int>(dtype));
+  if (diff && H > sa::kMaxDiffHeads)
+    return fail(SA_ERR_UNSUPPORTED, "%s: differential attention supports H <= %d (got %d)", fn,
+                sa::kMaxDiffHeads, H);
+  size_t n = 0;
+  const int dv = diff ? 2 * d : d;
+  if (!qk_elems(B, H, L, diff ? 2 : 1, &n) ||
+      static_cast<unsigned long long>(B) * H * L * dv >= (1ull << 40))
+    return fail(SA_ERR_INVALID_ARG, "%s: tensor sizes overflow", fn);
+  const int rows = sa::fmha_rows_per_cta(diff);
+  if (static_cast<long long>(B) * H * ((L + rows - 1) / rows) >= (1ll << 31))
+    return fail(SA_ERR_UNSUPPORTED, "%s: too many query tiles for one launch", fn);
+  return SA_OK;
+}
+
+sa_status check_lambda(const char* fn, const float* lambda, int H) {
+  if (!lambda) return SA_OK;
+  for (int i = 0; i < H; ++i)
+    if (!std::isfinite(lambda[i]))
+      return fail(SA_ERR_INVALID_ARG, "%s: lambda[%d] is not finite", fn, i);
+  return SA_OK;
+}
+
+sa_status launch_rope(const sa_attn_s* h, const void* q, const void* k, const int32_t* positions,
+                      void* q_rot, void* k_rot, int B, int H, int L, int nmaps, sa_dtype dtype,
+                      sa_stream_t stream) {
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return fail(SA_ERR_CUDA, "cannot select device %d", h->device);
+  sa::RopeArgs ra;
+  ra.q = static_cast<const uint16_t*>(q);
+  ra.k = static_cast<const uint16_t*>(k);
+  ra.q_out = static_cast<uint16_t*>(q_rot);
+  ra.k_out = static_cast<uint16_t*>(k_rot);
+  ra.positions = positions;
+  ra.planes = static_cast<long long>(B) * H * nmaps;
+  ra.L = L;
+  ra.planes_per_block = 1;
+  std::memcpy(ra.inv_freq, h->inv_freq, sizeof(ra.inv_freq));
+  cudaError_t e = sa::rope_launch(ra, dtype == SA_BF16, h->num_sms, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(SA_ERR_CUDA, "RoPE launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+sa_status launch_attn(const sa_attn_s* h, const void* q_rot, const void* k_rot, const void* v,
+                      void* out, int B, int H, int L, int window, const float* lambda,
+                      sa_dtype dtype, sa_stream_t stream) {
+  const bool diff = lambda != nullptr;
+  const bool bf16 = dtype == SA_BF16;
+  const int d = sa::kHeadDim;
+  const int dv = diff ? 2 * d : d;
+  const unsigned long long planes_qk = static_cast<unsigned long long>(B) * H * (diff ? 2 : 1);
+  const unsigned long long planes_v = static_cast<unsigned long long>(B) * H;
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (!encode_map(h, &tm_q, q_rot, bf16, d, L, planes_qk) ||
+      !encode_map(h, &tm_k, k_rot, bf16, d, L, planes_qk) ||
+      !encode_map(h, &tm_v, v, bf16, dv, L, planes_v))
+    return fail(SA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor map");
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return fail(SA_ERR_CUDA, "cannot select device %d", h->device);
+  sa::FmhaArgs fa;
+  std::memset(&fa, 0, sizeof(fa));
+  fa.out = out;
+  fa.err = h->d_err;
+  fa.L = L;
+  fa.H = H;
+  const int rows = sa::fmha_rows_per_cta(diff);
+  fa.n_qblocks = (L + rows - 1) / rows;
+  fa.window = (window < 0 || window >= L - 1) ? -1 : window;
+  fa.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  fa.timeout_ns = h->timeout_ns;
+  if (diff)
+    for (int i = 0; i < H; ++i) fa.lambda[i] = lambda[i];
+  const long long ctas = static_cast<long long>(B) * H * fa.n_qblocks;
+  cudaError_t e = sa::fmha_launch(diff, bf16, tm_q, tm_k, tm_v, fa, ctas, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(SA_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 }  // namespace
 
 extern "C" {
@@ -173,96 +261,62 @@ size_t sa_rope_attn_workspace_size(int B, int H, int L, int d, int differential)
   return 2 * align256(n * 2);
 }
 
+sa_status sa_rope_qk(sa_attn_t h, const void* q, const void* k, const int32_t* positions,
+                     void* q_rot, void* k_rot, int B, int H, int L, int d, int nmaps, sa_dtype dtype,
+                     sa_stream_t stream) {
+  const char* fn = "sa_rope_qk";
+  if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
+  if (!q || !k || !q_rot || !k_rot)
+    return fail(SA_ERR_INVALID_ARG, "%s: q, k, q_rot and k_rot must be non-NULL", fn);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(q_rot) || !aligned16(k_rot))
+    return fail(SA_ERR_INVALID_ARG, "%s: q, k, q_rot and k_rot must be 16-byte aligned", fn);
+  if (nmaps != 1 && nmaps != 2) return fail(SA_ERR_INVALID_ARG, "%s: nmaps must be 1 or 2", fn);
+  sa_status st = check_shape(fn, B, H, L, d, dtype, nmaps == 2);
+  if (st != SA_OK) return st;
+  return launch_rope(h, q, k, positions, q_rot, k_rot, B, H, L, nmaps, dtype, stream);
+}
+
+sa_status sa_attn_fwd(sa_attn_t h, const void* q_rot, const void* k_rot, const void* v, void* out,
+                      int B, int H, int L, int d, int window, const float* lambda, sa_dtype dtype,
+                      sa_stream_t stream) {
+  const char* fn = "sa_attn_fwd";
+  if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
+  if (!q_rot || !k_rot || !v || !out)
+    return fail(SA_ERR_INVALID_ARG, "%s: q_rot, k_rot, v and out must be non-NULL", fn);
+  if (!aligned16(q_rot) || !aligned16(k_rot) || !aligned16(v) || !aligned16(out))
+    return fail(SA_ERR_INVALID_ARG, "%s: q_rot, k_rot, v and out must be 16-byte aligned", fn);
+  sa_status st = check_shape(fn, B, H, L, d, dtype, lambda != nullptr);
+  if (st != SA_OK) return st;
+  if ((st = check_lambda(fn, lambda, H)) != SA_OK) return st;
+  return launch_attn(h, q_rot, k_rot, v, out, B, H, L, window, lambda, dtype, stream);
+}
+
 sa_status sa_rope_attn(sa_attn_t h, const void* q, const void* k, const void* v,
                        const int32_t* positions, void* out, int B, int H, int L, int d, int window,
                        const float* lambda, sa_dtype dtype, void* workspace,
                        size_t workspace_bytes, sa_stream_t stream) {
-  if (!h) return fail(SA_ERR_INVALID_ARG, "sa_rope_attn: handle is NULL");
+  const char* fn = "sa_rope_attn";
+  if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
   if (!q || !k || !v || !out)
-    return fail(SA_ERR_INVALID_ARG, "sa_rope_attn: q, k, v and out must be non-NULL");
+    return fail(SA_ERR_INVALID_ARG, "%s: q, k, v and out must be non-NULL", fn);
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
       (workspace && !aligned16(workspace)))
-    return fail(SA_ERR_INVALID_ARG, "sa_rope_attn: q, k, v, out and workspace must be 16-byte aligned");
-  if (B <= 0 || H <= 0 || L <= 0)
-    return fail(SA_ERR_INVALID_ARG, "sa_rope_attn: B, H, L must be >= 1 (got %d, %d, %d)", B, H, L);
-  if (L >= sa::kMaxL)
-    return fail(SA_ERR_UNSUPPORTED, "sa_rope_attn: L = %d exceeds the supported maximum %d", L,
-                sa::kMaxL - 1);
-  if (d != sa::kHeadDim)
-    return fail(SA_ERR_UNSUPPORTED, "sa_rope_attn: head dim d = %d; only d = 64 is supported", d);
-  if (dtype != SA_FP16 && dtype != SA_BF16)
-    return fail(SA_ERR_INVALID_ARG, "sa_rope_attn: unknown dtype %d", static_cast<int>(dtype));
+    return fail(SA_ERR_INVALID_ARG, "%s: q, k, v, out and workspace must be 16-byte aligned", fn);
   const bool diff = lambda != nullptr;
-  const int nmaps = diff ? 2 : 1;
-  const int dv = diff ? 2 * d : d;
-  if (diff && H > sa::kMaxDiffHeads)
-    return fail(SA_ERR_UNSUPPORTED, "sa_rope_attn: differential attention supports H <= %d (got %d)",
-                sa::kMaxDiffHeads, H);
-  size_t nqk = 0;
-  if (!qk_elems(B, H, L, nmaps, &nqk) ||
-      static_cast<unsigned long long>(B) * H * L * dv >= (1ull << 40))
-    return fail(SA_ERR_INVALID_ARG, "sa_rope_attn: tensor sizes overflow");
-  if (static_cast<long long>(B) * H * ((L + sa::fmha_rows_per_cta(diff) - 1) /
-                                       sa::fmha_rows_per_cta(diff)) >= (1ll << 31))
-    return fail(SA_ERR_UNSUPPORTED, "sa_rope_attn: too many query tiles for one launch");
-  if (diff) {
-    for (int i = 0; i < H; ++i)
-      if (!std::isfinite(lambda[i]))
-        return fail(SA_ERR_INVALID_ARG, "sa_rope_attn: lambda[%d] is not finite", i);
-  }
+  sa_status st = check_shape(fn, B, H, L, d, dtype, diff);
+  if (st != SA_OK) return st;
+  if ((st = check_lambda(fn, lambda, H)) != SA_OK) return st;
   const size_t need = sa_rope_attn_workspace_size(B, H, L, d, diff);
   if (!workspace || workspace_bytes < need)
-    return fail(SA_ERR_WORKSPACE, "sa_rope_attn: workspace of %zu bytes needed, %zu given%s", need,
+    return fail(SA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given%s", fn, need,
                 workspace_bytes, workspace ? "" : " (NULL)");
-
-  const bool bf16 = dtype == SA_BF16;
+  const size_t nqk = static_cast<size_t>(B) * H * (diff ? 2 : 1) * L * sa::kHeadDim;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  uint16_t* q_rot = reinterpret_cast<uint16_t*>(ws);
-  uint16_t* k_rot = reinterpret_cast<uint16_t*>(ws + align256(nqk * 2));
-
-  const unsigned long long planes_qk = static_cast<unsigned long long>(B) * H * nmaps;
-  const unsigned long long planes_v = static_cast<unsigned long long>(B) * H;
-  CUtensorMap tm_q, tm_k, tm_v;
-  if (!encode_map(h, &tm_q, q_rot, bf16, d, L, planes_qk) ||
-      !encode_map(h, &tm_k, k_rot, bf16, d, L, planes_qk) ||
-      !encode_map(h, &tm_v, v, bf16, dv, L, planes_v))
-    return fail(SA_ERR_CUDA, "sa_rope_attn: cuTensorMapEncodeTiled rejected a tensor map");
-
-  DeviceGuard guard(h->device);
-  if (!guard.ok) return fail(SA_ERR_CUDA, "sa_rope_attn: cannot select device %d", h->device);
-  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-
-  sa::RopeArgs ra;
-  ra.q = static_cast<const uint16_t*>(q);
-  ra.k = static_cast<const uint16_t*>(k);
-  ra.q_out = q_rot;
-  ra.k_out = k_rot;
-  ra.positions = positions;
-  ra.planes = static_cast<long long>(planes_qk);
-  ra.L = L;
-  ra.planes_per_block = 1;
-  std::memcpy(ra.inv_freq, h->inv_freq, sizeof(ra.inv_freq));
-  cudaError_t e = sa::rope_launch(ra, bf16, h->num_sms, st);
-  if (e != cudaSuccess) return fail(SA_ERR_CUDA, "sa_rope_attn: RoPE launch: %s", cudaGetErrorString(e));
-
-  sa::FmhaArgs fa;
-  std::memset(&fa, 0, sizeof(fa));
-  fa.out = out;
-  fa.err = h->d_err;
-  fa.L = L;
-  fa.H = H;
-  const int rows = sa::fmha_rows_per_cta(diff);
-  fa.n_qblocks = (L + rows - 1) / rows;
-  fa.window = (window < 0 || window >= L - 1) ? -1 : window;
-  fa.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
-  fa.timeout_ns = h->timeout_ns;
-  if (diff)
-    for (int i = 0; i < H; ++i) fa.lambda[i] = lambda[i];
-  const long long ctas = static_cast<long long>(B) * H * fa.n_qblocks;
-  e = sa::fmha_launch(diff, bf16, tm_q, tm_k, tm_v, fa, ctas, st);
-  if (e != cudaSuccess)
-    return fail(SA_ERR_CUDA, "sa_rope_attn: attention launch: %s", cudaGetErrorString(e));
-  return ok();
+  void* q_rot = ws;
+  void* k_rot = ws + align256(nqk * 2);
+  st = launch_rope(h, q, k, positions, q_rot, k_rot, B, H, L, diff ? 2 : 1, dtype, stream);
+  if (st != SA_OK) return st;
+  return launch_attn(h, q_rot, k_rot, v, out, B, H, L, window, lambda, dtype, stream);
 }
 
 sa_status sa_attn_check(sa_attn_t h) {

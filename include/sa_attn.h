@@ -130,6 +130,35 @@ SA_API sa_status sa_rope_attn(sa_attn_t handle,
                        sa_stream_t stream);
 
 /*
+ * The two stages sa_rope_attn is made of, for callers that want them apart
+ * (for instance to time the attention kernel alone, or to feed q/k that are
+ * already rotated).  Same conventions, layouts and errors as sa_rope_attn.
+ *
+ * sa_rope_qk: q_rot = cast(RoPE_fp32(q)), k_rot = cast(RoPE_fp32(k)) for all
+ *   B*H*nmaps planes of L rows (nmaps = 1 standard, 2 differential); q_rot and
+ *   k_rot have the layout of q and k and must not overlap them.
+ */
+SA_API sa_status sa_rope_qk(sa_attn_t handle,
+                            const void* q, const void* k,
+                            const int32_t* positions,
+                            void* q_rot, void* k_rot,
+                            int B, int H, int L, int d, int nmaps,
+                            sa_dtype dtype, sa_stream_t stream);
+
+/*
+ * sa_attn_fwd: scaled-dot-product attention (softmax in FP32; differential
+ *   when lambda != NULL; sliding window when window >= 0) on q_rot, k_rot
+ *   taken as already rotated.  No workspace.
+ */
+SA_API sa_status sa_attn_fwd(sa_attn_t handle,
+                             const void* q_rot, const void* k_rot, const void* v,
+                             void* out,
+                             int B, int H, int L, int d,
+                             int window,
+                             const float* lambda,
+                             sa_dtype dtype, sa_stream_t stream);
+
+/*
  * Synchronize the handle's device, then read and clear its device error
  * word.  SA_OK if no kernel since the last check gave up on a wait;
  * SA_ERR_DEVICE_TIMEOUT otherwise (its output is then unspecified).

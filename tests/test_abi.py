@@ -1,0 +1,99 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads and
+exports exactly what include/sa_attn.h declares; host validation rejects bad
+arguments before any device work."""
+
+import os
+import re
+import subprocess
+
+import pytest
+
+import diffusion_transformer_attention_rope_gb300 as sa
+from diffusion_transformer_attention_rope_gb300 import build as sa_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sa_attn.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sa_build.build()
+    return sa.load_library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^SA_API\s+[\w\s\*]+?\b(sa_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = _declared_functions()
+    for required in ["sa_attn_create", "sa_rope_attn", "sa_attn_destroy"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    out = subprocess.run(["nm", "-D", "--defined-only", sa.library_path()], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r"\sT\s(sa_\w+)$", out, flags=re.M))
+    declared = set(_declared_functions())
+    assert declared == exported, (declared ^ exported)
+    for name in declared:
+        assert hasattr(lib, name)
+
+
+def test_library_is_built_for_sm103a_only(lib):
+    # the fatbin holds sm_103a SASS; cuobjdump --list-elf prints only the ELF names
+    r = subprocess.run(["cuobjdump", "--list-elf", sa.library_path()], capture_output=True, text=True)
+    if r.returncode != 0:
+        pytest.skip("cuobjdump unavailable")
+    arches = set(re.findall(r"sm_(\d+a?)", r.stdout))
+    assert arches == {"103a"}, arches
+
+
+def test_workspace_size():
+    # two 256-byte-aligned buffers of B*H*nmaps*L*64 two-byte elements
+    n = 1 * 16 * 1292 * 64 * 2
+    assert sa.sa_rope_attn_workspace_size(1, 16, 1292, 64, False) == 2 * ((n + 255) // 256 * 256)
+    n = 1 * 16 * 2 * 4096 * 64 * 2
+    assert sa.sa_rope_attn_workspace_size(1, 16, 4096, 64, True) == 2 * n
+    assert sa.sa_rope_attn_workspace_size(1, 16, 4096, 128, True) == 0
+    assert sa.sa_rope_attn_workspace_size(0, 16, 4096, 64, False) == 0
+    assert sa.sa_rope_attn_workspace_size(1, 1, -5, 64, False) == 0
+
+
+def test_status_strings():
+    assert sa.sa_status_string(0) == "SA_OK"
+    assert sa.sa_status_string(6) == "SA_ERR_WORKSPACE"
+    assert sa.sa_status_string(99) == "SA_ERR_UNKNOWN"
+
+
+def test_null_handle_is_rejected_on_the_host():
+    with pytest.raises(sa.SaAttnError) as e:
+        sa.sa_rope_attn(0, 256, 256, 256, None, 256, 1, 1, 64, 64, -1, None, sa.SA_FP16, 256, 1 << 20, None)
+    assert e.value.status == 1
+    assert "handle" in sa.sa_last_error()
+
+
+def test_create_without_a_gpu_reports_no_device():
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(sa.SaAttnError) as e:
+        sa.sa_attn_create(0)
+    assert e.value.status == 5
+
+
+def test_create_rejects_bad_rope_base():
+    with pytest.raises(sa.SaAttnError) as e:
+        sa.sa_attn_create(0, rope_base=0.5)
+    assert e.value.status == 1
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    # the product path has no fallback: a missing .so is an error, not a slow path
+    monkeypatch.setattr(sa, "_lib", None)
+    monkeypatch.setattr(sa, "library_path", lambda: str(tmp_path / "libsa_attn.so"))
+    with pytest.raises(sa.SaAttnError):
+        sa.load_library()

@@ -1,0 +1,272 @@
+"""GPU parity: the CUDA path through the C ABI against the FP64 oracle.
+
+Tolerance (stated by the task's target for fp16/bf16 outputs): max-abs error
+<= 4e-3 and per-row cosine >= 0.9999 against the unrounded FP64 oracle.
+Sizes: full outputs at sizes the oracle finishes in seconds (several tiles and
+ragged tails), sampled rows plus size-independent properties at the five
+workload sizes, and the edge cases of the method (L = 1, windows 0 and >= L-1,
+window edges on and next to tile boundaries, explicit positions).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import diffusion_transformer_attention_rope_gb300 as sa
+import oracle
+import synth
+
+pytestmark = pytest.mark.gpu
+
+TOL_ABS = 4e-3
+TOL_COS = 0.9999
+TDT = {"fp16": torch.float16, "bf16": torch.bfloat16}
+
+
+@pytest.fixture(scope="module")
+def attn():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    a = sa.RopeAttention(0)
+    yield a
+    a.check()
+    a.close()
+
+
+def dev(bits, dtype):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(TDT[dtype])
+
+
+def run_gpu(attn, x, positions=None, window=None):
+    w = x["workload"]
+    q, k, v = dev(x["q"], w.dtype), dev(x["k"], w.dtype), dev(x["v"], w.dtype)
+    pos = None if positions is None else torch.from_numpy(positions.astype(np.int32)).cuda()
+    lam = None if x["lam"] is None else [float(t) for t in x["lam"]]
+    out = attn(q, k, v, positions=pos, window=w.window if window is None else window, lam=lam)
+    torch.cuda.synchronize()
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+def compare(got, ref, tag=""):
+    g = np.asarray(got, dtype=np.float64).reshape(-1, ref.shape[-1])
+    r = np.asarray(ref, dtype=np.float64).reshape(-1, ref.shape[-1])
+    assert np.all(np.isfinite(g)), f"{tag}: non-finite output"
+    err = np.abs(g - r).max()
+    cos = (g * r).sum(1) / np.maximum(np.linalg.norm(g, axis=1) * np.linalg.norm(r, axis=1), 1e-300)
+    bad = int(np.argmin(cos))
+    assert err <= TOL_ABS, f"{tag}: max-abs {err:.3e} > {TOL_ABS}"
+    assert cos.min() >= TOL_COS, f"{tag}: row {bad} cosine {cos.min():.6f} < {TOL_COS}"
+    return err, cos.min()
+
+
+def small(name, **kw):
+    return synth.Workload(name, **kw)
+
+
+# ----------------------------------------------------------------------------- RoPE pre-pass
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_rope_prepass_matches_oracle_rounding(attn, dtype):
+    # The rotated, cast-back q'/k' in the workspace equal the oracle's FP64 rotation
+    # rounded to the dtype, up to one unit in the last place where FP32 and FP64
+    # rotations straddle a rounding boundary.
+    w = small("rope", B=2, H=3, L=300, dtype=dtype, seed=11)
+    x = synth.make_inputs(w)
+    pos = (np.arange(w.L) * 7 + 1000).astype(np.int32)
+    run_gpu(attn, x, positions=pos)
+    n = x["q"].size
+    ws = attn._ws[: 2 * ((n * 2 + 255) // 256 * 256)].cpu().numpy()
+    q_rot = ws[: n * 2].view(np.uint16)
+    k_rot = ws[(n * 2 + 255) // 256 * 256:][: n * 2].view(np.uint16)
+    for bits, rot in ((x["q"], q_rot), (x["k"], k_rot)):
+        ref = oracle.round_to(oracle.rope(synth.decode(bits, dtype).astype(np.float64).reshape(-1, 64),
+                                          np.tile(pos, w.B * w.H)), dtype).reshape(-1)
+        got = synth.decode(rot, dtype).astype(np.float64)
+        diff = got != ref
+        assert diff.mean() < 0.01, f"{diff.mean():.4f} of elements differ"
+        ulp = np.abs(ref) * (2.0 ** -10 if dtype == "fp16" else 2.0 ** -7) + 2.0 ** -24
+        assert np.all(np.abs(got - ref)[diff] <= ulp[diff])
+
+
+# ----------------------------------------------------------------------------- full outputs
+
+def test_tiny_workload(attn):
+    x = synth.make_inputs(synth.WORKLOADS["tiny"])
+    compare(run_gpu(attn, x), oracle.rope_attn_workload(x), "tiny")
+
+
+@pytest.mark.parametrize("L", [1, 2, 17, 63, 64, 65, 127, 128, 129, 255, 256, 257, 300, 513])
+def test_length_sweep_standard_fp16(attn, L):
+    w = small("sweep", B=2, H=3, L=L, seed=100 + L)
+    x = synth.make_inputs(w)
+    compare(run_gpu(attn, x), oracle.rope_attn_workload(x), f"L={L}")
+
+
+@pytest.mark.parametrize("L", [1, 129, 384, 391])
+def test_length_sweep_standard_bf16(attn, L):
+    w = small("sweep", B=1, H=2, L=L, dtype="bf16", seed=200 + L)
+    x = synth.make_inputs(w)
+    compare(run_gpu(attn, x), oracle.rope_attn_workload(x), f"bf16 L={L}")
+
+
+@pytest.mark.parametrize("L,dtype", [(1, "bf16"), (64, "bf16"), (65, "bf16"), (128, "bf16"),
+                                     (129, "bf16"), (300, "bf16"), (257, "fp16")])
+def test_length_sweep_differential(attn, L, dtype):
+    w = small("dsweep", B=2, H=3, L=L, nmaps=2, dv=128, dtype=dtype, seed=300 + L,
+              lam=("uniform", 0.2, 0.8))
+    x = synth.make_inputs(w)
+    compare(run_gpu(attn, x), oracle.rope_attn_workload(x), f"diff L={L}")
+
+
+@pytest.mark.parametrize("win", [0, 1, 17, 127, 128, 129, 256, 599, 600, 10000])
+def test_window_sweep_standard(attn, win):
+    w = small("win", B=1, H=2, L=600, window=win, seed=400 + win % 997)
+    x = synth.make_inputs(w)
+    compare(run_gpu(attn, x), oracle.rope_attn_workload(x), f"window={win}")
+
+
+@pytest.mark.parametrize("win", [0, 17, 127, 128, 129, 256, 699])
+def test_window_sweep_differential(attn, win):
+    w = small("dwin", B=1, H=2, L=700, nmaps=2, dv=128, dtype="bf16", window=win, seed=500 + win,
+              lam=("uniform", 0.2, 0.8))
+    x = synth.make_inputs(w)
+    compare(run_gpu(attn, x), oracle.rope_attn_workload(x), f"diff window={win}")
+
+
+@pytest.mark.parametrize("kind", ["offset", "shuffled", "zeros"])
+def test_explicit_positions(attn, kind):
+    w = small("pos", B=1, H=2, L=333, seed=600)
+    x = synth.make_inputs(w)
+    rng = np.random.default_rng(601)
+    pos = {"offset": np.arange(w.L) + 7000,
+           "shuffled": rng.permutation(w.L) * 3,
+           "zeros": np.zeros(w.L)}[kind].astype(np.int32)
+    x["positions"] = pos
+    compare(run_gpu(attn, x, positions=pos), oracle.rope_attn_workload(x), f"positions {kind}")
+
+
+# ----------------------------------------------------------------------------- full-size workloads
+
+def sample_rows(w, rng, per_head_random=6):
+    L = w.L
+    fixed = [0, 1, 127, 128, 129, 255, 256, 257, L // 2, L - 257, L - 129, L - 128, L - 2, L - 1]
+    rows = []
+    for bh in range(w.B * w.H):
+        picks = set(i for i in fixed if 0 <= i < L) | set(rng.integers(0, L, per_head_random).tolist())
+        rows += [bh * L + i for i in sorted(picks)]
+    return np.array(rows, dtype=np.int64)
+
+
+@pytest.mark.parametrize("name", ["dit_l1292", "dit_l4096_outliers", "diff_l4096", "swa_diff_l8192"])
+def test_full_size_workload(attn, name):
+    w = synth.WORKLOADS[name]
+    x = synth.make_inputs(w)
+    got = run_gpu(attn, x)
+    rows = sample_rows(w, np.random.default_rng(700))
+    ref = oracle.rope_attn_workload(x, rows=rows)
+    compare(got.reshape(-1, w.dv)[rows], ref, name)
+    # property at every row: out is a convex combination of v rows (standard), or a
+    # difference of two such (differential), so |out| <= (1 + lambda) max |v| per column.
+    g = got.reshape(w.B, w.H, w.L, w.dv)
+    vmax = np.abs(synth.decode(x["v"], w.dtype)).max(axis=2, keepdims=True)
+    lam = np.zeros(w.H) if x["lam"] is None else x["lam"].astype(np.float64)
+    bound = (1 + lam)[None, :, None, None] * vmax * (1 + 1e-2) + 1e-3
+    assert np.all(np.abs(g) <= bound)
+
+
+# ----------------------------------------------------------------------------- behaviour
+
+def test_bit_reproducible(attn):
+    # the pages' fp16 engine is "bit-reproducible run to run"
+    x = synth.make_inputs(synth.WORKLOADS["diff_l4096"])
+    a = run_gpu(attn, x)
+    b = run_gpu(attn, x)
+    assert np.array_equal(a, b)
+
+
+def test_different_seeds_give_different_outputs(attn):
+    # guards against a silently skipped stage returning the same bytes for every input
+    w = synth.WORKLOADS["dit_l1292"]
+    a = run_gpu(attn, synth.make_inputs(w, seed=1))
+    b = run_gpu(attn, synth.make_inputs(w, seed=2))
+    assert not np.array_equal(a, b)
+    assert np.abs(a).max() > 0 and np.abs(b).max() > 0
+
+
+def test_cuda_graph_capture_and_replay(attn):
+    w = small("graph", B=1, H=4, L=777, seed=800)
+    x1, x2 = synth.make_inputs(w, seed=801), synth.make_inputs(w, seed=802)
+    q, k, v = dev(x1["q"], "fp16"), dev(x1["k"], "fp16"), dev(x1["v"], "fp16")
+    out = torch.empty((1, 4, 777, 64), dtype=torch.float16, device="cuda")
+    attn(q, k, v, out=out)  # warm-up sizes the workspace outside the capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            attn(q, k, v, out=out)
+    for x in (x2, x1):
+        q.copy_(dev(x["q"], "fp16"))
+        k.copy_(dev(x["k"], "fp16"))
+        v.copy_(dev(x["v"], "fp16"))
+        g.replay()
+        torch.cuda.synchronize()
+        compare(out.float().cpu().numpy(), oracle.rope_attn_workload(x), "graph replay")
+
+
+def test_side_stream(attn):
+    w = small("stream", B=1, H=2, L=500, seed=900)
+    x = synth.make_inputs(w)
+    s = torch.cuda.Stream()
+    q, k, v = dev(x["q"], "fp16"), dev(x["k"], "fp16"), dev(x["v"], "fp16")
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        out = attn(q, k, v)
+    s.synchronize()
+    compare(out.float().cpu().numpy(), oracle.rope_attn_workload(x), "side stream")
+
+
+def test_output_guard_bands_untouched(attn):
+    w = small("guard", B=1, H=3, L=130, seed=1000)
+    x = synth.make_inputs(w)
+    n = w.B * w.H * w.L * w.dv
+    pad = 4096
+    buf = torch.full((n + 2 * pad,), 12345, dtype=torch.int16, device="cuda")
+    out = buf[pad:pad + n].view(torch.float16).view(w.B, w.H, w.L, w.dv)
+    attn(dev(x["q"], "fp16"), dev(x["k"], "fp16"), dev(x["v"], "fp16"), out=out)
+    torch.cuda.synchronize()
+    b = buf.cpu().numpy()
+    assert np.all(b[:pad] == 12345) and np.all(b[pad + n:] == 12345)
+    compare(out.float().cpu().numpy(), oracle.rope_attn_workload(x), "guarded")
+
+
+def test_host_checks_reject_bad_arguments(attn):
+    w = small("bad", B=1, H=2, L=64, seed=1100)
+    x = synth.make_inputs(w)
+    q, k, v = dev(x["q"], "fp16"), dev(x["k"], "fp16"), dev(x["v"], "fp16")
+    out = torch.full((1, 2, 64, 64), 7.0, dtype=torch.float16, device="cuda")
+    ws = attn.workspace(1, 2, 64, False)
+    h = attn.handle
+    s = torch.cuda.current_stream().cuda_stream
+
+    def call(**kw):
+        args = dict(q=q.data_ptr(), k=k.data_ptr(), v=v.data_ptr(), positions=None, out=out.data_ptr(),
+                    B=1, H=2, L=64, d=64, window=-1, lam=None, dtype=sa.SA_FP16,
+                    workspace=ws.data_ptr(), workspace_bytes=ws.numel(), stream=s)
+        args.update(kw)
+        with pytest.raises(sa.SaAttnError) as e:
+            sa.sa_rope_attn(h, **args)
+        return e.value.status
+
+    assert call(d=128) == 2
+    assert call(q=q.data_ptr() + 2) == 1
+    assert call(out=None) == 1
+    assert call(L=0) == 1
+    assert call(dtype=7) == 1
+    assert call(workspace_bytes=100) == 6
+    assert call(workspace=None) == 6
+    assert call(H=200, lam=[0.5] * 200) == 2
+    assert call(lam=[float("nan"), 0.5]) == 1
+    torch.cuda.synchronize()
+    assert torch.all(out == 7.0)
+    attn.check()
