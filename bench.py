@@ -160,7 +160,8 @@ def dist_init(world, backend):
     return None
 
 
-def reduce_max(dist, value: float, device) -> float:
+def reduce_max(dist, value: float, device=None) -> float:
+    """Max over ranks (device None: a CPU tensor, for the gloo backend)."""
     if dist is None:
         return value
     import torch
@@ -168,6 +169,11 @@ def reduce_max(dist, value: float, device) -> float:
     t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(world: int, flops_per_rank_step: int, steps: int, max_total_ms: float) -> float:
+    """Whole-job TFLOP/s: the work of every rank divided by the slowest rank's time."""
+    return world * flops_per_rank_step * steps / (max_total_ms * 1e-3) / 1e12
 
 
 def barrier(dist):
@@ -208,6 +214,13 @@ def oracle_sample(w, x, budget_s: float, rng, threads=None):
 
 # ----------------------------------------------------------------------------- our arm
 
+def workload_of(args):
+    w = synth.WORKLOADS[args.workload]
+    if args.batch is not None and args.batch != w.B:
+        w = w.with_(B=args.batch)
+    return w
+
+
 def run_ours(args):
     import torch
 
@@ -217,7 +230,7 @@ def run_ours(args):
     dist = dist_init(world, "nccl")
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
-    w = synth.WORKLOADS[args.workload]
+    w = workload_of(args)
     x = synth.make_inputs(w, seed=w.seed + rank)
     tdt = torch.float16 if w.dtype == "fp16" else torch.bfloat16
     dtype = sa.SA_FP16 if w.dtype == "fp16" else sa.SA_BF16
@@ -311,7 +324,7 @@ def run_ours(args):
         return None
     fl = flops(w)
     peaks = load_peaks()
-    value = world * fl * args.steps / (total_ms * 1e-3) / 1e12
+    value = job_throughput(world, fl, args.steps, total_ms)
     attn_avg_s = statistics.mean(attn_ms) * 1e-3
     achieved = fl / attn_avg_s / 1e12
     cpu = None
@@ -343,7 +356,7 @@ def run_ours(args):
                      "avg_ms": attn_avg_s * 1e3},
         "stages_ms": {"rope": statistics.mean(rope_ms), "attention": statistics.mean(attn_ms)},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * fl * args.steps / (e2e_total * 1e-3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_throughput(world, fl, args.steps, e2e_total), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": 2 * args.steps,
         "clocks": clk,
@@ -357,7 +370,7 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return None
-    w = synth.WORKLOADS[args.workload]
+    w = workload_of(args)
     x = synth.make_inputs(w)
     rng = np.random.default_rng(1)
     per_step = max(0.2, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
@@ -401,6 +414,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size B")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
