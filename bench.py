@@ -77,68 +77,129 @@ def load_peaks():
         return {"hbm_gbs": 6800.0, "tflops": 1900.0, "tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def kernel_sha() -> str:
+    import hashlib
+
+    path = os.path.join(ROOT, "diffusion_transformer_attention_rope_gb300", "csrc", "sa_fmha.cu")
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
 def load_traffic(workload: str):
-    """DRAM bytes per attention launch from the committed ncu summary, if one exists."""
+    """DRAM bytes per attention launch from the committed ncu summary, or None when no
+    capture exists for this workload or the kernel source changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            t = json.load(f)
-        return t.get(workload)
+            t = json.load(f).get(workload)
+        if t and t.get("kernel_sha") == kernel_sha():
+            return t["bytes"]
     except Exception:
-        return None
+        pass
+    return None
 
 
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi clock / throttle samples every 200 ms while the timed region runs."""
+    """SM clock and throttle reasons sampled DURING the timed region.
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    A thread polls NVML (libnvidia-ml through ctypes) every ~0.5 ms, so even a
+    millisecond-long timed region gets samples; nvidia-smi (-lms 200) is the fallback.
+    Only reads are made: no clock or other GPU setting is changed.
+    """
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
-        self.path = os.path.join("/tmp", f"sa_clocks_{os.getpid()}.csv")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, cuda_index: int):
+        self.cuda_index = cuda_index
+        self.samples = []
+        self.max_mhz = None
+        self._stop = False
+        self._thread = None
+        self._nv = None
+        self._smi = None
+
+    def _nvml_handle(self):
+        import ctypes
+
+        import torch
+
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            return None
+        props = torch.cuda.get_device_properties(self.cuda_index)
+        bus = "%08X:%02X:%02X.0" % (getattr(props, "pci_domain_id", 0), props.pci_bus_id, props.pci_device_id)
+        h = ctypes.c_void_p()
+        if nv.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(h)) != 0:
+            return None
+        mx = ctypes.c_uint()
+        if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+            self.max_mhz = float(mx.value)
+        self._nv = nv
+        return h
+
+    def _poll(self, h):
+        import ctypes
+
+        clk = ctypes.c_uint()
+        rs = ctypes.c_ulonglong()
+        get_reasons = getattr(self._nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            self._nv.nvmlDeviceGetCurrentClocksThrottleReasons
+        while not self._stop:
+            if self._nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                r = rs.value if get_reasons(h, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((float(clk.value), int(r)))
+            time.sleep(0.0005)
 
     def start(self):
+        import threading
+
         try:
-            self.f = open(self.path, "w")
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=self.f, stderr=subprocess.DEVNULL)
+            h = self._nvml_handle()
         except Exception:
-            self.proc = None
+            h = None
+        if h is not None:
+            self._thread = threading.Thread(target=self._poll, args=(h,), daemon=True)
+            self._thread.start()
+            while not self.samples and self._thread.is_alive():
+                time.sleep(0.0005)
+            return
+        try:
+            self._path = os.path.join("/tmp", f"sa_clocks_{os.getpid()}.csv")
+            self._f = open(self._path, "w")
+            self._smi = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.cuda_index}", "--query-gpu=clocks.sm,clocks.max.sm,"
+                 "clocks_event_reasons.active", "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self._f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self._smi = None
 
     def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.f.close()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
+        if self._thread is not None:
+            self._stop = True
+            self._thread.join(timeout=5)
+        elif self._smi is not None:
+            self._smi.terminate()
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        os.unlink(self.path)
-        if not sm:
+                self._smi.wait(timeout=5)
+            except Exception:
+                self._smi.kill()
+            self._f.close()
+            for line in open(self._path):
+                parts = [p.strip() for p in line.split(",")]
+                try:
+                    self.samples.append((float(parts[0]), int(parts[2], 16)))
+                    self.max_mhz = float(parts[1])
+                except (ValueError, IndexError):
+                    continue
+            os.unlink(self._path)
+        if not self.samples:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        reasons = sorted({name for _, r in self.samples for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "samples": len(self.samples), "reasons": reasons,
+                "source": "nvml" if self._thread is not None else "nvidia-smi"}
 
 
 # ----------------------------------------------------------------------------- distributed
@@ -352,7 +413,8 @@ def run_ours(args):
         "frac_of_peak": value / world / peaks["tflops"],
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["tflops"], "traffic": load_traffic(w.name),
-                     "kernel": "attention (sa_attn_fwd)", "peak_source": peaks["source"] + " bf16 burst",
+                     "kernel": "attention (sa_attn_fwd)", "kernel_sha": kernel_sha(),
+                     "peak_source": peaks["source"] + " bf16 burst",
                      "avg_ms": attn_avg_s * 1e3},
         "stages_ms": {"rope": statistics.mean(rope_ms), "attention": statistics.mean(attn_ms)},
         "cpu_baseline": cpu,
