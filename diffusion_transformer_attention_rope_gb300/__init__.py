@@ -19,7 +19,7 @@ from typing import Optional, Sequence
 __all__ = [
     "SA_FP16", "SA_BF16", "SaAttnError", "library_path", "load_library",
     "sa_attn_create", "sa_attn_destroy", "sa_rope_attn_workspace_size", "sa_rope_attn",
-    "sa_rope_qk", "sa_attn_fwd", "sa_attn_check", "sa_last_error", "sa_status_string", "RopeAttention",
+    "sa_rope_qk", "sa_attn_fwd", "sa_rope_attn_noalloc", "sa_attn_check", "sa_last_error", "sa_status_string", "RopeAttention",
 ]
 
 SA_FP16 = 0
@@ -68,6 +68,9 @@ def load_library():
         lib.sa_rope_qk.restype = i
         lib.sa_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(f), i, vp]
         lib.sa_attn_fwd.restype = i
+        lib.sa_rope_attn_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i,
+                                             ctypes.POINTER(f), i, vp]
+        lib.sa_rope_attn_noalloc.restype = i
         lib.sa_attn_check.argtypes = [vp]
         lib.sa_attn_check.restype = i
         lib.sa_last_error.argtypes = []
@@ -142,6 +145,20 @@ def sa_attn_fwd(handle: int, q_rot: int, k_rot: int, v: int, out: int, B: int, H
         ctypes.c_void_p(handle), ctypes.c_void_p(q_rot), ctypes.c_void_p(k_rot), ctypes.c_void_p(v),
         ctypes.c_void_p(out), int(B), int(H), int(L), int(d), int(window), _lam(lam), int(dtype),
         ctypes.c_void_p(stream)))
+
+
+def sa_rope_attn_noalloc(handle: int, q: int, k: int, v: int, positions: Optional[int], out: int,
+                         B: int, H: int, L: int, d: int, window: int,
+                         lam: Optional[Sequence[float]], dtype: int, stream: Optional[int]) -> None:
+    """sa_rope_attn without a workspace: for callers that cannot allocate device memory.
+    The library's built-in scratch (SA_NOALLOC_SCRATCH_BYTES) is used and shared by all calls."""
+    _check(load_library().sa_rope_attn_noalloc(
+        ctypes.c_void_p(handle), ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v),
+        ctypes.c_void_p(positions), ctypes.c_void_p(out), int(B), int(H), int(L), int(d),
+        int(window), _lam(lam), int(dtype), ctypes.c_void_p(stream)))
+
+
+SA_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 def sa_attn_check(handle: int) -> None:

@@ -172,6 +172,36 @@ sa_status launch_attn(const sa_attn_s* h, const void* q_rot, const void* k_rot, 
 
 }  // namespace
 
+namespace sa {
+
+// Library-internal hooks used by sa_noalloc.cu (not exported).
+sa_status set_error(sa_status st, const char* msg) { return fail(st, "%s", msg); }
+
+int handle_device(sa_attn_t h) { return h->device; }
+
+// The checks and the two launches of sa_rope_attn, with q', k' placed at caller-given
+// device addresses instead of a workspace argument.
+sa_status rope_attn_into(const char* fn, sa_attn_t h, const void* q, const void* k, const void* v,
+                         const int32_t* positions, void* out, int B, int H, int L, int d,
+                         int window, const float* lambda, sa_dtype dtype, void* q_rot, void* k_rot,
+                         sa_stream_t stream) {
+  if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
+  if (!q || !k || !v || !out)
+    return fail(SA_ERR_INVALID_ARG, "%s: q, k, v and out must be non-NULL", fn);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(q_rot) ||
+      !aligned16(k_rot))
+    return fail(SA_ERR_INVALID_ARG, "%s: q, k, v and out must be 16-byte aligned", fn);
+  const bool diff = lambda != nullptr;
+  sa_status st = check_shape(fn, B, H, L, d, dtype, diff);
+  if (st != SA_OK) return st;
+  if ((st = check_lambda(fn, lambda, H)) != SA_OK) return st;
+  st = launch_rope(h, q, k, positions, q_rot, k_rot, B, H, L, diff ? 2 : 1, dtype, stream);
+  if (st != SA_OK) return st;
+  return launch_attn(h, q_rot, k_rot, v, out, B, H, L, window, lambda, dtype, stream);
+}
+
+}  // namespace sa
+
 extern "C" {
 
 const char* sa_last_error(void) { return g_msg; }

@@ -7,6 +7,8 @@
 
 #include <cstdint>
 
+#include "sa_attn.h"
+
 namespace sa {
 
 constexpr int kHeadDim = 64;          // d of q and k (the only supported value)
@@ -56,5 +58,13 @@ cudaError_t fmha_set_attributes();
 cudaError_t fmha_launch(bool diff, bool bf16, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                         const CUtensorMap& tm_v, const FmhaArgs& a, long long num_ctas,
                         cudaStream_t stream);
+
+// Library-internal hooks defined in sa_api.cu (not part of the exported C ABI).
+sa_status set_error(sa_status st, const char* msg);
+int handle_device(sa_attn_t h);
+sa_status rope_attn_into(const char* fn, sa_attn_t h, const void* q, const void* k, const void* v,
+                         const int32_t* positions, void* out, int B, int H, int L, int d,
+                         int window, const float* lambda, sa_dtype dtype, void* q_rot, void* k_rot,
+                         sa_stream_t stream);
 
 }  // namespace sa

@@ -159,6 +159,43 @@ SA_API sa_status sa_attn_fwd(sa_attn_t handle,
                              sa_dtype dtype, sa_stream_t stream);
 
 /*
+ * Size of the scratch array built into the library for sa_rope_attn_noalloc:
+ * 64 MiB, enough for 2 * B*H*nmaps*L*64 two-byte elements up to that total
+ * (every Stable Audio 3 shape here, up to B*H*nmaps*L = 262144 rows).
+ */
+#define SA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
+
+/*
+ * sa_rope_attn_noalloc: the same computation as sa_rope_attn, for callers
+ * that cannot allocate device memory -- an engine plugin whose enqueue hook
+ * only hands over tensor pointers and a stream, a real-time audio thread that
+ * must not block in an allocator, a process whose device memory belongs to
+ * another allocator.  The pages have no counterpart: this is an interface
+ * convenience, not part of the method.
+ *
+ * It takes no workspace and allocates nothing: the rotated q', k' go to one
+ * static device array of SA_NOALLOC_SCRATCH_BYTES inside the library, which
+ * every GPU that loads the library keeps until the process exits.  The first
+ * call on a device looks up that array's device address (with the device
+ * current), so make that first call before any stream capture.  All calls
+ * share the array: calls that may overlap on the GPU race on it, so order them
+ * (one stream).  Nothing in it needs clearing between calls.
+ *
+ * Arguments, layouts and errors are those of sa_rope_attn, except that a shape
+ * whose scratch (sa_rope_attn_workspace_size) exceeds SA_NOALLOC_SCRATCH_BYTES
+ * is rejected with SA_ERR_WORKSPACE before anything is enqueued.
+ */
+SA_API sa_status sa_rope_attn_noalloc(sa_attn_t handle,
+                                      const void* q, const void* k, const void* v,
+                                      const int32_t* positions,
+                                      void* out,
+                                      int B, int H, int L, int d,
+                                      int window,
+                                      const float* lambda,
+                                      sa_dtype dtype,
+                                      sa_stream_t stream);
+
+/*
  * Synchronize the handle's device, then read and clear its device error
  * word.  SA_OK if no kernel since the last check gave up on a wait;
  * SA_ERR_DEVICE_TIMEOUT otherwise (its output is then unspecified).
