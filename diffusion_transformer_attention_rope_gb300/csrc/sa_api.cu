@@ -270,6 +270,15 @@ sa_status sa_attn_create(sa_attn_t* handle, int device, float rope_base) {
     delete h;
     return fail(SA_ERR_CUDA, "sa_attn_create: %s", cudaGetErrorString(e));
   }
+  int regs = -1;
+  if (!sa::fmha_check_registers(&regs)) {
+    // The warpgroup register split (setmaxnreg) is sized for this launch allocation; any
+    // other value could make the register grow wait forever, so refuse to run.
+    cudaFree(h->d_err);
+    delete h;
+    return fail(SA_ERR_UNSUPPORTED, "sa_attn_create: attention kernel built with %d registers per "
+                "thread, expected %d", regs, sa::kFmhaLaunchRegs);
+  }
   *handle = h;
   return ok();
 }

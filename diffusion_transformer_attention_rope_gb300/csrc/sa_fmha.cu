@@ -33,7 +33,8 @@ namespace {
 
 constexpr int kTile = kBlockM * kHeadDim * 2;  // bytes of one 128 x 64 fp16/bf16 tile (16 KB)
 constexpr int kTmaWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaWarp = 9;    // first MMA issuer (stream 0); also allocates TMEM
+constexpr int kMmaWarp1 = 10;  // second MMA issuer (stream 1)
 constexpr uint32_t kTmemCols = 512;
 
 template <bool DIFF>
@@ -49,8 +50,8 @@ struct Cfg {
   static constexpr int OFF_V = OFF_K + NS * K_STAGE;
   static constexpr int OFF_BAR = OFF_V + NS * V_STAGE;
   // barriers: q_full, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full[2],
-  //           pv_done[2], o_full, drain
-  static constexpr int NBAR = 1 + 3 * NS + 2 + 2 + 2 + 1 + 1;
+  //           pv_done[2], s_free[2], o_full[2], drain[2], turn[2]
+  static constexpr int NBAR = 1 + 3 * NS + 2 + 2 + 2 + 2 + 2 + 2 + 2;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;           // tmem base, abort flag
   static constexpr int OFF_LSUM = OFF_MISC + 16;                // float [2][128]
   static constexpr int SMEM_USED = OFF_LSUM + 2 * kBlockM * 4;
@@ -65,7 +66,8 @@ static_assert(Cfg<true>::SMEM_ALLOC <= 227 * 1024, "smem budget");
 static_assert(Cfg<false>::SMEM_USED > 114 * 1024, "one CTA per SM keeps TMEM allocation uncontended");
 
 struct Barriers {
-  uint32_t q_full, k_full0, v_full0, kv_empty0, s_full0, p_full0, pv_done0, o_full, drain;
+  uint32_t q_full, k_full0, v_full0, kv_empty0, s_full0, p_full0, pv_done0, s_free0, o_full0, drain0,
+      turn0;
   int ns;
   __device__ uint32_t k_full(int i) const { return k_full0 + 8 * i; }
   __device__ uint32_t v_full(int i) const { return v_full0 + 8 * i; }
@@ -73,12 +75,19 @@ struct Barriers {
   __device__ uint32_t s_full(int s) const { return s_full0 + 8 * s; }
   __device__ uint32_t p_full(int s) const { return p_full0 + 8 * s; }
   __device__ uint32_t pv_done(int s) const { return pv_done0 + 8 * s; }
+  __device__ uint32_t s_free(int s) const { return s_free0 + 8 * s; }
+  __device__ uint32_t o_full(int s) const { return o_full0 + 8 * s; }
+  __device__ uint32_t drain(int s) const { return drain0 + 8 * s; }
+  __device__ uint32_t turn(int s) const { return turn0 + 8 * s; }
 };
 
-// Pipeline wait: bounded by the wall clock and by the CTA abort flag.
+// Pipeline wait: bounded by the wall clock and by the CTA abort flag.  The first probes
+// skip the abort / clock checks (most waits end within a few probes).
 __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                       int* err, int err_bit, uint64_t timeout_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+#pragma unroll 1
+  for (int i = 0; i < 4; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
@@ -111,8 +120,10 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
   bar.s_full0 = bar.kv_empty0 + 8 * C::NS;
   bar.p_full0 = bar.s_full0 + 16;
   bar.pv_done0 = bar.p_full0 + 16;
-  bar.o_full = bar.pv_done0 + 16;
-  bar.drain = bar.o_full + 8;
+  bar.s_free0 = bar.pv_done0 + 16;
+  bar.o_full0 = bar.s_free0 + 16;
+  bar.drain0 = bar.o_full0 + 16;
+  bar.turn0 = bar.drain0 + 16;
 
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -140,15 +151,17 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     for (int i = 0; i < C::NS; ++i) {
       mbar_init(bar.k_full(i), 1);
       mbar_init(bar.v_full(i), 1);
-      mbar_init(bar.kv_empty(i), 1);
+      mbar_init(bar.kv_empty(i), 2);   // one commit from each MMA issuer
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar.s_full(s), 1);
       mbar_init(bar.p_full(s), kBlockM);
       mbar_init(bar.pv_done(s), 1);
+      mbar_init(bar.s_free(s), kBlockM);
+      mbar_init(bar.o_full(s), 1);
+      mbar_init(bar.drain(s), 1);
+      mbar_init(bar.turn(s), kBlockM);
     }
-    mbar_init(bar.o_full, 1);
-    mbar_init(bar.drain, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -166,6 +179,9 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
+  if (warp >= 8) {
+  // Control warpgroup (TMA producer, two MMA issuers, one spare warp): few registers.
+  regs_dec<kControlRegs>();
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
@@ -211,35 +227,39 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == kMmaWarp) {
-    // ------------------------------------------------------------------ MMA issuer
+  } else if (warp == kMmaWarp || warp == kMmaWarp1) {
+    // ------------------------------------------------------------------ MMA issuers
+    // One issuing thread per stream s (query tile s, or map s): each runs its own
+    // S -> softmax -> P.V chain so the two chains never wait on each other's issue.
+    const int s = warp - kMmaWarp;
     if (lane == 0) {
       constexpr uint32_t idesc_s = make_idesc_f16(kBlockM, kBlockN, BF16, false);
       constexpr uint32_t idesc_o = make_idesc_f16(kBlockM, C::DV, BF16, true);
-      auto issue_s = [&](int s, int st) {
-        const uint32_t qa = sQ + s * kTile;
-        const uint32_t kb = sK + st * C::K_STAGE + (DIFF ? s * kTile : 0);
+      // Descriptors computed once; the 14-bit address field advances by constant steps
+      // (32 B along K inside a swizzle row, 2 KB per 16 keys of V, one stage per ring slot).
+      const uint64_t dq = smem_desc_sw128(sQ + s * kTile, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(sK + (DIFF ? s * kTile : 0), 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(sV, kTile, 1024);
+      const uint32_t d_s = tmem + C::s_col(s), d_o = tmem + C::o_col(s), a_p = tmem + C::p_col(s);
+      auto issue_s = [&](int st) {
+        const uint64_t dk = dk0 + static_cast<uint64_t>(st * (C::K_STAGE >> 4));
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk)
-          umma_ss(tmem + C::s_col(s), smem_desc_sw128(qa + 32 * kk, 16, 1024),
-                  smem_desc_sw128(kb + 32 * kk, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+          umma_ss(d_s, dq + 2 * kk, dk + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
       };
-      auto issue_pv = [&](int s, int st, bool accumulate) {
-        const uint32_t vb = sV + st * C::V_STAGE;
+      auto issue_pv = [&](int st, bool accumulate) {
+        const uint64_t dv = dv0 + static_cast<uint64_t>(st * (C::V_STAGE >> 4));
 #pragma unroll
         for (int kk = 0; kk < kBlockN / 16; ++kk)
-          umma_ts(tmem + C::o_col(s), tmem + C::p_col(s) + 8 * kk,
-                  smem_desc_sw128(vb + 2048 * kk, kTile, 1024), idesc_o,
-                  (accumulate || kk > 0) ? 1u : 0u);
+          umma_ts(d_o, a_p + 8 * kk, dv + 128 * kk, idesc_o, (accumulate || kk > 0) ? 1u : 0u);
       };
-      bool ok = pwait(bar.q_full, 0, abort_flag, a.err, kErrMma, tmo) &&
-                pwait(bar.k_full(0), 0, abort_flag, a.err, kErrMma, tmo);
+      const int eb = kErrMma;
+      bool ok = pwait(bar.q_full, 0, abort_flag, a.err, eb, tmo) &&
+                pwait(bar.k_full(0), 0, abort_flag, a.err, eb, tmo);
       if (ok) {
         tc_fence_after();
-        issue_s(0, 0);
-        umma_commit(bar.s_full(0));
-        issue_s(1, 0);
-        umma_commit(bar.s_full(1));
+        issue_s(0);
+        umma_commit(bar.s_full(s));
       }
       for (int it = 0; ok && it < n_tiles; ++it) {
         const int st = it % C::NS;
@@ -247,53 +267,43 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         const bool last = it + 1 == n_tiles;
         const int st2 = (it + 1) % C::NS;
         const uint32_t ph2 = ((it + 1) / C::NS) & 1;
-        if (!DIFF) {
-          for (int s = 0; s < 2 && ok; ++s) {
-            ok = pwait(bar.p_full(s), it & 1, abort_flag, a.err, kErrMma, tmo);
-            if (ok && s == 0) ok = pwait(bar.v_full(st), ph, abort_flag, a.err, kErrMma, tmo);
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv(s, st, it > 0);
-            if (s == 1) umma_commit(bar.kv_empty(st));
-            if (!last) {
-              if (s == 0) ok = pwait(bar.k_full(st2), ph2, abort_flag, a.err, kErrMma, tmo);
-              if (!ok) break;
-              tc_fence_after();
-              issue_s(s, st2);
-              umma_commit(bar.s_full(s));
-            }
-          }
-        } else {
-          ok = pwait(bar.v_full(st), ph, abort_flag, a.err, kErrMma, tmo);
-          for (int s = 0; s < 2 && ok; ++s) {
-            ok = pwait(bar.p_full(s), it & 1, abort_flag, a.err, kErrMma, tmo);
-            if (!ok) break;
-            tc_fence_after();
-            issue_pv(s, st, it > 0);
-            umma_commit(bar.pv_done(s));
-          }
-          if (ok) umma_commit(bar.kv_empty(st));
-          if (ok && !last) {
-            ok = pwait(bar.k_full(st2), ph2, abort_flag, a.err, kErrMma, tmo);
-            for (int s = 0; s < 2 && ok; ++s) {
-              // P_s lives in the S_s columns: the next S_s may only be written once P_s V is done.
-              ok = pwait(bar.pv_done(s), it & 1, abort_flag, a.err, kErrMma, tmo);
-              if (!ok) break;
-              tc_fence_after();
-              issue_s(s, st2);
-              umma_commit(bar.s_full(s));
-            }
-          }
+        if (!DIFF && !last) {
+          // S(it+1) as soon as the softmax warps hold S(it) in registers (S and P have
+          // separate TMEM columns), overlapping their exponentials.
+          ok = pwait(bar.k_full(st2), ph2, abort_flag, a.err, eb, tmo) &&
+               pwait(bar.s_free(s), it & 1, abort_flag, a.err, eb, tmo);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(st2);
+          umma_commit(bar.s_full(s));
         }
-        if (ok && last) umma_commit(bar.o_full);
+        ok = pwait(bar.p_full(s), it & 1, abort_flag, a.err, eb, tmo) &&
+             pwait(bar.v_full(st), ph, abort_flag, a.err, eb, tmo);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(st, it > 0);
+        umma_commit(bar.pv_done(s));
+        umma_commit(bar.kv_empty(st));
+        if (DIFF && !last) {
+          // P lives in the S columns here: the next S may only be written once P.V is done.
+          ok = pwait(bar.k_full(st2), ph2, abort_flag, a.err, eb, tmo) &&
+               pwait(bar.pv_done(s), it & 1, abort_flag, a.err, eb, tmo);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(st2);
+          umma_commit(bar.s_full(s));
+        }
+        if (last) umma_commit(bar.o_full(s));
       }
-      // No MMA may still be running when TMEM is released.
-      umma_commit(bar.drain);
-      mbar_wait_limit(bar.drain, 0, tmo);
+      // No MMA of this issuer may still be running when TMEM is released.
+      umma_commit(bar.drain(s));
+      mbar_wait_limit(bar.drain(s), 0, tmo);
     }
     __syncwarp();
+  }
   } else {
     // ------------------------------------------------------------------ softmax warpgroups
+    regs_inc<kSoftmaxRegs>();
     const int s = warp >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                     // TMEM lane = tile row
@@ -305,6 +315,10 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     float m_use = -INFINITY;
     float l_sum = 0.0f;
     bool ok = true;
+    // The two warpgroups take turns on the exponential phase (the exp unit is the scarce
+    // resource): warpgroup 0 goes first, each hands the turn over when its exponentials are
+    // issued, so one group's max / TMEM / barrier work overlaps the other's exponentials.
+    if (s == 1) mbar_arrive(bar.turn(0));
 
     for (int it = 0; it < n_tiles; ++it) {
       ok = pwait(bar.s_full(s), it & 1, abort_flag, a.err, kErrSoftmax, tmo);
@@ -316,6 +330,11 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       for (int cc = 0; cc < kBlockN / 32; ++cc)
         tmem_ld32_nowait(tmem + C::s_col(s) + lane_off + 32 * cc, sr + 32 * cc);
       tmem_wait_ld_128(sr);
+      if (!DIFF) {
+        // S_s is in registers: the issuer may write the next S_s into these columns now.
+        tc_fence_before();
+        mbar_arrive(bar.s_free(s));
+      }
 
       const int key0 = (t_lo + it) * kBlockN;
       const bool need_mask =
@@ -330,16 +349,17 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
           if (!valid) sr[j] = __float_as_uint(-INFINITY);
         }
       }
-      float mx0 = __uint_as_float(sr[0]), mx1 = __uint_as_float(sr[1]);
-      float mx2 = __uint_as_float(sr[2]), mx3 = __uint_as_float(sr[3]);
+      // 8 independent chains; chain q covers elements q, q + 8, ..., q + 120.
+      float mx[8];
 #pragma unroll
-      for (int j = 4; j < kBlockN; j += 4) {
-        mx0 = fmaxf(mx0, __uint_as_float(sr[j]));
-        mx1 = fmaxf(mx1, __uint_as_float(sr[j + 1]));
-        mx2 = fmaxf(mx2, __uint_as_float(sr[j + 2]));
-        mx3 = fmaxf(mx3, __uint_as_float(sr[j + 3]));
+      for (int q = 0; q < 8; ++q) mx[q] = fmaxf(__uint_as_float(sr[q]), __uint_as_float(sr[q + 8]));
+#pragma unroll
+      for (int j = 16; j < kBlockN; j += 16) {
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+          mx[q] = fmax3(mx[q], __uint_as_float(sr[j + q]), __uint_as_float(sr[j + 8 + q]));
       }
-      const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3));
+      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
 
       // Lazy rescale: keep the old running max unless this tile raises it by more than tau
       // (P then stays <= 2^8).  The decision is warp-uniform because tcgen05.ld/st are.
@@ -354,29 +374,54 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         rescale = true;
       }
       const float mb = (m_use == -INFINITY) ? 0.0f : m_use * c;
-      float sum0 = 0.0f, sum1 = 0.0f;
-      uint32_t pk[kBlockN / 2];
-#pragma unroll
-      for (int j = 0; j < kBlockN / 2; ++j) {
-        const float p0 = ex2_approx(fmaf(__uint_as_float(sr[2 * j]), c, -mb));
-        const float p1 = ex2_approx(fmaf(__uint_as_float(sr[2 * j + 1]), c, -mb));
-        sum0 += p0;
-        sum1 += p1;
-        pk[j] = pack2<BF16>(p0, p1);
+      const float2 c2 = make_float2(c, c), nmb2 = make_float2(-mb, -mb);
+      if (!DIFF && it > 0) {
+        // P_s and O_s are still read / written by P_s V of the previous tile until it is done.
+        ok = pwait(bar.pv_done(s), (it - 1) & 1, abort_flag, a.err, kErrSoftmax, tmo);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
       }
-      l_sum = fmaf(l_sum, f, sum0 + sum1);
-      tmem_st32(tmem + C::p_col(s) + lane_off, pk);
-      tmem_st32(tmem + C::p_col(s) + lane_off + 32, pk + 32);
+      ok = pwait(bar.turn(s), it & 1, abort_flag, a.err, kErrSoftmax, tmo);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      float2 sum0 = make_float2(0.0f, 0.0f), sum1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        // exponentials of columns [64 h, 64 h + 64) -> 32 packed pairs -> TMEM
+        uint32_t pk[32];
+#pragma unroll
+        for (int j = 0; j < 32; j += 2) {
+          const int e = 64 * h + 2 * j;
+          const float2 x0 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nmb2);
+          const float2 x1 = ffma2(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nmb2);
+          const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+          const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+          sum0 = fadd2(sum0, p0);
+          sum1 = fadd2(sum1, p1);
+          pk[j] = pack2<BF16>(p0.x, p0.y);
+          pk[j + 1] = pack2<BF16>(p1.x, p1.y);
+        }
+        tmem_st32(tmem + C::p_col(s) + lane_off + 32 * h, pk);
+      }
+      mbar_arrive(bar.turn(1 - s));
+      const float2 sum = fadd2(sum0, sum1);
+      l_sum = fmaf(l_sum, f, sum.x + sum.y);
       if (rescale) {
-        // O_s is stable here: P_s V of the previous tile finished before S_s of this tile
-        // was committed, and P_s V of this tile waits for the arrive below.
+        // O_s is stable here: P_s V of the previous tile has finished and P_s V of this
+        // tile waits for the arrive below.
 #pragma unroll
         for (int cc = 0; cc < C::DV / 32; ++cc) {
           uint32_t o[32];
           tmem_ld32_nowait(tmem + C::o_col(s) + lane_off + 32 * cc, o);
           tmem_wait_ld_32(o);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+          for (int j = 0; j < 32; j += 2) {
+            const float2 v2 = fmul2(make_float2(__uint_as_float(o[j]), __uint_as_float(o[j + 1])),
+                                    make_float2(f, f));
+            o[j] = __float_as_uint(v2.x);
+            o[j + 1] = __float_as_uint(v2.y);
+          }
           tmem_st32(tmem + C::o_col(s) + lane_off + 32 * cc, o);
         }
       }
@@ -386,7 +431,8 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     }
 
     // ---------------------------------------------------------------- epilogue
-    if (ok) ok = pwait(bar.o_full, 0, abort_flag, a.err, kErrSoftmax, tmo);
+    if (ok) ok = pwait(bar.o_full(s), 0, abort_flag, a.err, kErrSoftmax, tmo);
+    if (DIFF && ok) ok = pwait(bar.o_full(1 - s), 0, abort_flag, a.err, kErrSoftmax, tmo);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
     if (!DIFF) {
@@ -473,6 +519,20 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
 }
 
 }  // namespace
+
+bool fmha_check_registers(int* got) {
+  const void* fns[4] = {reinterpret_cast<const void*>(fmha_kernel<false, false>),
+                        reinterpret_cast<const void*>(fmha_kernel<false, true>),
+                        reinterpret_cast<const void*>(fmha_kernel<true, false>),
+                        reinterpret_cast<const void*>(fmha_kernel<true, true>)};
+  for (const void* f : fns) {
+    cudaFuncAttributes attr;
+    if (cudaFuncGetAttributes(&attr, f) != cudaSuccess) return false;
+    *got = attr.numRegs;
+    if (attr.numRegs != kFmhaLaunchRegs) return false;
+  }
+  return true;
+}
 
 cudaError_t fmha_set_attributes() {
   cudaError_t e;

@@ -15,7 +15,15 @@ constexpr int kHeadDim = 64;          // d of q and k (the only supported value)
 constexpr int kBlockM = 128;          // query rows per tile = TMEM lanes
 constexpr int kBlockN = 128;          // keys per K/V tile
 constexpr int kMaxDiffHeads = 128;    // lambda is carried by value in the kernel arguments
-constexpr int kFmhaThreads = 320;     // 8 softmax warps + 1 TMA warp + 1 MMA warp
+constexpr int kFmhaThreads = 384;     // 3 warpgroups: 2 softmax + (TMA, 2 MMA issuers, 1 spare)
+// Register split (setmaxnreg): the kernel is launched with kFmhaLaunchRegs per thread; the
+// softmax warpgroups grow to kSoftmaxRegs, the TMA/MMA warpgroup shrinks to kControlRegs.
+// The split must not exceed the launch total: 2*128*224 + 128*56 = 384*168.
+constexpr int kFmhaLaunchRegs = 168;
+constexpr int kSoftmaxRegs = 224;
+constexpr int kControlRegs = 56;
+static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kFmhaThreads * kFmhaLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr int kMaxL = 1 << 24;        // positions and row indices stay exact in FP32 / int32
 
 // Bits of the device error word.
@@ -55,6 +63,8 @@ constexpr int fmha_rows_per_cta(bool diff) { return diff ? kBlockM : 2 * kBlockM
 cudaError_t rope_launch(const RopeArgs& a, bool bf16, int num_sms, cudaStream_t stream);
 
 cudaError_t fmha_set_attributes();
+// Registers per thread ptxas assigned to each attention kernel (must equal kFmhaLaunchRegs).
+bool fmha_check_registers(int* got);
 cudaError_t fmha_launch(bool diff, bool bf16, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                         const CUtensorMap& tm_v, const FmhaArgs& a, long long num_ctas,
                         cudaStream_t stream);
