@@ -186,6 +186,9 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
       const int plane_q = DIFF ? 2 * bh : bh;
+      // This grid may have been started early (programmatic dependent launch) while the RoPE
+      // pass that writes q', k' is still running: wait for it before the first load.
+      asm volatile("griddepcontrol.wait;" ::: "memory");
       mbar_arrive_expect_tx(bar.q_full, C::Q_BYTES);
       if (DIFF) {
         tma_load_3d(sQ, &tm_q, bar.q_full, 0, q0, plane_q);
@@ -510,12 +513,22 @@ cudaError_t set_attr() {
                               Cfg<DIFF>::SMEM_ALLOC);
 }
 
+// Launched with programmatic stream serialization: the CTAs may start while the previous
+// kernel on the stream (the RoPE pass) finishes; only the TMA warp waits for it.
 template <bool DIFF, bool BF16>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                    const FmhaArgs& a, long long num_ctas, cudaStream_t stream) {
-  fmha_kernel<DIFF, BF16><<<static_cast<unsigned>(num_ctas), kFmhaThreads, Cfg<DIFF>::SMEM_ALLOC,
-                            stream>>>(tq, tk, tv, a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_ctas));
+  cfg.blockDim = dim3(kFmhaThreads);
+  cfg.dynamicSmemBytes = Cfg<DIFF>::SMEM_ALLOC;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fmha_kernel<DIFF, BF16>, tq, tk, tv, a);
 }
 
 }  // namespace

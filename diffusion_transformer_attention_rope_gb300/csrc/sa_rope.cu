@@ -8,9 +8,12 @@
 // README ("Retired: bf16") shows what a low-precision angle does at long sequence lengths.
 //
 // One block rotates 32 positions of every plane in its slice of planes (a plane is one
-// (batch, head, map) sequence).  sin/cos are computed once per (position, pair) and reused
-// across all planes of the slice and across q and k.  The pass is HBM-bound: it reads q and k
-// once and writes q', k' once, with 16-byte accesses.
+// (batch, head, map) sequence of L rows).  A thread owns 8 rotation pairs of one position
+// (two 16-byte chunks per row) and up to kPlaneBatch planes at a time: it issues all the loads
+// of a batch first, then computes its 8 (cos, sin) pairs once, then rotates and stores, so
+// many bytes are in flight per thread.  The pass is HBM-bound: q, k read once, q', k' written
+// once.  Each block signals early that the dependent attention launch may start (its CTAs
+// then only prepare; they wait for this grid before reading q', k').
 #include "sa_kernels.h"
 #include "sa_ptx.cuh"
 
@@ -19,6 +22,7 @@ namespace {
 
 constexpr int kRopeRows = 32;      // positions per block
 constexpr int kRopeThreads = 128;  // 32 positions x 4 groups of 8 rotation pairs
+constexpr int kPlaneBatch = 4;     // planes whose loads are issued together
 
 __device__ __forceinline__ uint4 ld_stream(const uint16_t* p) {
   uint4 v;
@@ -34,13 +38,10 @@ __device__ __forceinline__ void st_v4(uint16_t* p, uint4 v) {
                : "memory");
 }
 
-// Rotate elements [8g, 8g+8) together with their partners [32+8g, 32+8g+8) of one row.
+// Rotate 8 pairs: lo = x[8g .. 8g+8), hi = x[32+8g .. 32+8g+8).
 template <bool BF16>
-__device__ __forceinline__ void rotate_chunk(const uint16_t* __restrict__ src,
-                                             uint16_t* __restrict__ dst, const float (&c)[8],
-                                             const float (&s)[8]) {
-  const uint4 lo = ld_stream(src);
-  const uint4 hi = ld_stream(src + 32);
+__device__ __forceinline__ void rotate(const uint4& lo, const uint4& hi, const float (&c)[8],
+                                       const float (&s)[8], uint4& out_lo, uint4& out_hi) {
   const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w};
   const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w};
   uint32_t ol[4], oh[4];
@@ -49,40 +50,65 @@ __device__ __forceinline__ void rotate_chunk(const uint16_t* __restrict__ src,
     const float2 a = unpack2<BF16>(lw[j]);  // x_i, x_{i+1}
     const float2 b = unpack2<BF16>(hw[j]);  // x_{i+32}, x_{i+33}
     const int i0 = 2 * j, i1 = 2 * j + 1;
-    const float ya0 = fmaf(a.x, c[i0], -(b.x * s[i0]));
-    const float ya1 = fmaf(a.y, c[i1], -(b.y * s[i1]));
-    const float yb0 = fmaf(b.x, c[i0], a.x * s[i0]);
-    const float yb1 = fmaf(b.y, c[i1], a.y * s[i1]);
-    ol[j] = pack2<BF16>(ya0, ya1);
-    oh[j] = pack2<BF16>(yb0, yb1);
+    ol[j] = pack2<BF16>(fmaf(a.x, c[i0], -(b.x * s[i0])), fmaf(a.y, c[i1], -(b.y * s[i1])));
+    oh[j] = pack2<BF16>(fmaf(b.x, c[i0], a.x * s[i0]), fmaf(b.y, c[i1], a.y * s[i1]));
   }
-  st_v4(dst, make_uint4(ol[0], ol[1], ol[2], ol[3]));
-  st_v4(dst + 32, make_uint4(oh[0], oh[1], oh[2], oh[3]));
+  out_lo = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+  out_hi = make_uint4(oh[0], oh[1], oh[2], oh[3]);
 }
 
 template <bool BF16>
 __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constant__ RopeArgs a) {
+  // Let the dependent attention grid begin its prologue while this grid streams.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int r = threadIdx.x >> 2;  // position within the block
   const int g = threadIdx.x & 3;   // group of 8 pairs: pairs [8g, 8g + 8)
   const int l = blockIdx.x * kRopeRows + r;
   if (l >= a.L) return;
-  const int p = a.positions ? a.positions[l] : l;
-  const float pf = static_cast<float>(p);
-  float c[8], s[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float theta = __fmul_rn(pf, a.inv_freq[8 * g + i]);
-    sincosf(theta, &s[i], &c[i]);
-  }
   const long long first = static_cast<long long>(blockIdx.y) * a.planes_per_block;
   long long last = first + a.planes_per_block;
   if (last > a.planes) last = a.planes;
   const size_t row_stride = static_cast<size_t>(a.L) * kHeadDim;
-  size_t off = static_cast<size_t>(first) * row_stride + static_cast<size_t>(l) * kHeadDim + 8 * g;
-#pragma unroll 2
-  for (long long pl = first; pl < last; ++pl, off += row_stride) {
-    rotate_chunk<BF16>(a.q + off, a.q_out + off, c, s);
-    rotate_chunk<BF16>(a.k + off, a.k_out + off, c, s);
+  const size_t base = static_cast<size_t>(l) * kHeadDim + 8 * g;
+
+  float c[8], s[8];
+  bool have_cs = false;
+  for (long long p0 = first; p0 < last; p0 += kPlaneBatch) {
+    const int n = static_cast<int>(last - p0 < kPlaneBatch ? last - p0 : kPlaneBatch);
+    uint4 qlo[kPlaneBatch], qhi[kPlaneBatch], klo[kPlaneBatch], khi[kPlaneBatch];
+#pragma unroll
+    for (int i = 0; i < kPlaneBatch; ++i) {
+      if (i < n) {
+        const size_t off = static_cast<size_t>(p0 + i) * row_stride + base;
+        qlo[i] = ld_stream(a.q + off);
+        qhi[i] = ld_stream(a.q + off + 32);
+        klo[i] = ld_stream(a.k + off);
+        khi[i] = ld_stream(a.k + off + 32);
+      }
+    }
+    if (!have_cs) {
+      const int p = a.positions ? a.positions[l] : l;
+      const float pf = static_cast<float>(p);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float theta = __fmul_rn(pf, a.inv_freq[8 * g + i]);
+        sincosf(theta, &s[i], &c[i]);
+      }
+      have_cs = true;
+    }
+#pragma unroll
+    for (int i = 0; i < kPlaneBatch; ++i) {
+      if (i < n) {
+        const size_t off = static_cast<size_t>(p0 + i) * row_stride + base;
+        uint4 lo, hi;
+        rotate<BF16>(qlo[i], qhi[i], c, s, lo, hi);
+        st_v4(a.q_out + off, lo);
+        st_v4(a.q_out + off + 32, hi);
+        rotate<BF16>(klo[i], khi[i], c, s, lo, hi);
+        st_v4(a.k_out + off, lo);
+        st_v4(a.k_out + off + 32, hi);
+      }
+    }
   }
 }
 
@@ -91,6 +117,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constan
 cudaError_t rope_launch(const RopeArgs& a_in, bool bf16, int num_sms, cudaStream_t stream) {
   RopeArgs a = a_in;
   const long long bx = (a.L + kRopeRows - 1) / kRopeRows;
+  // Aim for about 8 resident blocks per SM; each block takes a slice of the planes.
   const long long want = 8LL * (num_sms > 0 ? num_sms : 148);
   long long by = (want + bx - 1) / bx;
   if (by > a.planes) by = a.planes;
