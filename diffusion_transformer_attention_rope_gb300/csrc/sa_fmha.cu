@@ -155,12 +155,12 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar.s_full(s), 1);
-      mbar_init(bar.p_full(s), kBlockM);
+      mbar_init(bar.p_full(s), 4);       // one elected arrival per softmax warp
       mbar_init(bar.pv_done(s), 1);
-      mbar_init(bar.s_free(s), kBlockM);
+      mbar_init(bar.s_free(s), 4);
       mbar_init(bar.o_full(s), 1);
       mbar_init(bar.drain(s), 1);
-      mbar_init(bar.turn(s), kBlockM);
+      mbar_init(bar.turn(s), 4);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -321,7 +321,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     // The two warpgroups take turns on the exponential phase (the exp unit is the scarce
     // resource): warpgroup 0 goes first, each hands the turn over when its exponentials are
     // issued, so one group's max / TMEM / barrier work overlaps the other's exponentials.
-    if (s == 1) mbar_arrive(bar.turn(0));
+    if (s == 1 && lane == 0) mbar_arrive(bar.turn(0));
 
     for (int it = 0; it < n_tiles; ++it) {
       ok = pwait(bar.s_full(s), it & 1, abort_flag, a.err, kErrSoftmax, tmo);
@@ -335,8 +335,10 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       tmem_wait_ld_128(sr);
       if (!DIFF) {
         // S_s is in registers: the issuer may write the next S_s into these columns now.
+        // Every lane has waited for its own load; after the warp sync one lane arrives.
         tc_fence_before();
-        mbar_arrive(bar.s_free(s));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.s_free(s));
       }
 
       const int key0 = (t_lo + it) * kBlockN;
@@ -407,7 +409,8 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         }
         tmem_st32(tmem + C::p_col(s) + lane_off + 32 * h, pk);
       }
-      mbar_arrive(bar.turn(1 - s));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.turn(1 - s));
       const float2 sum = fadd2(sum0, sum1);
       l_sum = fmaf(l_sum, f, sum.x + sum.y);
       if (rescale) {
@@ -430,7 +433,8 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar.p_full(s));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.p_full(s));
     }
 
     // ---------------------------------------------------------------- epilogue
