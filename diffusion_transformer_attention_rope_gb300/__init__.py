@@ -19,7 +19,7 @@ from typing import Optional, Sequence
 __all__ = [
     "SA_FP16", "SA_BF16", "SaAttnError", "library_path", "load_library",
     "sa_attn_create", "sa_attn_destroy", "sa_rope_attn_workspace_size", "sa_rope_attn",
-    "sa_rope_qk", "sa_attn_fwd", "sa_rope_attn_noalloc", "sa_attn_check", "sa_last_error", "sa_status_string", "RopeAttention",
+    "sa_rope_qk", "sa_attn_fwd", "sa_rope_attn_noalloc", "sa_attn_check", "sa_attn_set_timeout", "sa_last_error", "sa_status_string", "RopeAttention",
 ]
 
 SA_FP16 = 0
@@ -71,6 +71,8 @@ def load_library():
         lib.sa_rope_attn_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i,
                                              ctypes.POINTER(f), i, vp]
         lib.sa_rope_attn_noalloc.restype = i
+        lib.sa_attn_set_timeout.argtypes = [vp, ctypes.c_ulonglong]
+        lib.sa_attn_set_timeout.restype = i
         lib.sa_attn_check.argtypes = [vp]
         lib.sa_attn_check.restype = i
         lib.sa_last_error.argtypes = []
@@ -159,6 +161,11 @@ def sa_rope_attn_noalloc(handle: int, q: int, k: int, v: int, positions: Optiona
 
 
 SA_NOALLOC_SCRATCH_BYTES = 64 << 20
+
+
+def sa_attn_set_timeout(handle: int, timeout_ns: int) -> None:
+    """Limit of every pipeline wait in the attention kernel (default 1 s)."""
+    _check(load_library().sa_attn_set_timeout(ctypes.c_void_p(handle), int(timeout_ns)))
 
 
 def sa_attn_check(handle: int) -> None:

@@ -358,6 +358,14 @@ sa_status sa_rope_attn(sa_attn_t h, const void* q, const void* k, const void* v,
   return launch_attn(h, q_rot, k_rot, v, out, B, H, L, window, lambda, dtype, stream);
 }
 
+sa_status sa_attn_set_timeout(sa_attn_t h, unsigned long long timeout_ns) {
+  if (!h) return fail(SA_ERR_INVALID_ARG, "sa_attn_set_timeout: handle is NULL");
+  if (timeout_ns < 100)
+    return fail(SA_ERR_INVALID_ARG, "sa_attn_set_timeout: limit must be at least 100 ns");
+  h->timeout_ns = timeout_ns;
+  return ok();
+}
+
 sa_status sa_attn_check(sa_attn_t h) {
   if (!h) return fail(SA_ERR_INVALID_ARG, "sa_attn_check: handle is NULL");
   DeviceGuard guard(h->device);

@@ -145,6 +145,9 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
   }
   const int n_tiles = t_hi - t_lo + 1;
   const uint64_t tmo = a.timeout_ns;
+  // Waits for work already in flight (copies, MMAs) before shared memory / TMEM are released
+  // always get at least a second, whatever the pipeline limit is.
+  const uint64_t drain_tmo = tmo > 1000000000ull ? tmo : 1000000000ull;
 
   if (threadIdx.x == 0) {
     mbar_init(bar.q_full, 1);
@@ -217,15 +220,16 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         if (DIFF) tma_load_3d(v_dst + kTile, &tm_v, bar.v_full(st), 64, key0, bh);
         issued = it + 1;
       }
-      if (*abort_flag) {
-        // Let the copies already issued land before the CTA's shared memory goes away.
-        mbar_wait_limit(bar.q_full, 0, tmo);
+      {
+        // Let the copies already issued land before the CTA's shared memory goes away (after
+        // a normal run these phases have completed and the waits return at once).
+        mbar_wait_limit(bar.q_full, 0, drain_tmo);
         const int first = issued > C::NS ? issued - C::NS : 0;
         for (int it = first; it < issued; ++it) {
           const int st = it % C::NS;
           const uint32_t ph = (it / C::NS) & 1;
-          mbar_wait_limit(bar.k_full(st), ph, tmo);
-          mbar_wait_limit(bar.v_full(st), ph, tmo);
+          mbar_wait_limit(bar.k_full(st), ph, drain_tmo);
+          mbar_wait_limit(bar.v_full(st), ph, drain_tmo);
         }
       }
     }
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       }
       // No MMA of this issuer may still be running when TMEM is released.
       umma_commit(bar.drain(s));
-      mbar_wait_limit(bar.drain(s), 0, tmo);
+      mbar_wait_limit(bar.drain(s), 0, drain_tmo);
     }
     __syncwarp();
   }

@@ -196,6 +196,17 @@ SA_API sa_status sa_rope_attn_noalloc(sa_attn_t handle,
                                       sa_stream_t stream);
 
 /*
+ * Set the limit, in nanoseconds, of every pipeline wait inside the attention
+ * kernel launched with this handle (default 1 s; at least 100 ns).  A wait
+ * that runs out makes the kernel give up cleanly (it waits up to a second more
+ * for its own copies and MMAs in flight, frees its tensor memory and exits) and
+ * sets the error word that sa_attn_check reports as SA_ERR_DEVICE_TIMEOUT.
+ * Meant for tests of that failure path; it changes no result when no wait
+ * runs out.  Applies to launches enqueued after the call.
+ */
+SA_API sa_status sa_attn_set_timeout(sa_attn_t handle, unsigned long long timeout_ns);
+
+/*
  * Synchronize the handle's device, then read and clear its device error
  * word.  SA_OK if no kernel since the last check gave up on a wait;
  * SA_ERR_DEVICE_TIMEOUT otherwise (its output is then unspecified).

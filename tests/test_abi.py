@@ -97,3 +97,9 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(sa, "library_path", lambda: str(tmp_path / "libsa_attn.so"))
     with pytest.raises(sa.SaAttnError):
         sa.load_library()
+
+
+def test_set_timeout_null_handle_is_rejected():
+    with pytest.raises(sa.SaAttnError) as e:
+        sa.sa_attn_set_timeout(0, 1000)
+    assert e.value.status == 1
