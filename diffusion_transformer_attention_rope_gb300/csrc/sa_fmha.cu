@@ -48,7 +48,11 @@ struct Cfg {
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + NS * K_STAGE;
-  static constexpr int OFF_BAR = OFF_V + NS * V_STAGE;
+  // Differential only: P of both maps in shared memory (128 rows x 128 keys each, two
+  // 64-key swizzle atoms), the A operand of an SS P.V MMA.
+  static constexpr int P_BYTES = DIFF ? 4 * kTile : 0;
+  static constexpr int OFF_P = OFF_V + NS * V_STAGE;
+  static constexpr int OFF_BAR = OFF_P + P_BYTES;
   // barriers: q_full, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full[2],
   //           pv_done[2], s_free[2], o_full[2], drain[2], turn[2]
   static constexpr int NBAR = 1 + 3 * NS + 2 + 2 + 2 + 2 + 2 + 2 + 2;
@@ -57,7 +61,7 @@ struct Cfg {
   static constexpr int SMEM_USED = OFF_LSUM + 2 * kBlockM * 4;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;           // slack for 1 KB alignment
   __device__ static uint32_t s_col(int s) { return s * 128; }
-  __device__ static uint32_t p_col(int s) { return DIFF ? s * 128 : 256 + s * 64; }
+  __device__ static uint32_t p_col(int s) { return 256 + s * 64; }   // standard only
   __device__ static uint32_t o_col(int s) { return DIFF ? 256 + s * 128 : 384 + s * 64; }
 };
 
@@ -109,7 +113,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(smem);
-  const uint32_t sQ = sb + C::OFF_Q, sK = sb + C::OFF_K, sV = sb + C::OFF_V;
+  const uint32_t sQ = sb + C::OFF_Q, sK = sb + C::OFF_K, sV = sb + C::OFF_V, sP = sb + C::OFF_P;
 
   Barriers bar;
   bar.ns = C::NS;
@@ -248,6 +252,8 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       const uint64_t dk0 = smem_desc_sw128(sK + (DIFF ? s * kTile : 0), 16, 1024);
       const uint64_t dv0 = smem_desc_sw128(sV, kTile, 1024);
       const uint32_t d_s = tmem + C::s_col(s), d_o = tmem + C::o_col(s), a_p = tmem + C::p_col(s);
+      // differential: P_s in shared memory, two 64-key atoms of 16 KB (K-major, 128 B swizzle)
+      const uint64_t dp0 = smem_desc_sw128(sP + s * 2 * kTile, 16, 1024);
       auto issue_s = [&](int st) {
         const uint64_t dk = dk0 + static_cast<uint64_t>(st * (C::K_STAGE >> 4));
 #pragma unroll
@@ -257,8 +263,13 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       auto issue_pv = [&](int st, bool accumulate) {
         const uint64_t dv = dv0 + static_cast<uint64_t>(st * (C::V_STAGE >> 4));
 #pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk)
-          umma_ts(d_o, a_p + 8 * kk, dv + 128 * kk, idesc_o, (accumulate || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          if (DIFF)
+            umma_ss(d_o, dp0 + (kk >> 2) * (kTile >> 4) + 2 * (kk & 3), dv + 128 * kk, idesc_o,
+                    (accumulate || kk > 0) ? 1u : 0u);
+          else
+            umma_ts(d_o, a_p + 8 * kk, dv + 128 * kk, idesc_o, (accumulate || kk > 0) ? 1u : 0u);
+        }
       };
       const int eb = kErrMma;
       bool ok = pwait(bar.q_full, 0, abort_flag, a.err, eb, tmo) &&
@@ -274,9 +285,10 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         const bool last = it + 1 == n_tiles;
         const int st2 = (it + 1) % C::NS;
         const uint32_t ph2 = ((it + 1) / C::NS) & 1;
-        if (!DIFF && !last) {
-          // S(it+1) as soon as the softmax warps hold S(it) in registers (S and P have
-          // separate TMEM columns), overlapping their exponentials.
+        if (!last) {
+          // S(it+1) as soon as the softmax warps hold S(it) in registers (P lives apart from
+          // S: in TMEM for the standard kernel, in shared memory for the differential one),
+          // overlapping their exponentials.
           ok = pwait(bar.k_full(st2), ph2, abort_flag, a.err, eb, tmo) &&
                pwait(bar.s_free(s), it & 1, abort_flag, a.err, eb, tmo);
           if (!ok) break;
@@ -291,15 +303,6 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         issue_pv(st, it > 0);
         umma_commit(bar.pv_done(s));
         umma_commit(bar.kv_empty(st));
-        if (DIFF && !last) {
-          // P lives in the S columns here: the next S may only be written once P.V is done.
-          ok = pwait(bar.k_full(st2), ph2, abort_flag, a.err, eb, tmo) &&
-               pwait(bar.pv_done(s), it & 1, abort_flag, a.err, eb, tmo);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(st2);
-          umma_commit(bar.s_full(s));
-        }
         if (last) umma_commit(bar.o_full(s));
       }
       // No MMA of this issuer may still be running when TMEM is released.
@@ -337,7 +340,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       for (int cc = 0; cc < kBlockN / 32; ++cc)
         tmem_ld32_nowait(tmem + C::s_col(s) + lane_off + 32 * cc, sr + 32 * cc);
       tmem_wait_ld_128(sr);
-      if (!DIFF) {
+      {
         // S_s is in registers: the issuer may write the next S_s into these columns now.
         // Every lane has waited for its own load; after the warp sync one lane arrives.
         tc_fence_before();
@@ -384,7 +387,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       }
       const float mb = (m_use == -INFINITY) ? 0.0f : m_use * c;
       const float2 c2 = make_float2(c, c), nmb2 = make_float2(-mb, -mb);
-      if (!DIFF && it > 0) {
+      if (it > 0) {
         // P_s and O_s are still read / written by P_s V of the previous tile until it is done.
         ok = pwait(bar.pv_done(s), (it - 1) & 1, abort_flag, a.err, kErrSoftmax, tmo);
         ok = __all_sync(0xffffffffu, ok);
@@ -411,8 +414,19 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
           pk[j] = pack2<BF16>(p0.x, p0.y);
           pk[j + 1] = pack2<BF16>(p1.x, p1.y);
         }
-        tmem_st32(tmem + C::p_col(s) + lane_off + 32 * h, pk);
+        if (DIFF) {
+          // row r of the K-major, 128-byte-swizzled P tile: atom h (keys 64h..64h+63),
+          // 16-byte chunk kq lands at chunk kq ^ (r & 7)
+          const uint32_t row_base = sP + s * 2 * kTile + h * kTile + r * 128;
+#pragma unroll
+          for (int kq = 0; kq < 8; ++kq)
+            st_shared_v4(row_base + ((kq ^ (r & 7)) << 4), pk[4 * kq], pk[4 * kq + 1], pk[4 * kq + 2],
+                         pk[4 * kq + 3]);
+        } else {
+          tmem_st32(tmem + C::p_col(s) + lane_off + 32 * h, pk);
+        }
       }
+      if (DIFF) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.turn(1 - s));
       const float2 sum = fadd2(sum0, sum1);
