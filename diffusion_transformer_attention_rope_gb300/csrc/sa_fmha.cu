@@ -32,14 +32,18 @@ namespace sa {
 namespace {
 
 constexpr int kTile = kBlockM * kHeadDim * 2;  // bytes of one 128 x 64 fp16/bf16 tile (16 KB)
-constexpr int kTmaWarp = 8;
+constexpr int kTmaWarp = 8;   // TMA producer of Q and the K ring
 constexpr int kMmaWarp = 9;    // first MMA issuer (stream 0); also allocates TMEM
 constexpr int kMmaWarp1 = 10;  // second MMA issuer (stream 1)
+constexpr int kTmaWarpV = 11;  // TMA producer of the V ring
 constexpr uint32_t kTmemCols = 512;
 
 template <bool DIFF>
 struct Cfg {
-  static constexpr int NS = DIFF ? 2 : 3;                       // K/V ring stages
+  // K and V have rings of their own: a K stage is free again as soon as the S MMAs that read it
+  // are done, a V stage once the P.V MMAs are, so each K tile can be fetched well ahead of use.
+  static constexpr int NSK = DIFF ? 2 : 4;                      // K ring stages
+  static constexpr int NSV = DIFF ? 2 : 4;                      // V ring stages
   static constexpr int DV = DIFF ? 128 : 64;                    // value / output width
   static constexpr int ROWS = fmha_rows_per_cta(DIFF);          // query rows per CTA
   static constexpr int Q_BYTES = 2 * kTile;                     // two Q tiles (or maps)
@@ -47,15 +51,15 @@ struct Cfg {
   static constexpr int V_STAGE = DIFF ? 2 * kTile : kTile;      // V: 128 keys x DV
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
-  static constexpr int OFF_V = OFF_K + NS * K_STAGE;
+  static constexpr int OFF_V = OFF_K + NSK * K_STAGE;
   // Differential only: P of both maps in shared memory (128 rows x 128 keys each, two
   // 64-key swizzle atoms), the A operand of an SS P.V MMA.
   static constexpr int P_BYTES = DIFF ? 4 * kTile : 0;
-  static constexpr int OFF_P = OFF_V + NS * V_STAGE;
+  static constexpr int OFF_P = OFF_V + NSV * V_STAGE;
   static constexpr int OFF_BAR = OFF_P + P_BYTES;
-  // barriers: q_full, k_full[NS], v_full[NS], kv_empty[NS], s_full[2], p_full[2],
-  //           pv_done[2], s_free[2], o_full[2], drain[2], turn[2]
-  static constexpr int NBAR = 1 + 3 * NS + 2 + 2 + 2 + 2 + 2 + 2 + 2;
+  // barriers: q_full, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2],
+  //           p_full[2], pv_done[2], s_free[2], o_full[2], drain[2], turn[2][4]
+  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 2 + 2 + 2 + 2 + 2 + 2 + 8;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;           // tmem base, abort flag
   static constexpr int OFF_LSUM = OFF_MISC + 16;                // float [2][128]
   static constexpr int SMEM_USED = OFF_LSUM + 2 * kBlockM * 4;
@@ -70,19 +74,20 @@ static_assert(Cfg<true>::SMEM_ALLOC <= 227 * 1024, "smem budget");
 static_assert(Cfg<false>::SMEM_USED > 114 * 1024, "one CTA per SM keeps TMEM allocation uncontended");
 
 struct Barriers {
-  uint32_t q_full, k_full0, v_full0, kv_empty0, s_full0, p_full0, pv_done0, s_free0, o_full0, drain0,
-      turn0;
-  int ns;
+  uint32_t q_full, k_full0, k_empty0, v_full0, v_empty0, s_full0, p_full0, pv_done0, s_free0, o_full0,
+      drain0, turn0;
   __device__ uint32_t k_full(int i) const { return k_full0 + 8 * i; }
+  __device__ uint32_t k_empty(int i) const { return k_empty0 + 8 * i; }
   __device__ uint32_t v_full(int i) const { return v_full0 + 8 * i; }
-  __device__ uint32_t kv_empty(int i) const { return kv_empty0 + 8 * i; }
+  __device__ uint32_t v_empty(int i) const { return v_empty0 + 8 * i; }
   __device__ uint32_t s_full(int s) const { return s_full0 + 8 * s; }
   __device__ uint32_t p_full(int s) const { return p_full0 + 8 * s; }
   __device__ uint32_t pv_done(int s) const { return pv_done0 + 8 * s; }
   __device__ uint32_t s_free(int s) const { return s_free0 + 8 * s; }
   __device__ uint32_t o_full(int s) const { return o_full0 + 8 * s; }
   __device__ uint32_t drain(int s) const { return drain0 + 8 * s; }
-  __device__ uint32_t turn(int s) const { return turn0 + 8 * s; }
+  // exp-phase turn of warpgroup s on SM sub-partition q (warps q and q + 4 share it)
+  __device__ uint32_t turn(int s, int q) const { return turn0 + 8 * (4 * s + q); }
 };
 
 // Pipeline wait: bounded by the wall clock and by the CTA abort flag.  The first probes
@@ -116,12 +121,12 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
   const uint32_t sQ = sb + C::OFF_Q, sK = sb + C::OFF_K, sV = sb + C::OFF_V, sP = sb + C::OFF_P;
 
   Barriers bar;
-  bar.ns = C::NS;
   bar.q_full = sb + C::OFF_BAR;
   bar.k_full0 = bar.q_full + 8;
-  bar.v_full0 = bar.k_full0 + 8 * C::NS;
-  bar.kv_empty0 = bar.v_full0 + 8 * C::NS;
-  bar.s_full0 = bar.kv_empty0 + 8 * C::NS;
+  bar.k_empty0 = bar.k_full0 + 8 * C::NSK;
+  bar.v_full0 = bar.k_empty0 + 8 * C::NSK;
+  bar.v_empty0 = bar.v_full0 + 8 * C::NSV;
+  bar.s_full0 = bar.v_empty0 + 8 * C::NSV;
   bar.p_full0 = bar.s_full0 + 16;
   bar.pv_done0 = bar.p_full0 + 16;
   bar.s_free0 = bar.pv_done0 + 16;
@@ -155,10 +160,13 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar.q_full, 1);
-    for (int i = 0; i < C::NS; ++i) {
+    for (int i = 0; i < C::NSK; ++i) {
       mbar_init(bar.k_full(i), 1);
+      mbar_init(bar.k_empty(i), 2);    // one commit from each MMA issuer
+    }
+    for (int i = 0; i < C::NSV; ++i) {
       mbar_init(bar.v_full(i), 1);
-      mbar_init(bar.kv_empty(i), 2);   // one commit from each MMA issuer
+      mbar_init(bar.v_empty(i), 2);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(bar.s_full(s), 1);
@@ -167,7 +175,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       mbar_init(bar.s_free(s), 4);
       mbar_init(bar.o_full(s), 1);
       mbar_init(bar.drain(s), 1);
-      mbar_init(bar.turn(s), 4);
+      for (int q = 0; q < 4; ++q) mbar_init(bar.turn(s, q), 1);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -179,62 +187,68 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
   if (warp == kTmaWarp && lane == 0) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
   }
+  if (warp == kTmaWarpV && lane == 0) tma_prefetch_desc(&tm_v);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
   if (warp >= 8) {
-  // Control warpgroup (TMA producer, two MMA issuers, one spare warp): few registers.
+  // Control warpgroup (two TMA producers, two MMA issuers): few registers.
   regs_dec<kControlRegs>();
-  if (warp == kTmaWarp) {
-    // ------------------------------------------------------------------ TMA producer
+  if (warp == kTmaWarp || warp == kTmaWarpV) {
+    // ------------------------------------------------------------------ TMA producers
+    // Warp 8 loads the Q tiles once and then runs the K ring; warp 11 runs the V ring.
+    const bool is_k = warp == kTmaWarp;
     if (lane == 0) {
-      const int plane_q = DIFF ? 2 * bh : bh;
-      // This grid may have been started early (programmatic dependent launch) while the RoPE
-      // pass that writes q', k' is still running: wait for it before the first load.
+      // This grid may have been started early (programmatic dependent launch) while the kernel
+      // before it on the stream (the RoPE pass, which writes q', k') is still running: wait for
+      // it before the first load.
       asm volatile("griddepcontrol.wait;" ::: "memory");
-      mbar_arrive_expect_tx(bar.q_full, C::Q_BYTES);
-      if (DIFF) {
-        tma_load_3d(sQ, &tm_q, bar.q_full, 0, q0, plane_q);
-        tma_load_3d(sQ + kTile, &tm_q, bar.q_full, 0, q0, plane_q + 1);
-      } else {
-        tma_load_3d(sQ, &tm_q, bar.q_full, 0, q0, plane_q);
-        tma_load_3d(sQ + kTile, &tm_q, bar.q_full, 0, q0 + kBlockM, plane_q);
+      const int ns = is_k ? C::NSK : C::NSV;
+      if (is_k) {
+        const int plane_q = DIFF ? 2 * bh : bh;
+        mbar_arrive_expect_tx(bar.q_full, C::Q_BYTES);
+        if (DIFF) {
+          tma_load_3d(sQ, &tm_q, bar.q_full, 0, q0, plane_q);
+          tma_load_3d(sQ + kTile, &tm_q, bar.q_full, 0, q0, plane_q + 1);
+        } else {
+          tma_load_3d(sQ, &tm_q, bar.q_full, 0, q0, plane_q);
+          tma_load_3d(sQ + kTile, &tm_q, bar.q_full, 0, q0 + kBlockM, plane_q);
+        }
       }
       int issued = 0;
       for (int it = 0; it < n_tiles; ++it) {
-        const int st = it % C::NS;
-        const uint32_t ph = (it / C::NS) & 1;
-        if (!pwait(bar.kv_empty(st), ph ^ 1, abort_flag, a.err, kErrProducer, tmo)) break;
+        const int st = it % ns;
+        const uint32_t ph = (it / ns) & 1;
         const int key0 = (t_lo + it) * kBlockN;
-        const uint32_t k_dst = sK + st * C::K_STAGE;
-        const uint32_t v_dst = sV + st * C::V_STAGE;
-        mbar_arrive_expect_tx(bar.k_full(st), C::K_STAGE);
-        if (DIFF) {
-          tma_load_3d(k_dst, &tm_k, bar.k_full(st), 0, key0, 2 * bh);
-          tma_load_3d(k_dst + kTile, &tm_k, bar.k_full(st), 0, key0, 2 * bh + 1);
+        if (is_k) {
+          if (!pwait(bar.k_empty(st), ph ^ 1, abort_flag, a.err, kErrProducer, tmo)) break;
+          const uint32_t k_dst = sK + st * C::K_STAGE;
+          mbar_arrive_expect_tx(bar.k_full(st), C::K_STAGE);
+          if (DIFF) {
+            tma_load_3d(k_dst, &tm_k, bar.k_full(st), 0, key0, 2 * bh);
+            tma_load_3d(k_dst + kTile, &tm_k, bar.k_full(st), 0, key0, 2 * bh + 1);
+          } else {
+            tma_load_3d(k_dst, &tm_k, bar.k_full(st), 0, key0, bh);
+          }
         } else {
-          tma_load_3d(k_dst, &tm_k, bar.k_full(st), 0, key0, bh);
+          if (!pwait(bar.v_empty(st), ph ^ 1, abort_flag, a.err, kErrProducer, tmo)) break;
+          const uint32_t v_dst = sV + st * C::V_STAGE;
+          mbar_arrive_expect_tx(bar.v_full(st), C::V_STAGE);
+          tma_load_3d(v_dst, &tm_v, bar.v_full(st), 0, key0, bh);
+          if (DIFF) tma_load_3d(v_dst + kTile, &tm_v, bar.v_full(st), 64, key0, bh);
         }
-        mbar_arrive_expect_tx(bar.v_full(st), C::V_STAGE);
-        tma_load_3d(v_dst, &tm_v, bar.v_full(st), 0, key0, bh);
-        if (DIFF) tma_load_3d(v_dst + kTile, &tm_v, bar.v_full(st), 64, key0, bh);
         issued = it + 1;
       }
       {
         // Let the copies already issued land before the CTA's shared memory goes away (after
         // a normal run these phases have completed and the waits return at once).
-        mbar_wait_limit(bar.q_full, 0, drain_tmo);
-        const int first = issued > C::NS ? issued - C::NS : 0;
-        for (int it = first; it < issued; ++it) {
-          const int st = it % C::NS;
-          const uint32_t ph = (it / C::NS) & 1;
-          mbar_wait_limit(bar.k_full(st), ph, drain_tmo);
-          mbar_wait_limit(bar.v_full(st), ph, drain_tmo);
-        }
+        if (is_k) mbar_wait_limit(bar.q_full, 0, drain_tmo);
+        const int first = issued > ns ? issued - ns : 0;
+        for (int it = first; it < issued; ++it)
+          mbar_wait_limit(is_k ? bar.k_full(it % ns) : bar.v_full(it % ns), (it / ns) & 1, drain_tmo);
       }
     }
     __syncwarp();
@@ -278,13 +292,14 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         tc_fence_after();
         issue_s(0);
         umma_commit(bar.s_full(s));
+        umma_commit(bar.k_empty(0));
       }
       for (int it = 0; ok && it < n_tiles; ++it) {
-        const int st = it % C::NS;
-        const uint32_t ph = (it / C::NS) & 1;
+        const int sv = it % C::NSV;
+        const uint32_t phv = (it / C::NSV) & 1;
         const bool last = it + 1 == n_tiles;
-        const int st2 = (it + 1) % C::NS;
-        const uint32_t ph2 = ((it + 1) / C::NS) & 1;
+        const int st2 = (it + 1) % C::NSK;
+        const uint32_t ph2 = ((it + 1) / C::NSK) & 1;
         if (!last) {
           // S(it+1) as soon as the softmax warps hold S(it) in registers (P lives apart from
           // S: in TMEM for the standard kernel, in shared memory for the differential one),
@@ -295,14 +310,15 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
           tc_fence_after();
           issue_s(st2);
           umma_commit(bar.s_full(s));
+          umma_commit(bar.k_empty(st2));
         }
         ok = pwait(bar.p_full(s), it & 1, abort_flag, a.err, eb, tmo) &&
-             pwait(bar.v_full(st), ph, abort_flag, a.err, eb, tmo);
+             pwait(bar.v_full(sv), phv, abort_flag, a.err, eb, tmo);
         if (!ok) break;
         tc_fence_after();
-        issue_pv(st, it > 0);
+        issue_pv(sv, it > 0);
         umma_commit(bar.pv_done(s));
-        umma_commit(bar.kv_empty(st));
+        umma_commit(bar.v_empty(sv));
         if (last) umma_commit(bar.o_full(s));
       }
       // No MMA of this issuer may still be running when TMEM is released.
@@ -326,9 +342,11 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     float l_sum = 0.0f;
     bool ok = true;
     // The two warpgroups take turns on the exponential phase (the exp unit is the scarce
-    // resource): warpgroup 0 goes first, each hands the turn over when its exponentials are
-    // issued, so one group's max / TMEM / barrier work overlaps the other's exponentials.
-    if (s == 1 && lane == 0) mbar_arrive(bar.turn(0));
+    // resource), pairwise per SM sub-partition (warp q of group 0 with warp q of group 1,
+    // which share one): group 0 goes first, each warp hands the turn to its partner when its
+    // exponentials are issued, so one warp's max / TMEM / barrier work overlaps the other's
+    // exponentials without waiting for the slowest warp of the other group.
+    if (s == 1 && lane == 0) mbar_arrive(bar.turn(0, quarter));
 
     for (int it = 0; it < n_tiles; ++it) {
       ok = pwait(bar.s_full(s), it & 1, abort_flag, a.err, kErrSoftmax, tmo);
@@ -394,7 +412,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         if (!ok) break;
         tc_fence_after();
       }
-      ok = pwait(bar.turn(s), it & 1, abort_flag, a.err, kErrSoftmax, tmo);
+      ok = pwait(bar.turn(s, quarter), it & 1, abort_flag, a.err, kErrSoftmax, tmo);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       float2 sum0 = make_float2(0.0f, 0.0f), sum1 = make_float2(0.0f, 0.0f);
@@ -428,7 +446,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       }
       if (DIFF) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar.turn(1 - s));
+      if (lane == 0) mbar_arrive(bar.turn(1 - s, quarter));
       const float2 sum = fadd2(sum0, sum1);
       l_sum = fmaf(l_sum, f, sum.x + sum.y);
       if (rescale) {
