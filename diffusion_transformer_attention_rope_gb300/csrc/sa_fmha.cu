@@ -25,6 +25,8 @@
 // masks are applied only on tiles that are not entirely inside every row's window.
 // Every wait is bounded: on timeout a warp sets the device error word and a CTA-wide abort
 // flag, waits (bounded) for its own copies / MMAs in flight, and the CTA frees TMEM and exits.
+#include <type_traits>
+
 #include "sa_kernels.h"
 #include "sa_ptx.cuh"
 
@@ -90,16 +92,17 @@ struct Barriers {
   __device__ uint32_t turn(int s, int q) const { return turn0 + 8 * (4 * s + q); }
 };
 
-// Pipeline wait: bounded by the wall clock and by the CTA abort flag.  The first probes
-// skip the abort / clock checks (most waits end within a few probes).
+// Pipeline wait: bounded by the wall clock and by the CTA abort flag.  Most waits end at the
+// first probe, before the clock is ever read.  A suspending probe returns only once the phase
+// completes or after a limit of about a microsecond or more, so with bounds that short
+// (failure tests) the wait polls instead and reads the clock after each probe.
 __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                       int* err, int err_bit, uint64_t timeout_ns) {
-#pragma unroll 1
-  for (int i = 0; i < 4; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+  const bool poll = timeout_ns < 4000u;
+  if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
     if (globaltimer_ns() - t0 > timeout_ns) {
       *abort_flag = 1;
@@ -107,6 +110,12 @@ __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, volatile in
       return false;
     }
   }
+}
+
+// Warp-uniform pipeline wait: every lane waits, and the warp agrees on the outcome.
+__device__ __forceinline__ bool pwait_w(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                        int* err, int err_bit, uint64_t timeout_ns) {
+  return __all_sync(0xffffffffu, pwait(bar, parity, abort_flag, err, err_bit, timeout_ns));
 }
 
 template <bool DIFF, bool BF16>
@@ -195,69 +204,74 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp >= 8) {
-  // Control warpgroup (two TMA producers, two MMA issuers): few registers.
+  // Control warpgroup: K producer, the two MMA issuers, V producer; few registers.  These warps
+  // run warp-uniform code: every lane waits on the barriers and one lane, elected inside each
+  // issuing instruction, issues the copies / MMAs / commits (the operands stay warp-uniform,
+  // which keeps the issue of each tcgen05.mma short).
   regs_dec<kControlRegs>();
-  if (warp == kTmaWarp || warp == kTmaWarpV) {
-    // ------------------------------------------------------------------ TMA producers
-    // Warp 8 loads the Q tiles once and then runs the K ring; warp 11 runs the V ring.
-    const bool is_k = warp == kTmaWarp;
-    if (lane == 0) {
-      // This grid may have been started early (programmatic dependent launch) while the kernel
-      // before it on the stream (the RoPE pass, which writes q', k') is still running: wait for
-      // it before the first load.
-      asm volatile("griddepcontrol.wait;" ::: "memory");
-      const int ns = is_k ? C::NSK : C::NSV;
-      if (is_k) {
-        const int plane_q = DIFF ? 2 * bh : bh;
-        mbar_arrive_expect_tx(bar.q_full, C::Q_BYTES);
-        if (DIFF) {
-          tma_load_3d(sQ, &tm_q, bar.q_full, 0, q0, plane_q);
-          tma_load_3d(sQ + kTile, &tm_q, bar.q_full, 0, q0, plane_q + 1);
-        } else {
-          tma_load_3d(sQ, &tm_q, bar.q_full, 0, q0, plane_q);
-          tma_load_3d(sQ + kTile, &tm_q, bar.q_full, 0, q0 + kBlockM, plane_q);
-        }
-      }
-      int issued = 0;
-      for (int it = 0; it < n_tiles; ++it) {
-        const int st = it % ns;
-        const uint32_t ph = (it / ns) & 1;
-        const int key0 = (t_lo + it) * kBlockN;
-        if (is_k) {
-          if (!pwait(bar.k_empty(st), ph ^ 1, abort_flag, a.err, kErrProducer, tmo)) break;
-          const uint32_t k_dst = sK + st * C::K_STAGE;
-          mbar_arrive_expect_tx(bar.k_full(st), C::K_STAGE);
-          if (DIFF) {
-            tma_load_3d(k_dst, &tm_k, bar.k_full(st), 0, key0, 2 * bh);
-            tma_load_3d(k_dst + kTile, &tm_k, bar.k_full(st), 0, key0, 2 * bh + 1);
-          } else {
-            tma_load_3d(k_dst, &tm_k, bar.k_full(st), 0, key0, bh);
-          }
-        } else {
-          if (!pwait(bar.v_empty(st), ph ^ 1, abort_flag, a.err, kErrProducer, tmo)) break;
-          const uint32_t v_dst = sV + st * C::V_STAGE;
-          mbar_arrive_expect_tx(bar.v_full(st), C::V_STAGE);
-          tma_load_3d(v_dst, &tm_v, bar.v_full(st), 0, key0, bh);
-          if (DIFF) tma_load_3d(v_dst + kTile, &tm_v, bar.v_full(st), 64, key0, bh);
-        }
-        issued = it + 1;
-      }
-      {
-        // Let the copies already issued land before the CTA's shared memory goes away (after
-        // a normal run these phases have completed and the waits return at once).
-        if (is_k) mbar_wait_limit(bar.q_full, 0, drain_tmo);
-        const int first = issued > ns ? issued - ns : 0;
-        for (int it = first; it < issued; ++it)
-          mbar_wait_limit(is_k ? bar.k_full(it % ns) : bar.v_full(it % ns), (it / ns) & 1, drain_tmo);
-      }
+  if (warp == kTmaWarp) {
+    // ------------------------------------------------------------------ K producer (+ Q)
+    // This grid may have been started early (programmatic dependent launch) while the kernel
+    // before it on the stream (the RoPE pass, which writes q', k') is still running: wait for
+    // it before the first load.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int plane_q = DIFF ? 2 * bh : bh;
+    mbar_arrive_expect_tx_w(bar.q_full, C::Q_BYTES);
+    if (DIFF) {
+      tma_load_3d_w(sQ, &tm_q, bar.q_full, 0, q0, plane_q);
+      tma_load_3d_w(sQ + kTile, &tm_q, bar.q_full, 0, q0, plane_q + 1);
+    } else {
+      tma_load_3d_w(sQ, &tm_q, bar.q_full, 0, q0, plane_q);
+      tma_load_3d_w(sQ + kTile, &tm_q, bar.q_full, 0, q0 + kBlockM, plane_q);
     }
+    int issued = 0;
+    for (int it = 0; it < n_tiles; ++it) {
+      const int st = it % C::NSK;
+      if (!pwait_w(bar.k_empty(st), ((it / C::NSK) & 1) ^ 1, abort_flag, a.err, kErrProducer, tmo))
+        break;
+      const int key0 = (t_lo + it) * kBlockN;
+      const uint32_t k_dst = sK + st * C::K_STAGE;
+      mbar_arrive_expect_tx_w(bar.k_full(st), C::K_STAGE);
+      if (DIFF) {
+        tma_load_3d_w(k_dst, &tm_k, bar.k_full(st), 0, key0, 2 * bh);
+        tma_load_3d_w(k_dst + kTile, &tm_k, bar.k_full(st), 0, key0, 2 * bh + 1);
+      } else {
+        tma_load_3d_w(k_dst, &tm_k, bar.k_full(st), 0, key0, bh);
+      }
+      issued = it + 1;
+    }
+    // Let the copies already issued land before the CTA's shared memory goes away (after a
+    // normal run these phases have completed and the waits return at once).
+    mbar_wait_limit(bar.q_full, 0, drain_tmo);
+    for (int it = issued > C::NSK ? issued - C::NSK : 0; it < issued; ++it)
+      mbar_wait_limit(bar.k_full(it % C::NSK), (it / C::NSK) & 1, drain_tmo);
     __syncwarp();
-  } else if (warp == kMmaWarp || warp == kMmaWarp1) {
+  } else if (warp == kTmaWarpV) {
+    // ------------------------------------------------------------------ V producer
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    int issued = 0;
+    for (int it = 0; it < n_tiles; ++it) {
+      const int st = it % C::NSV;
+      if (!pwait_w(bar.v_empty(st), ((it / C::NSV) & 1) ^ 1, abort_flag, a.err, kErrProducer, tmo))
+        break;
+      const int key0 = (t_lo + it) * kBlockN;
+      const uint32_t v_dst = sV + st * C::V_STAGE;
+      mbar_arrive_expect_tx_w(bar.v_full(st), C::V_STAGE);
+      tma_load_3d_w(v_dst, &tm_v, bar.v_full(st), 0, key0, bh);
+      if (DIFF) tma_load_3d_w(v_dst + kTile, &tm_v, bar.v_full(st), 64, key0, bh);
+      issued = it + 1;
+    }
+    for (int it = issued > C::NSV ? issued - C::NSV : 0; it < issued; ++it)
+      mbar_wait_limit(bar.v_full(it % C::NSV), (it / C::NSV) & 1, drain_tmo);
+    __syncwarp();
+  } else {
     // ------------------------------------------------------------------ MMA issuers
-    // One issuing thread per stream s (query tile s, or map s): each runs its own
-    // S -> softmax -> P.V chain so the two chains never wait on each other's issue.
-    const int s = warp - kMmaWarp;
-    if (lane == 0) {
+    // One issuing warp per stream s (query tile s, or map s).  After the prologue each issues,
+    // per tile, one block: P.V_s(i) as soon as P_s(i) is ready, then S_s(i + 2) (it overwrites
+    // S_s(i + 1), which the softmax warps load right after P_s(i)).  The stream index is a
+    // compile-time constant in each instance so that every operand is warp-uniform.
+    auto issuer = [&](auto stream) {
+      constexpr int s = decltype(stream)::value;
       constexpr uint32_t idesc_s = make_idesc_f16(kBlockM, kBlockN, BF16, false);
       constexpr uint32_t idesc_o = make_idesc_f16(kBlockM, C::DV, BF16, true);
       // Descriptors computed once; the 14-bit address field advances by constant steps
@@ -268,64 +282,67 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       const uint32_t d_s = tmem + C::s_col(s), d_o = tmem + C::o_col(s), a_p = tmem + C::p_col(s);
       // differential: P_s in shared memory, two 64-key atoms of 16 KB (K-major, 128 B swizzle)
       const uint64_t dp0 = smem_desc_sw128(sP + s * 2 * kTile, 16, 1024);
-      auto issue_s = [&](int st) {
+      constexpr int eb = kErrMma;
+      auto wait_k = [&](int it) {
+        return pwait_w(bar.k_full(it % C::NSK), (it / C::NSK) & 1, abort_flag, a.err, eb, tmo);
+      };
+      auto issue_s = [&](int it) {
+        const int st = it % C::NSK;
         const uint64_t dk = dk0 + static_cast<uint64_t>(st * (C::K_STAGE >> 4));
 #pragma unroll
         for (int kk = 0; kk < kHeadDim / 16; ++kk)
-          umma_ss(d_s, dq + 2 * kk, dk + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
+          umma_ss_w(d_s, dq + 2 * kk, dk + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
+        umma_commit_w(bar.s_full(s));
+        umma_commit_w(bar.k_empty(st));
       };
-      auto issue_pv = [&](int st, bool accumulate) {
-        const uint64_t dv = dv0 + static_cast<uint64_t>(st * (C::V_STAGE >> 4));
-#pragma unroll
-        for (int kk = 0; kk < kBlockN / 16; ++kk) {
-          if (DIFF)
-            umma_ss(d_o, dp0 + (kk >> 2) * (kTile >> 4) + 2 * (kk & 3), dv + 128 * kk, idesc_o,
-                    (accumulate || kk > 0) ? 1u : 0u);
-          else
-            umma_ts(d_o, a_p + 8 * kk, dv + 128 * kk, idesc_o, (accumulate || kk > 0) ? 1u : 0u);
-        }
-      };
-      const int eb = kErrMma;
-      bool ok = pwait(bar.q_full, 0, abort_flag, a.err, eb, tmo) &&
-                pwait(bar.k_full(0), 0, abort_flag, a.err, eb, tmo);
+      bool ok = pwait_w(bar.q_full, 0, abort_flag, a.err, eb, tmo) && wait_k(0);
       if (ok) {
         tc_fence_after();
         issue_s(0);
-        umma_commit(bar.s_full(s));
-        umma_commit(bar.k_empty(0));
+      }
+      if (ok && n_tiles > 1) {
+        // S_s(1) once the softmax warps hold S_s(0) in registers
+        ok = pwait_w(bar.s_free(s), 0, abort_flag, a.err, eb, tmo) && wait_k(1);
+        if (ok) {
+          tc_fence_after();
+          issue_s(1);
+        }
       }
       for (int it = 0; ok && it < n_tiles; ++it) {
         const int sv = it % C::NSV;
-        const uint32_t phv = (it / C::NSV) & 1;
-        const bool last = it + 1 == n_tiles;
-        const int st2 = (it + 1) % C::NSK;
-        const uint32_t ph2 = ((it + 1) / C::NSK) & 1;
-        if (!last) {
-          // S(it+1) as soon as the softmax warps hold S(it) in registers (P lives apart from
-          // S: in TMEM for the standard kernel, in shared memory for the differential one),
-          // overlapping their exponentials.
-          ok = pwait(bar.k_full(st2), ph2, abort_flag, a.err, eb, tmo) &&
-               pwait(bar.s_free(s), it & 1, abort_flag, a.err, eb, tmo);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(st2);
-          umma_commit(bar.s_full(s));
-          umma_commit(bar.k_empty(st2));
-        }
-        ok = pwait(bar.p_full(s), it & 1, abort_flag, a.err, eb, tmo) &&
-             pwait(bar.v_full(sv), phv, abort_flag, a.err, eb, tmo);
+        // V(it) arrived long ago in the steady state: check it before waiting for P
+        ok = pwait_w(bar.v_full(sv), (it / C::NSV) & 1, abort_flag, a.err, eb, tmo) &&
+             pwait_w(bar.p_full(s), it & 1, abort_flag, a.err, eb, tmo);
         if (!ok) break;
         tc_fence_after();
-        issue_pv(sv, it > 0);
-        umma_commit(bar.pv_done(s));
-        umma_commit(bar.v_empty(sv));
-        if (last) umma_commit(bar.o_full(s));
+        const uint64_t dv = dv0 + static_cast<uint64_t>(sv * (C::V_STAGE >> 4));
+#pragma unroll
+        for (int kk = 0; kk < kBlockN / 16; ++kk) {
+          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+          if (DIFF)
+            umma_ss_w(d_o, dp0 + (kk >> 2) * (kTile >> 4) + 2 * (kk & 3), dv + 128 * kk, idesc_o, acc);
+          else
+            umma_ts_w(d_o, a_p + 8 * kk, dv + 128 * kk, idesc_o, acc);
+        }
+        umma_commit_w(bar.pv_done(s));
+        umma_commit_w(bar.v_empty(sv));
+        if (it + 1 == n_tiles) umma_commit_w(bar.o_full(s));
+        if (it + 2 < n_tiles) {
+          ok = pwait_w(bar.s_free(s), (it + 1) & 1, abort_flag, a.err, eb, tmo) && wait_k(it + 2);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(it + 2);
+        }
       }
       // No MMA of this issuer may still be running when TMEM is released.
-      umma_commit(bar.drain(s));
+      umma_commit_w(bar.drain(s));
       mbar_wait_limit(bar.drain(s), 0, drain_tmo);
-    }
-    __syncwarp();
+      __syncwarp();
+    };
+    if (warp == kMmaWarp)
+      issuer(std::integral_constant<int, 0>{});
+    else
+      issuer(std::integral_constant<int, 1>{});
   }
   } else {
     // ------------------------------------------------------------------ softmax warpgroups
