@@ -92,14 +92,15 @@ struct Barriers {
   __device__ uint32_t turn(int s, int q) const { return turn0 + 8 * (4 * s + q); }
 };
 
-// Pipeline wait: bounded by the wall clock and by the CTA abort flag.  Most waits end at the
-// first probe, before the clock is ever read.  A suspending probe returns only once the phase
-// completes or after a limit of about a microsecond or more, so with bounds that short
-// (failure tests) the wait polls instead and reads the clock after each probe.
+// Pipeline wait: bounded by the wall clock and by the CTA abort flag.  The first probe is a
+// non-blocking test (several times cheaper than a suspending probe when the phase has already
+// completed, the common case); the clock is read only after it fails.  A suspending probe
+// returns only once the phase completes or after a limit of about a microsecond or more, so
+// with bounds that short (failure tests) the wait keeps polling and reads the clock each time.
 __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                       int* err, int err_bit, uint64_t timeout_ns) {
+  if (mbar_test_wait(bar, parity)) return true;
   const bool poll = timeout_ns < 4000u;
-  if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   while (true) {
     if (poll ? mbar_test_wait(bar, parity) : mbar_try_wait(bar, parity)) return true;
