@@ -423,6 +423,29 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       }
       const float mb = (m_use == -INFINITY) ? 0.0f : m_use * c;
       const float2 c2 = make_float2(c, c), nmb2 = make_float2(-mb, -mb);
+      ok = pwait(bar.turn(s, quarter), it & 1, abort_flag, a.err, kErrSoftmax, tmo);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      // Exponentials of the whole row into registers (packed pairs): P_s(it) is computed
+      // before the wait for P_s V(it - 1), which has the whole exponential phase to finish.
+      float2 sum0 = make_float2(0.0f, 0.0f), sum1 = make_float2(0.0f, 0.0f);
+      uint32_t pk[kBlockN / 2];
+#pragma unroll
+      for (int j = 0; j < kBlockN / 2; j += 2) {
+        const int e = 2 * j;
+        const float2 x0 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nmb2);
+        const float2 x1 = ffma2(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nmb2);
+        const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+        const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+        sum0 = fadd2(sum0, p0);
+        sum1 = fadd2(sum1, p1);
+        pk[j] = pack2<BF16>(p0.x, p0.y);
+        pk[j + 1] = pack2<BF16>(p1.x, p1.y);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.turn(1 - s, quarter));
+      const float2 sum = fadd2(sum0, sum1);
+      l_sum = fmaf(l_sum, f, sum.x + sum.y);
       if (it > 0) {
         // P_s and O_s are still read / written by P_s V of the previous tile until it is done.
         ok = pwait(bar.pv_done(s), (it - 1) & 1, abort_flag, a.err, kErrSoftmax, tmo);
@@ -430,43 +453,22 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         if (!ok) break;
         tc_fence_after();
       }
-      ok = pwait(bar.turn(s, quarter), it & 1, abort_flag, a.err, kErrSoftmax, tmo);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      float2 sum0 = make_float2(0.0f, 0.0f), sum1 = make_float2(0.0f, 0.0f);
+      if (DIFF) {
+        // row r of the K-major, 128-byte-swizzled P tile: atom h (keys 64h..64h+63),
+        // 16-byte chunk kq lands at chunk kq ^ (r & 7)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        // exponentials of columns [64 h, 64 h + 64) -> 32 packed pairs -> TMEM
-        uint32_t pk[32];
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const int e = 64 * h + 2 * j;
-          const float2 x0 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nmb2);
-          const float2 x1 = ffma2(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nmb2);
-          const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
-          const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
-          sum0 = fadd2(sum0, p0);
-          sum1 = fadd2(sum1, p1);
-          pk[j] = pack2<BF16>(p0.x, p0.y);
-          pk[j + 1] = pack2<BF16>(p1.x, p1.y);
-        }
-        if (DIFF) {
-          // row r of the K-major, 128-byte-swizzled P tile: atom h (keys 64h..64h+63),
-          // 16-byte chunk kq lands at chunk kq ^ (r & 7)
+        for (int h = 0; h < 2; ++h) {
           const uint32_t row_base = sP + s * 2 * kTile + h * kTile + r * 128;
 #pragma unroll
           for (int kq = 0; kq < 8; ++kq)
-            st_shared_v4(row_base + ((kq ^ (r & 7)) << 4), pk[4 * kq], pk[4 * kq + 1], pk[4 * kq + 2],
-                         pk[4 * kq + 3]);
-        } else {
-          tmem_st32(tmem + C::p_col(s) + lane_off + 32 * h, pk);
+            st_shared_v4(row_base + ((kq ^ (r & 7)) << 4), pk[32 * h + 4 * kq], pk[32 * h + 4 * kq + 1],
+                         pk[32 * h + 4 * kq + 2], pk[32 * h + 4 * kq + 3]);
         }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      } else {
+        tmem_st32(tmem + C::p_col(s) + lane_off, pk);
+        tmem_st32(tmem + C::p_col(s) + lane_off + 32, pk + 32);
       }
-      if (DIFF) asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar.turn(1 - s, quarter));
-      const float2 sum = fadd2(sum0, sum1);
-      l_sum = fmaf(l_sum, f, sum.x + sum.y);
       if (rescale) {
         // O_s is stable here: P_s V of the previous tile has finished and P_s V of this
         // tile waits for the arrive below.

@@ -15,7 +15,7 @@ constexpr int kHeadDim = 64;          // d of q and k (the only supported value)
 constexpr int kBlockM = 128;          // query rows per tile = TMEM lanes
 constexpr int kBlockN = 128;          // keys per K/V tile
 constexpr int kMaxDiffHeads = 128;    // lambda is carried by value in the kernel arguments
-constexpr int kFmhaThreads = 384;     // 3 warpgroups: 2 softmax + (TMA, 2 MMA issuers, 1 spare)
+constexpr int kFmhaThreads = 384;     // 3 warpgroups: 2 softmax + (2 TMA producers, 2 MMA issuers)
 // Register split (setmaxnreg): the kernel is launched with kFmhaLaunchRegs per thread; the
 // softmax warpgroups grow to kSoftmaxRegs, the TMA/MMA warpgroup shrinks to kControlRegs.
 // The split must not exceed the launch total: 2*128*224 + 128*56 = 384*168.
