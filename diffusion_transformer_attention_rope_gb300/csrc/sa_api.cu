@@ -16,6 +16,7 @@
 struct sa_attn_s {
   int device;
   int num_sms;
+  int rope_blocks_per_sm;
   float rope_base;
   float inv_freq[sa::kHeadDim / 2];
   int* d_err;  // 4-byte device error word
@@ -130,7 +131,8 @@ sa_status launch_rope(const sa_attn_s* h, const void* q, const void* k, const in
   ra.L = L;
   ra.planes_per_block = 1;
   std::memcpy(ra.inv_freq, h->inv_freq, sizeof(ra.inv_freq));
-  cudaError_t e = sa::rope_launch(ra, dtype == SA_BF16, h->num_sms, reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = sa::rope_launch(ra, dtype == SA_BF16, h->num_sms, h->rope_blocks_per_sm,
+                                  reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(SA_ERR_CUDA, "RoPE launch: %s", cudaGetErrorString(e));
   return ok();
 }
@@ -264,6 +266,7 @@ sa_status sa_attn_create(sa_attn_t* handle, int device, float rope_base) {
     delete h;
     return fail(SA_ERR_CUDA, "sa_attn_create: cudaMalloc: %s", cudaGetErrorString(e));
   }
+  h->rope_blocks_per_sm = sa::rope_blocks_per_sm();
   if ((e = cudaMemset(h->d_err, 0, sizeof(int))) != cudaSuccess ||
       (e = sa::fmha_set_attributes()) != cudaSuccess) {
     cudaFree(h->d_err);

@@ -60,7 +60,9 @@ struct FmhaArgs {
 // Rows of queries one CTA owns: two 128-row tiles (standard) or one tile with two maps.
 constexpr int fmha_rows_per_cta(bool diff) { return diff ? kBlockM : 2 * kBlockM; }
 
-cudaError_t rope_launch(const RopeArgs& a, bool bf16, int num_sms, cudaStream_t stream);
+// Blocks of the RoPE kernel resident per SM (from the occupancy calculator).
+int rope_blocks_per_sm();
+cudaError_t rope_launch(const RopeArgs& a, bool bf16, int num_sms, int blocks_per_sm, cudaStream_t stream);
 
 cudaError_t fmha_set_attributes();
 // Registers per thread ptxas assigned to each attention kernel (must equal kFmhaLaunchRegs).

@@ -114,16 +114,30 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constan
 
 }  // namespace
 
-cudaError_t rope_launch(const RopeArgs& a_in, bool bf16, int num_sms, cudaStream_t stream) {
+int rope_blocks_per_sm() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, rope_kernel<false>, kRopeThreads, 0) != cudaSuccess)
+    return 1;
+  int m = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&m, rope_kernel<true>, kRopeThreads, 0) != cudaSuccess)
+    return 1;
+  n = n < m ? n : m;
+  return n > 0 ? n : 1;
+}
+
+cudaError_t rope_launch(const RopeArgs& a_in, bool bf16, int num_sms, int blocks_per_sm,
+                        cudaStream_t stream) {
   RopeArgs a = a_in;
   const long long bx = (a.L + kRopeRows - 1) / kRopeRows;
-  // Aim for about 8 resident blocks per SM; each block takes a slice of the planes.
-  const long long want = 8LL * (num_sms > 0 ? num_sms : 148);
-  long long by = (want + bx - 1) / bx;
-  if (by > a.planes) by = a.planes;
-  if (by < 1) by = 1;
-  long long ppb = (a.planes + by - 1) / by;
-  by = (a.planes + ppb - 1) / ppb;
+  // A thread issues the loads of up to kPlaneBatch planes at once.  Take the fewest planes per
+  // block (the (cos, sin) pairs are computed once per thread and reused for its planes) that
+  // fits the grid into what is resident at once, up to one batch per thread; past that, more
+  // blocks (waves) rather than more serial batches per thread.
+  const long long resident = static_cast<long long>(num_sms > 0 ? num_sms : 148) *
+                             (blocks_per_sm > 0 ? blocks_per_sm : 1);
+  long long ppb = 1;
+  while (ppb < a.planes && ppb < kPlaneBatch && bx * ((a.planes + ppb - 1) / ppb) > resident) ++ppb;
+  long long by = (a.planes + ppb - 1) / ppb;
   if (by > 65535) {
     by = 65535;
     ppb = (a.planes + by - 1) / by;
