@@ -316,9 +316,11 @@ def run_ours(args):
         sa.sa_rope_qk(h, q.data_ptr(), k.data_ptr(), None, q_rot.data_ptr(), k_rot.data_ptr(),
                       w.B, w.H, w.L, w.d, w.nmaps, dtype, s)
 
+    split = ws[2 * ((nqk * 2 + 255) // 256 * 256):]   # the split region after q', k'
+
     def attn():
         sa.sa_attn_fwd(h, q_rot.data_ptr(), k_rot.data_ptr(), v.data_ptr(), out.data_ptr(),
-                       w.B, w.H, w.L, w.d, w.window, lam, dtype, s)
+                       w.B, w.H, w.L, w.d, w.window, lam, dtype, s, split.data_ptr(), split.numel())
 
     def full():
         sa.sa_rope_attn(h, q.data_ptr(), k.data_ptr(), v.data_ptr(), None, out.data_ptr(), w.B, w.H,

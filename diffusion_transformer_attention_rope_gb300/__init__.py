@@ -18,7 +18,7 @@ from typing import Optional, Sequence
 
 __all__ = [
     "SA_FP16", "SA_BF16", "SaAttnError", "library_path", "load_library",
-    "sa_attn_create", "sa_attn_destroy", "sa_rope_attn_workspace_size", "sa_rope_attn",
+    "sa_attn_create", "sa_attn_destroy", "sa_rope_attn_workspace_size", "sa_attn_fwd_workspace_size", "sa_rope_attn",
     "sa_rope_qk", "sa_attn_fwd", "sa_rope_attn_noalloc", "sa_attn_check", "sa_attn_set_timeout", "sa_last_error", "sa_status_string", "RopeAttention",
 ]
 
@@ -66,7 +66,9 @@ def load_library():
         lib.sa_rope_attn.restype = i
         lib.sa_rope_qk.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
         lib.sa_rope_qk.restype = i
-        lib.sa_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(f), i, vp]
+        lib.sa_attn_fwd_workspace_size.argtypes = [i, i, i, i, i]
+        lib.sa_attn_fwd_workspace_size.restype = sz
+        lib.sa_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(f), i, vp, sz, vp]
         lib.sa_attn_fwd.restype = i
         lib.sa_rope_attn_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i,
                                              ctypes.POINTER(f), i, vp]
@@ -110,6 +112,10 @@ def sa_rope_attn_workspace_size(B: int, H: int, L: int, d: int, differential: bo
     return int(load_library().sa_rope_attn_workspace_size(B, H, L, d, 1 if differential else 0))
 
 
+def sa_attn_fwd_workspace_size(B: int, H: int, L: int, d: int, differential: bool) -> int:
+    return int(load_library().sa_attn_fwd_workspace_size(B, H, L, d, 1 if differential else 0))
+
+
 def sa_rope_attn(handle: int, q: int, k: int, v: int, positions: Optional[int], out: int,
                  B: int, H: int, L: int, d: int, window: int, lam: Optional[Sequence[float]],
                  dtype: int, workspace: Optional[int], workspace_bytes: int,
@@ -141,12 +147,12 @@ def sa_rope_qk(handle: int, q: int, k: int, positions: Optional[int], q_rot: int
 
 def sa_attn_fwd(handle: int, q_rot: int, k_rot: int, v: int, out: int, B: int, H: int, L: int,
                 d: int, window: int, lam: Optional[Sequence[float]], dtype: int,
-                stream: Optional[int]) -> None:
-    """Enqueue the attention stage alone on already-rotated q/k."""
+                stream: Optional[int], workspace: Optional[int] = None, workspace_bytes: int = 0) -> None:
+    """Enqueue the attention stage alone on already-rotated q/k (workspace: optional split region)."""
     _check(load_library().sa_attn_fwd(
         ctypes.c_void_p(handle), ctypes.c_void_p(q_rot), ctypes.c_void_p(k_rot), ctypes.c_void_p(v),
         ctypes.c_void_p(out), int(B), int(H), int(L), int(d), int(window), _lam(lam), int(dtype),
-        ctypes.c_void_p(stream)))
+        ctypes.c_void_p(workspace), ctypes.c_size_t(workspace_bytes), ctypes.c_void_p(stream)))
 
 
 def sa_rope_attn_noalloc(handle: int, q: int, k: int, v: int, positions: Optional[int], out: int,

@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
@@ -137,9 +139,34 @@ sa_status launch_rope(const sa_attn_s* h, const void* q, const void* k, const in
   return ok();
 }
 
+// Key tiles visited by query block qb (the kernel's own rule).
+int block_tiles_host(int L, int window, int rows, int qb) {
+  int lo = 0, hi = (L - 1) / sa::kBlockN;
+  if (window >= 0) {
+    const int q0 = qb * rows;
+    const int q_last = std::min(L, q0 + rows) - 1;
+    lo = std::max(0, q0 - window) / sa::kBlockN;
+    hi = std::min(L - 1, q_last + window) / sa::kBlockN;
+  }
+  return hi - lo + 1;
+}
+
+// Every launch gets its own epoch: it tags the unit counters of the split region, so they
+// never need clearing by the caller.
+std::atomic<unsigned> g_epoch{0};
+
+// Bytes of the split region for this shape: one 8-byte counter per unit, then one partial-result
+// slot per piece CTA (at most kMaxPieces).
+size_t split_bytes(int B, int H, int L, bool diff) {
+  const int rows = sa::fmha_rows_per_cta(diff);
+  const unsigned long long units = static_cast<unsigned long long>(B) * H * ((L + rows - 1) / rows);
+  return align256(units * 8) +
+         align256(static_cast<size_t>(sa::kMaxPieces) * sa::fmha_partial_floats(diff) * sizeof(float));
+}
+
 sa_status launch_attn(const sa_attn_s* h, const void* q_rot, const void* k_rot, const void* v,
                       void* out, int B, int H, int L, int window, const float* lambda,
-                      sa_dtype dtype, sa_stream_t stream) {
+                      sa_dtype dtype, void* split_ws, sa_stream_t stream) {
   const bool diff = lambda != nullptr;
   const bool bf16 = dtype == SA_BF16;
   const int d = sa::kHeadDim;
@@ -166,7 +193,31 @@ sa_status launch_attn(const sa_attn_s* h, const void* q_rot, const void* k_rot, 
   fa.timeout_ns = h->timeout_ns;
   if (diff)
     for (int i = 0; i < H; ++i) fa.lambda[i] = lambda[i];
-  const long long ctas = static_cast<long long>(B) * H * fa.n_qblocks;
+  // One CTA per unit, except that when the units leave the GPU's last wave partly empty and a
+  // split region is given, the tail units (those of that last wave) are cut into tail_k pieces
+  // of their key range, one CTA each, with tail_k as large as the wave allows.
+  const long long units = static_cast<long long>(B) * H * fa.n_qblocks;
+  fa.whole_ctas = static_cast<int>(units);
+  fa.tail_k = 1;
+  long long ctas = units;
+  const long long G = std::min<long long>(h->num_sms, sa::kMaxPieces);
+  const long long tail = units % G;
+  if (split_ws != nullptr && tail > 0) {
+    int min_nt = 1 << 30;
+    for (int qb = 0; qb < fa.n_qblocks; ++qb) min_nt = std::min(min_nt, block_tiles_host(L, fa.window, rows, qb));
+    const long long k = std::min<long long>(std::min<long long>(G / tail, min_nt), sa::kMaxTailK);
+    if (k >= 2) {
+      fa.whole_ctas = static_cast<int>(units - tail);
+      fa.tail_k = static_cast<int>(k);
+      ctas = (units - tail) + tail * k;
+      uint8_t* ws = static_cast<uint8_t*>(split_ws);
+      fa.counters = reinterpret_cast<unsigned long long*>(ws);
+      fa.partials = reinterpret_cast<float*>(ws + align256(static_cast<size_t>(units) * 8));
+      unsigned ep = g_epoch.fetch_add(1u) + 1u;
+      if (ep == 0) ep = g_epoch.fetch_add(1u) + 1u;
+      fa.epoch = ep;
+    }
+  }
   cudaError_t e = sa::fmha_launch(diff, bf16, tm_q, tm_k, tm_v, fa, ctas, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(SA_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
   return ok();
@@ -199,7 +250,7 @@ sa_status rope_attn_into(const char* fn, sa_attn_t h, const void* q, const void*
   if ((st = check_lambda(fn, lambda, H)) != SA_OK) return st;
   st = launch_rope(h, q, k, positions, q_rot, k_rot, B, H, L, diff ? 2 : 1, dtype, stream);
   if (st != SA_OK) return st;
-  return launch_attn(h, q_rot, k_rot, v, out, B, H, L, window, lambda, dtype, stream);
+  return launch_attn(h, q_rot, k_rot, v, out, B, H, L, window, lambda, dtype, nullptr, stream);
 }
 
 }  // namespace sa
@@ -300,7 +351,13 @@ sa_status sa_attn_destroy(sa_attn_t h) {
 size_t sa_rope_attn_workspace_size(int B, int H, int L, int d, int differential) {
   size_t n = 0;
   if (d != sa::kHeadDim || !qk_elems(B, H, L, differential ? 2 : 1, &n)) return 0;
-  return 2 * align256(n * 2);
+  return 2 * align256(n * 2) + split_bytes(B, H, L, differential != 0);
+}
+
+size_t sa_attn_fwd_workspace_size(int B, int H, int L, int d, int differential) {
+  size_t n = 0;
+  if (d != sa::kHeadDim || !qk_elems(B, H, L, differential ? 2 : 1, &n)) return 0;
+  return split_bytes(B, H, L, differential != 0);
 }
 
 sa_status sa_rope_qk(sa_attn_t h, const void* q, const void* k, const int32_t* positions,
@@ -320,17 +377,22 @@ sa_status sa_rope_qk(sa_attn_t h, const void* q, const void* k, const int32_t* p
 
 sa_status sa_attn_fwd(sa_attn_t h, const void* q_rot, const void* k_rot, const void* v, void* out,
                       int B, int H, int L, int d, int window, const float* lambda, sa_dtype dtype,
-                      sa_stream_t stream) {
+                      void* workspace, size_t workspace_bytes, sa_stream_t stream) {
   const char* fn = "sa_attn_fwd";
   if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
   if (!q_rot || !k_rot || !v || !out)
     return fail(SA_ERR_INVALID_ARG, "%s: q_rot, k_rot, v and out must be non-NULL", fn);
-  if (!aligned16(q_rot) || !aligned16(k_rot) || !aligned16(v) || !aligned16(out))
-    return fail(SA_ERR_INVALID_ARG, "%s: q_rot, k_rot, v and out must be 16-byte aligned", fn);
-  sa_status st = check_shape(fn, B, H, L, d, dtype, lambda != nullptr);
+  if (!aligned16(q_rot) || !aligned16(k_rot) || !aligned16(v) || !aligned16(out) ||
+      (workspace && !aligned16(workspace)))
+    return fail(SA_ERR_INVALID_ARG, "%s: q_rot, k_rot, v, out and workspace must be 16-byte aligned", fn);
+  const bool diff = lambda != nullptr;
+  sa_status st = check_shape(fn, B, H, L, d, dtype, diff);
   if (st != SA_OK) return st;
   if ((st = check_lambda(fn, lambda, H)) != SA_OK) return st;
-  return launch_attn(h, q_rot, k_rot, v, out, B, H, L, window, lambda, dtype, stream);
+  if (workspace && workspace_bytes < split_bytes(B, H, L, diff))
+    return fail(SA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn,
+                split_bytes(B, H, L, diff), workspace_bytes);
+  return launch_attn(h, q_rot, k_rot, v, out, B, H, L, window, lambda, dtype, workspace, stream);
 }
 
 sa_status sa_rope_attn(sa_attn_t h, const void* q, const void* k, const void* v,
@@ -356,9 +418,10 @@ sa_status sa_rope_attn(sa_attn_t h, const void* q, const void* k, const void* v,
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   void* q_rot = ws;
   void* k_rot = ws + align256(nqk * 2);
+  void* split_ws = ws + 2 * align256(nqk * 2);
   st = launch_rope(h, q, k, positions, q_rot, k_rot, B, H, L, diff ? 2 : 1, dtype, stream);
   if (st != SA_OK) return st;
-  return launch_attn(h, q_rot, k_rot, v, out, B, H, L, window, lambda, dtype, stream);
+  return launch_attn(h, q_rot, k_rot, v, out, B, H, L, window, lambda, dtype, split_ws, stream);
 }
 
 sa_status sa_attn_set_timeout(sa_attn_t h, unsigned long long timeout_ns) {

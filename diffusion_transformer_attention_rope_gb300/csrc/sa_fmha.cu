@@ -62,7 +62,7 @@ struct Cfg {
   // barriers: q_full, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2],
   //           p_full[2], pv_done[2], s_free[2], o_full[2], drain[2], turn[2][4]
   static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 2 + 2 + 2 + 2 + 2 + 2 + 8;
-  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;           // tmem base, abort flag
+  static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;           // tmem base, abort flag, ticket
   static constexpr int OFF_LSUM = OFF_MISC + 16;                // float [2][128]
   static constexpr int SMEM_USED = OFF_LSUM + 2 * kBlockM * 4;
   static constexpr int SMEM_ALLOC = SMEM_USED + 1024;           // slack for 1 KB alignment
@@ -113,6 +113,31 @@ __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, volatile in
   }
 }
 
+// This CTA's index, read from the special register each time (not a value the compiler keeps).
+__device__ __forceinline__ unsigned cta_index() {
+  unsigned x;
+  asm volatile("mov.u32 %0, %%ctaid.x;" : "=r"(x));
+  return x;
+}
+
+// Counts one finished piece of a unit in this launch; true for the piece that completes the
+// unit.  The counter's upper half holds the launch's epoch (never 0), so a value left by an
+// earlier launch starts a fresh count; the last piece also clears the counter, so that a
+// replay of the same launch (a CUDA graph keeps its epoch) starts fresh too.
+__device__ bool take_ticket(unsigned long long* cnt, unsigned epoch, int npieces) {
+  const unsigned long long tag = static_cast<unsigned long long>(epoch) << 32;
+  unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(cnt), assumed;
+  do {
+    assumed = old;
+    const unsigned long long nv = (assumed >> 32) == epoch ? assumed + 1 : (tag | 1ull);
+    old = atomicCAS(cnt, assumed, nv);
+  } while (old != assumed);
+  const unsigned long long mine = (old >> 32) == epoch ? (old & 0xffffffffull) + 1 : 1ull;
+  if (mine != static_cast<unsigned long long>(npieces)) return false;
+  atomicExch(cnt, 0ull);
+  return true;
+}
+
 // Warp-uniform pipeline wait: every lane waits, and the warp agrees on the outcome.
 __device__ __forceinline__ bool pwait_w(uint32_t bar, uint32_t parity, volatile int* abort_flag,
                                         int* err, int err_bit, uint64_t timeout_ns) {
@@ -146,13 +171,18 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
 
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  volatile int* ticket = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 8);
   float* lsum = reinterpret_cast<float*>(smem + C::OFF_LSUM);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int L = a.L;
-  const int bh = blockIdx.x / a.n_qblocks;
-  const int q0 = (blockIdx.x % a.n_qblocks) * C::ROWS;
+  // The unit of this CTA: a whole one, or a piece (a share of the key tiles) of a tail unit.
+  const bool piece = static_cast<int>(blockIdx.x) >= a.whole_ctas;
+  const int pidx = static_cast<int>(blockIdx.x) - a.whole_ctas;   // piece index (pieces only)
+  const int unit = piece ? a.whole_ctas + pidx / a.tail_k : static_cast<int>(blockIdx.x);
+  const int bh = unit / a.n_qblocks;
+  const int q0 = (unit % a.n_qblocks) * C::ROWS;
   const int q_last = min(L, q0 + C::ROWS) - 1;
   const int w = a.window;
 
@@ -161,6 +191,13 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
   if (w >= 0) {
     t_lo = max(0, q0 - w) / kBlockN;
     t_hi = min(L - 1, q_last + w) / kBlockN;
+  }
+  if (piece) {
+    // piece k of tail_k: tiles [t_lo + k nt / tail_k, t_lo + (k + 1) nt / tail_k), never empty
+    // (the host keeps tail_k <= nt)
+    const int nt = t_hi - t_lo + 1, k = pidx % a.tail_k;
+    t_hi = t_lo + (k + 1) * nt / a.tail_k - 1;
+    t_lo = t_lo + k * nt / a.tail_k;
   }
   const int n_tiles = t_hi - t_lo + 1;
   const uint64_t tmo = a.timeout_ns;
@@ -498,7 +535,99 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     if (DIFF && ok) ok = pwait(bar.o_full(1 - s), 0, abort_flag, a.err, kErrSoftmax, tmo);
     ok = __all_sync(0xffffffffu, ok);
     tc_fence_after();
-    if (!DIFF) {
+    bool write_out = true;
+    // The piece index is read again here rather than kept live through the loop (registers are
+    // the softmax warps' scarce resource there).
+    const int pidx_e = static_cast<int>(cta_index()) - a.whole_ctas;
+    if (pidx_e >= 0) {
+      // A piece of a tail unit: store its un-normalised O, running max (raw score units) and row
+      // sum; the piece that finishes last merges all of the unit's pieces, in piece order, into
+      // O_s in TMEM and l_sum, and writes the output below as for a whole unit.  A slot holds O
+      // as [d_v / 4][256 rows] float4 (a warp's access is 512 contiguous bytes), then the
+      // running maxima [256] and the row sums [256].
+      constexpr int PF = fmha_partial_floats(DIFF);
+      constexpr int NR = 2 * kBlockM;                    // rows of a slot (both streams)
+      const size_t row_off = static_cast<size_t>(s * kBlockM + r);
+      float* part = a.partials + static_cast<size_t>(pidx_e) * PF;
+      if (ok) {
+        float4* d4 = reinterpret_cast<float4*>(part) + row_off;
+#pragma unroll
+        for (int cc = 0; cc < C::DV / 32; ++cc) {
+          uint32_t o[32];
+          tmem_ld32_nowait(tmem + C::o_col(s) + lane_off + 32 * cc, o);
+          tmem_wait_ld_32(o);
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            d4[(8 * cc + q) * NR] = make_float4(__uint_as_float(o[4 * q]), __uint_as_float(o[4 * q + 1]),
+                                                __uint_as_float(o[4 * q + 2]), __uint_as_float(o[4 * q + 3]));
+        }
+        part[2 * kBlockM * C::DV + row_off] = m_use;
+        part[2 * kBlockM * C::DV + 2 * kBlockM + row_off] = l_sum;
+      }
+      __threadfence();
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (threadIdx.x == 0)
+        *ticket = take_ticket(a.counters + a.whole_ctas + pidx_e / a.tail_k, a.epoch, a.tail_k) ? 1 : 0;
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      write_out = *ticket != 0;
+      if (write_out) {
+        // every other piece's stores are visible after this fence
+        __threadfence();
+        const int p0 = pidx_e - pidx_e % a.tail_k;
+        const float* base = a.partials + static_cast<size_t>(p0) * PF;
+        // Piece weights 2^((m_p - mm) c); a piece whose keys all lie outside this row's window
+        // (m_p = -inf) contributes nothing.  Every load of a step is issued before its use.
+        float mp[kMaxTailK], lp[kMaxTailK], wt[kMaxTailK];
+#pragma unroll
+        for (int i = 0; i < kMaxTailK; ++i) {
+          mp[i] = i < a.tail_k ? __ldcg(base + i * PF + 2 * kBlockM * C::DV + row_off) : -INFINITY;
+          lp[i] = i < a.tail_k ? __ldcg(base + i * PF + 2 * kBlockM * C::DV + 2 * kBlockM + row_off) : 0.0f;
+        }
+        float mm = mp[0];
+#pragma unroll
+        for (int i = 1; i < kMaxTailK; ++i) mm = fmaxf(mm, mp[i]);
+        float lm = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kMaxTailK; ++i) {
+          wt[i] = mp[i] == -INFINITY ? 0.0f : ex2_approx((mp[i] - mm) * c);
+          lm = fmaf(lp[i], wt[i], lm);
+        }
+        l_sum = lm;
+        // the merged O, 32 columns at a time, goes back to TMEM for the output code below
+#pragma unroll
+        for (int cc = 0; cc < C::DV / 32; ++cc) {
+          float4 v4[kMaxTailK][8];
+#pragma unroll
+          for (int i = 0; i < kMaxTailK; ++i) {
+            const float4* po = reinterpret_cast<const float4*>(base + i * PF) + row_off;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              v4[i][q] = i < a.tail_k ? __ldcg(po + (8 * cc + q) * NR) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+          uint32_t o[32];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < kMaxTailK; ++i) {
+              acc.x = fmaf(v4[i][q].x, wt[i], acc.x);
+              acc.y = fmaf(v4[i][q].y, wt[i], acc.y);
+              acc.z = fmaf(v4[i][q].z, wt[i], acc.z);
+              acc.w = fmaf(v4[i][q].w, wt[i], acc.w);
+            }
+            o[4 * q] = __float_as_uint(acc.x);
+            o[4 * q + 1] = __float_as_uint(acc.y);
+            o[4 * q + 2] = __float_as_uint(acc.z);
+            o[4 * q + 3] = __float_as_uint(acc.w);
+          }
+          tmem_st32(tmem + C::o_col(s) + lane_off + 32 * cc, o);
+        }
+        tmem_wait_st();
+      }
+    }
+    if (!write_out) {
+      // another piece of this unit writes its output
+    } else if (!DIFF) {
       const float inv = l_sum > 0.0f ? 1.0f / l_sum : 0.0f;
       uint16_t* dst = static_cast<uint16_t*>(a.out) +
                       (static_cast<size_t>(bh) * L + grow) * static_cast<size_t>(C::DV);
@@ -522,7 +651,9 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       }
     } else {
       lsum[s * kBlockM + r] = l_sum;
+      tc_fence_before();
       asm volatile("bar.sync 1, 256;" ::: "memory");
+      tc_fence_after();
       const float l0 = lsum[r], l1 = lsum[kBlockM + r];
       const float inv0 = l0 > 0.0f ? 1.0f / l0 : 0.0f;
       const float inv1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;

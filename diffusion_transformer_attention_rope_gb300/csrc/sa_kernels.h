@@ -45,20 +45,39 @@ struct RopeArgs {
 };
 
 // Attention kernel arguments (tensor maps are passed separately as __grid_constant__).
+//
+// Grid.  A unit is the query rows of one (batch, head) block (fmha_rows_per_cta) with the key
+// tiles they visit.  CTAs [0, whole_ctas) take units 0 .. whole_ctas - 1 whole.  When the
+// units do not fill the last wave of the GPU, the units after those (the tail) are each cut
+// into tail_k pieces of their key range, one CTA per piece, so that the last wave is spread
+// over more SMs; a piece stores its un-normalised O, running max and row sum (FP32) in
+// `partials` and the piece that finishes last merges them and writes the output.
 struct FmhaArgs {
   void* out;                  // [B, H, L, d_v]
   int* err;                   // device error word (bits above), atomically OR-ed
   int L;
   int H;
-  int n_qblocks;              // CTAs per (b, h)
+  int n_qblocks;              // units per (b, h)
   int window;                 // < 0: full attention, else |i - j| <= window (< L - 1)
   float scale_log2;           // log2(e) / sqrt(d)
+  int whole_ctas;             // CTAs that take a whole unit (the first ones)
+  int tail_k;                 // pieces per tail unit (1: no pieces)
+  unsigned epoch;             // nonzero, distinct for every launch (tags the unit counters)
+  unsigned long long* counters;  // tail_k > 1: [units] epoch-tagged piece counts
+  float* partials;            // tail_k > 1: one slot of fmha_partial_floats per piece CTA
   unsigned long long timeout_ns;
   float lambda[kMaxDiffHeads];
 };
 
-// Rows of queries one CTA owns: two 128-row tiles (standard) or one tile with two maps.
+// Rows of queries in one unit: two 128-row tiles (standard) or one tile with two maps.
 constexpr int fmha_rows_per_cta(bool diff) { return diff ? kBlockM : 2 * kBlockM; }
+// FP32 values of one partial-result slot: per stream (tile or map) and row, O (d_v values),
+// then the running max and the row sum.
+constexpr int fmha_partial_floats(bool diff) { return 2 * kBlockM * ((diff ? 2 * kHeadDim : kHeadDim) + 2); }
+// Most piece CTAs one launch uses (the split workspace is sized for that many slots), and most
+// pieces one unit is cut into.
+constexpr int kMaxPieces = 160;
+constexpr int kMaxTailK = 4;
 
 // Blocks of the RoPE kernel resident per SM (from the occupancy calculator).
 int rope_blocks_per_sm();

@@ -69,9 +69,12 @@ extern "C" sa_status sa_rope_attn_noalloc(sa_attn_t h, const void* q, const void
                                           sa_stream_t stream) {
   if (!h) return sa::set_error(SA_ERR_INVALID_ARG, "sa_rope_attn_noalloc: handle is NULL");
   const bool diff = lambda != nullptr;
-  const size_t need = sa_rope_attn_workspace_size(B, H, L, d, diff ? 1 : 0);
-  if (need == 0)
+  if (sa_rope_attn_workspace_size(B, H, L, d, diff ? 1 : 0) == 0)
     return sa::set_error(SA_ERR_INVALID_ARG, "sa_rope_attn_noalloc: invalid sizes (B, H, L >= 1, d = 64)");
+  // The scratch holds q' and k' only: this entry point runs the attention stage without the
+  // split region (one CTA per query block).
+  const size_t nqk = static_cast<size_t>(B) * H * (diff ? 2 : 1) * L * d;
+  const size_t need = 2 * round256(nqk * 2);
   if (need > kScratchBytes) {
     char msg[256];
     snprintf(msg, sizeof(msg),
@@ -83,7 +86,6 @@ extern "C" sa_status sa_rope_attn_noalloc(sa_attn_t h, const void* q, const void
   void* base = nullptr;
   const sa_status st = scratch_address(sa::handle_device(h), &base);
   if (st != SA_OK) return st;
-  const size_t nqk = static_cast<size_t>(B) * H * (diff ? 2 : 1) * L * d;
   unsigned char* ws = static_cast<unsigned char*>(base);
   return sa::rope_attn_into("sa_rope_attn_noalloc", h, q, k, v, positions, out, B, H, L, d, window,
                             lambda, dtype, ws, ws + round256(nqk * 2), stream);

@@ -87,10 +87,28 @@ SA_API sa_status sa_attn_destroy(sa_attn_t handle);
 /*
  * Bytes of device workspace sa_rope_attn needs for this shape: the rotated
  * and cast-back q and k (two buffers of B*H*nmaps*L*d elements of 2 bytes,
- * each rounded up to 256 bytes).  differential != 0 selects nmaps = 2.
+ * each rounded up to 256 bytes), followed by the split region of
+ * sa_attn_fwd_workspace_size bytes.  differential != 0 selects nmaps = 2.
  * Returns 0 for invalid sizes.
  */
 SA_API size_t sa_rope_attn_workspace_size(int B, int H, int L, int d, int differential);
+
+/*
+ * Bytes of the split region that sa_attn_fwd may be given: one 8-byte counter
+ * per query block (256 rows standard, 128 differential) of every (batch,
+ * head), rounded up to 256 bytes, then 160 FP32 partial-result slots of
+ * 2*128*(d_v + 2) values.
+ *
+ * The attention kernel runs one CTA per query block.  When those leave the
+ * GPU's last wave partly empty and the split region is given, each block of
+ * that last wave is cut into k pieces of its key range (k as large as the wave
+ * allows), one CTA each; the pieces leave FP32 partial results in the region
+ * and the piece that finishes last merges them in a fixed order (results are
+ * reproducible run to run).  The counters carry a per-launch tag and are
+ * cleared by the launch that used them, so the region never needs clearing by
+ * the caller (also across CUDA-graph replays).  Returns 0 for invalid sizes.
+ */
+SA_API size_t sa_attn_fwd_workspace_size(int B, int H, int L, int d, int differential);
 
 /*
  * Enqueue RoPE + attention on `stream`.
@@ -148,7 +166,10 @@ SA_API sa_status sa_rope_qk(sa_attn_t handle,
 /*
  * sa_attn_fwd: scaled-dot-product attention (softmax in FP32; differential
  *   when lambda != NULL; sliding window when window >= 0) on q_rot, k_rot
- *   taken as already rotated.  No workspace.
+ *   taken as already rotated.  workspace is optional: NULL runs one CTA per
+ *   query block; otherwise it is a device split region (16-byte aligned) of at
+ *   least sa_attn_fwd_workspace_size bytes (SA_ERR_WORKSPACE if smaller), and
+ *   calls that use the same region must be ordered on the GPU (same stream).
  */
 SA_API sa_status sa_attn_fwd(sa_attn_t handle,
                              const void* q_rot, const void* k_rot, const void* v,
@@ -156,7 +177,9 @@ SA_API sa_status sa_attn_fwd(sa_attn_t handle,
                              int B, int H, int L, int d,
                              int window,
                              const float* lambda,
-                             sa_dtype dtype, sa_stream_t stream);
+                             sa_dtype dtype,
+                             void* workspace, size_t workspace_bytes,
+                             sa_stream_t stream);
 
 /*
  * Size of the scratch array built into the library for sa_rope_attn_noalloc:

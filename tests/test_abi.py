@@ -51,14 +51,31 @@ def test_library_is_built_for_sm103a_only(lib):
     assert arches == {"103a"}, arches
 
 
+def _a256(x):
+    return (x + 255) // 256 * 256
+
+
+def _split_bytes(B, H, L, diff):
+    # one 8-byte counter per query block (256 rows standard, 128 differential), then 160
+    # FP32 partial-result slots of 2*128*(d_v + 2) values
+    rows = 128 if diff else 256
+    dv = 128 if diff else 64
+    units = B * H * ((L + rows - 1) // rows)
+    return _a256(units * 8) + _a256(160 * 2 * 128 * (dv + 2) * 4)
+
+
 def test_workspace_size():
-    # two 256-byte-aligned buffers of B*H*nmaps*L*64 two-byte elements
+    # two 256-byte-aligned buffers of B*H*nmaps*L*64 two-byte elements, then the split region
     n = 1 * 16 * 1292 * 64 * 2
-    assert sa.sa_rope_attn_workspace_size(1, 16, 1292, 64, False) == 2 * ((n + 255) // 256 * 256)
+    assert sa.sa_rope_attn_workspace_size(1, 16, 1292, 64, False) == 2 * _a256(n) + _split_bytes(1, 16, 1292, False)
     n = 1 * 16 * 2 * 4096 * 64 * 2
-    assert sa.sa_rope_attn_workspace_size(1, 16, 4096, 64, True) == 2 * n
+    assert sa.sa_rope_attn_workspace_size(1, 16, 4096, 64, True) == 2 * n + _split_bytes(1, 16, 4096, True)
+    assert sa.sa_attn_fwd_workspace_size(1, 24, 4096, 64, False) == _split_bytes(1, 24, 4096, False)
+    assert sa.sa_attn_fwd_workspace_size(2, 3, 777, 64, True) == _split_bytes(2, 3, 777, True)
     assert sa.sa_rope_attn_workspace_size(1, 16, 4096, 128, True) == 0
+    assert sa.sa_attn_fwd_workspace_size(1, 16, 4096, 128, True) == 0
     assert sa.sa_rope_attn_workspace_size(0, 16, 4096, 64, False) == 0
+    assert sa.sa_attn_fwd_workspace_size(0, 16, 4096, 64, False) == 0
     assert sa.sa_rope_attn_workspace_size(1, 1, -5, 64, False) == 0
 
 

@@ -297,3 +297,79 @@ def test_host_checks_reject_bad_arguments(attn):
     torch.cuda.synchronize()
     assert torch.all(out == 7.0)
     attn.check()
+
+
+# ----------------------------------------------------------------------------- split last wave
+
+def pieces_per_tail_unit(B, H, L, window, diff):
+    """Host rule of the attention launch: how many key-range pieces each tail unit gets."""
+    sms = min(torch.cuda.get_device_properties(0).multi_processor_count, 160)
+    rows = 128 if diff else 256
+    nqb = (L + rows - 1) // rows
+    units = B * H * nqb
+    tail = units % sms
+    if tail == 0:
+        return 1
+    w = -1 if window < 0 or window >= L - 1 else window
+    nts = []
+    for qb in range(nqb):
+        lo, hi = 0, (L - 1) // 128
+        if w >= 0:
+            q0 = qb * rows
+            lo, hi = max(0, q0 - w) // 128, min(L - 1, min(L, q0 + rows) - 1 + w) // 128
+        nts.append(hi - lo + 1)
+    return min(sms // tail, min(nts), 4)
+
+
+@pytest.mark.parametrize("B,H,L,window,diff,dtype", [
+    (1, 3, 1000, -1, False, "fp16"),    # 12 units, 4 pieces of two key tiles each
+    (2, 2, 777, 129, False, "bf16"),    # window: pieces whose tiles miss some rows' windows
+    (1, 2, 900, -1, True, "bf16"),      # differential: merged O of both maps
+    (1, 1, 1200, 17, True, "bf16"),     # differential, narrow window
+    (1, 2, 4096, -1, False, "fp16"),    # long rows: 4 pieces of 8 key tiles
+    (1, 1, 700, 0, False, "fp16"),      # window 0: units of one key tile are never cut
+])
+def test_split_pieces_match_oracle_and_whole_units(attn, B, H, L, window, diff, dtype):
+    k = pieces_per_tail_unit(B, H, L, window, diff)
+    assert k >= 2 or window == 0, "shape chosen to exercise the pieces"
+    w = small("split", B=B, H=H, L=L, window=window, nmaps=2 if diff else 1, dv=128 if diff else 64,
+              dtype=dtype, seed=1200 + L + window, lam=("uniform", 0.2, 0.8) if diff else None)
+    x = synth.make_inputs(w)
+    q, k_, v = dev(x["q"], dtype), dev(x["k"], dtype), dev(x["v"], dtype)
+    nm = 2 if diff else 1
+    qr, kr = torch.empty_like(q), torch.empty_like(k_)
+    split = torch.empty(sa.sa_attn_fwd_workspace_size(B, H, L, 64, diff), dtype=torch.uint8, device="cuda")
+    split.fill_(0xA5)   # the region needs no clearing: any prior content is fine
+    lam = None if x["lam"] is None else [float(t) for t in x["lam"]]
+    dt = sa.SA_BF16 if dtype == "bf16" else sa.SA_FP16
+    s = torch.cuda.current_stream().cuda_stream
+    sa.sa_rope_qk(attn.handle, q.data_ptr(), k_.data_ptr(), None, qr.data_ptr(), kr.data_ptr(),
+                  B, H, L, 64, nm, dt, s)
+    outs = []
+    for ws in (None, split, split):       # whole units, then pieces twice (counters reused)
+        out = torch.empty((B, H, L, w.dv), dtype=TDT[dtype], device="cuda")
+        sa.sa_attn_fwd(attn.handle, qr.data_ptr(), kr.data_ptr(), v.data_ptr(), out.data_ptr(),
+                       B, H, L, 64, window, lam, dt, s,
+                       None if ws is None else ws.data_ptr(), 0 if ws is None else ws.numel())
+        torch.cuda.synchronize()
+        outs.append(out.float().cpu().numpy().astype(np.float64))
+    attn.check()
+    ref = oracle.rope_attn_workload(x)
+    compare(outs[0], ref, "whole units", dtype=dtype)
+    compare(outs[1], ref, "pieces", dtype=dtype)
+    assert np.array_equal(outs[1], outs[2]), "pieces are merged in a fixed order"
+    assert np.abs(outs[1] - outs[0]).max() <= 2 * TOL_ABS
+
+
+def test_split_region_too_small_is_refused(attn):
+    B, H, L = 1, 2, 300
+    q = torch.zeros((B, H, L, 64), dtype=torch.float16, device="cuda")
+    out = torch.full((B, H, L, 64), 3.0, dtype=torch.float16, device="cuda")
+    need = sa.sa_attn_fwd_workspace_size(B, H, L, 64, False)
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    with pytest.raises(sa.SaAttnError) as e:
+        sa.sa_attn_fwd(attn.handle, q.data_ptr(), q.data_ptr(), q.data_ptr(), out.data_ptr(), B, H, L, 64,
+                       -1, None, sa.SA_FP16, torch.cuda.current_stream().cuda_stream, ws.data_ptr(), need - 1)
+    assert e.value.status == 6
+    torch.cuda.synchronize()
+    assert torch.all(out == 3.0)
