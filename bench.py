@@ -305,22 +305,27 @@ def run_ours(args):
     ws_bytes = sa.sa_rope_attn_workspace_size(w.B, w.H, w.L, w.d, w.differential)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
     nqk = q.numel()
-    q_rot = ws[: nqk * 2]
-    k_rot = ws[(nqk * 2 + 255) // 256 * 256:][: nqk * 2]
+    # the workspace of sa_rope_attn: the (cos, sin) table, k', the split region; region 2 runs
+    # the same two stages through their own entry points on the same buffers
+    a256 = lambda n: (n + 255) // 256 * 256
+    off_k = a256(sa.sa_rope_table_bytes(w.L))
+    off_split = off_k + a256(nqk * 2)
+    cs_table = ws[:off_k]
+    k_rot = ws[off_k:off_k + nqk * 2]
+    split = ws[off_split:]
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=device)
     h = sa.sa_attn_create(local)
     stream = torch.cuda.current_stream(device)
     s = stream.cuda_stream
 
     def rope():
-        sa.sa_rope_qk(h, q.data_ptr(), k.data_ptr(), None, q_rot.data_ptr(), k_rot.data_ptr(),
-                      w.B, w.H, w.L, w.d, w.nmaps, dtype, s)
-
-    split = ws[2 * ((nqk * 2 + 255) // 256 * 256):]   # the split region after q', k'
+        sa.sa_rope_k(h, k.data_ptr(), None, k_rot.data_ptr(), cs_table.data_ptr(),
+                     w.B, w.H, w.L, w.d, w.nmaps, dtype, s)
 
     def attn():
-        sa.sa_attn_fwd(h, q_rot.data_ptr(), k_rot.data_ptr(), v.data_ptr(), out.data_ptr(),
-                       w.B, w.H, w.L, w.d, w.window, lam, dtype, s, split.data_ptr(), split.numel())
+        sa.sa_attn_fwd_rope_q(h, q.data_ptr(), k_rot.data_ptr(), cs_table.data_ptr(), v.data_ptr(),
+                              out.data_ptr(), w.B, w.H, w.L, w.d, w.window, lam, dtype, s,
+                              split.data_ptr(), split.numel())
 
     def full():
         sa.sa_rope_attn(h, q.data_ptr(), k.data_ptr(), v.data_ptr(), None, out.data_ptr(), w.B, w.H,
@@ -433,7 +438,7 @@ def run_ours(args):
         "frac_of_peak": value / world / peaks["tflops"],
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["tflops"], "traffic": load_traffic(w.name),
-                     "kernel": "attention (sa_attn_fwd)", "kernel_sha": kernel_sha(),
+                     "kernel": "attention (sa_attn_fwd_rope_q)", "kernel_sha": kernel_sha(),
                      "peak_source": peaks["source"] + " bf16 burst",
                      "avg_ms": attn_avg_s * 1e3},
         "stages_ms": {"rope": statistics.mean(rope_ms), "attention": statistics.mean(attn_ms)},

@@ -18,7 +18,7 @@ from typing import Optional, Sequence
 
 __all__ = [
     "SA_FP16", "SA_BF16", "SaAttnError", "library_path", "load_library",
-    "sa_attn_create", "sa_attn_destroy", "sa_rope_attn_workspace_size", "sa_attn_fwd_workspace_size", "sa_rope_attn",
+    "sa_attn_create", "sa_attn_destroy", "sa_rope_attn_workspace_size", "sa_attn_fwd_workspace_size", "sa_rope_table_bytes", "sa_rope_k", "sa_attn_fwd_rope_q", "sa_rope_attn",
     "sa_rope_qk", "sa_attn_fwd", "sa_rope_attn_noalloc", "sa_attn_check", "sa_attn_set_timeout", "sa_last_error", "sa_status_string", "RopeAttention",
 ]
 
@@ -66,6 +66,13 @@ def load_library():
         lib.sa_rope_attn.restype = i
         lib.sa_rope_qk.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
         lib.sa_rope_qk.restype = i
+        lib.sa_rope_table_bytes.argtypes = [i]
+        lib.sa_rope_table_bytes.restype = sz
+        lib.sa_rope_k.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
+        lib.sa_rope_k.restype = i
+        lib.sa_attn_fwd_rope_q.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(f), i,
+                                           vp, sz, vp]
+        lib.sa_attn_fwd_rope_q.restype = i
         lib.sa_attn_fwd_workspace_size.argtypes = [i, i, i, i, i]
         lib.sa_attn_fwd_workspace_size.restype = sz
         lib.sa_attn_fwd.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(f), i, vp, sz, vp]
@@ -114,6 +121,29 @@ def sa_rope_attn_workspace_size(B: int, H: int, L: int, d: int, differential: bo
 
 def sa_attn_fwd_workspace_size(B: int, H: int, L: int, d: int, differential: bool) -> int:
     return int(load_library().sa_attn_fwd_workspace_size(B, H, L, d, 1 if differential else 0))
+
+
+def sa_rope_table_bytes(L: int) -> int:
+    return int(load_library().sa_rope_table_bytes(int(L)))
+
+
+def sa_rope_k(handle: int, k: int, positions: Optional[int], k_rot: int, cs_table: int, B: int, H: int,
+              L: int, d: int, nmaps: int, dtype: int, stream: Optional[int]) -> None:
+    """Enqueue the RoPE pass of k alone, also writing the (cos, sin) table for the Q prologue."""
+    _check(load_library().sa_rope_k(
+        ctypes.c_void_p(handle), ctypes.c_void_p(k), ctypes.c_void_p(positions), ctypes.c_void_p(k_rot),
+        ctypes.c_void_p(cs_table), int(B), int(H), int(L), int(d), int(nmaps), int(dtype),
+        ctypes.c_void_p(stream)))
+
+
+def sa_attn_fwd_rope_q(handle: int, q: int, k_rot: int, cs_table: int, v: int, out: int, B: int, H: int,
+                       L: int, d: int, window: int, lam: Optional[Sequence[float]], dtype: int,
+                       stream: Optional[int], workspace: Optional[int] = None, workspace_bytes: int = 0) -> None:
+    """Enqueue attention on raw q (rotated in the kernel's prologue with cs_table) and rotated k."""
+    _check(load_library().sa_attn_fwd_rope_q(
+        ctypes.c_void_p(handle), ctypes.c_void_p(q), ctypes.c_void_p(k_rot), ctypes.c_void_p(cs_table),
+        ctypes.c_void_p(v), ctypes.c_void_p(out), int(B), int(H), int(L), int(d), int(window), _lam(lam),
+        int(dtype), ctypes.c_void_p(workspace), ctypes.c_size_t(workspace_bytes), ctypes.c_void_p(stream)))
 
 
 def sa_rope_attn(handle: int, q: int, k: int, v: int, positions: Optional[int], out: int,

@@ -118,9 +118,10 @@ sa_status check_lambda(const char* fn, const float* lambda, int H) {
   return SA_OK;
 }
 
+// q == nullptr: rotate k only and write the (cos, sin) table cs (for the Q prologue).
 sa_status launch_rope(const sa_attn_s* h, const void* q, const void* k, const int32_t* positions,
                       void* q_rot, void* k_rot, int B, int H, int L, int nmaps, sa_dtype dtype,
-                      sa_stream_t stream) {
+                      sa_stream_t stream, void* cs = nullptr) {
   DeviceGuard guard(h->device);
   if (!guard.ok) return fail(SA_ERR_CUDA, "cannot select device %d", h->device);
   sa::RopeArgs ra;
@@ -128,6 +129,7 @@ sa_status launch_rope(const sa_attn_s* h, const void* q, const void* k, const in
   ra.k = static_cast<const uint16_t*>(k);
   ra.q_out = static_cast<uint16_t*>(q_rot);
   ra.k_out = static_cast<uint16_t*>(k_rot);
+  ra.cs = static_cast<float2*>(cs);
   ra.positions = positions;
   ra.planes = static_cast<long long>(B) * H * nmaps;
   ra.L = L;
@@ -164,9 +166,11 @@ size_t split_bytes(int B, int H, int L, bool diff) {
          align256(static_cast<size_t>(sa::kMaxPieces) * sa::fmha_partial_floats(diff) * sizeof(float));
 }
 
+// cs == nullptr: q_rot is rotated already; else q_rot is the raw q and the kernel rotates it
+// in its prologue with the (cos, sin) table cs.
 sa_status launch_attn(const sa_attn_s* h, const void* q_rot, const void* k_rot, const void* v,
                       void* out, int B, int H, int L, int window, const float* lambda,
-                      sa_dtype dtype, void* split_ws, sa_stream_t stream) {
+                      sa_dtype dtype, void* split_ws, sa_stream_t stream, const void* cs = nullptr) {
   const bool diff = lambda != nullptr;
   const bool bf16 = dtype == SA_BF16;
   const int d = sa::kHeadDim;
@@ -191,6 +195,7 @@ sa_status launch_attn(const sa_attn_s* h, const void* q_rot, const void* k_rot, 
   fa.window = (window < 0 || window >= L - 1) ? -1 : window;
   fa.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   fa.timeout_ns = h->timeout_ns;
+  fa.cs = static_cast<const float2*>(cs);
   if (diff)
     for (int i = 0; i < H; ++i) fa.lambda[i] = lambda[i];
   // One CTA per unit, except that when the units leave the GPU's last wave partly empty and a
@@ -218,6 +223,7 @@ sa_status launch_attn(const sa_attn_s* h, const void* q_rot, const void* k_rot, 
       fa.epoch = ep;
     }
   }
+  fa.wave = h->num_sms;
   cudaError_t e = sa::fmha_launch(diff, bf16, tm_q, tm_k, tm_v, fa, ctas, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(SA_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
   return ok();
@@ -348,10 +354,15 @@ sa_status sa_attn_destroy(sa_attn_t h) {
   return ok();
 }
 
+size_t sa_rope_table_bytes(int L) {
+  if (L <= 0 || L >= sa::kMaxL) return 0;
+  return static_cast<size_t>(L) * (sa::kHeadDim / 2) * 2 * sizeof(float);
+}
+
 size_t sa_rope_attn_workspace_size(int B, int H, int L, int d, int differential) {
   size_t n = 0;
   if (d != sa::kHeadDim || !qk_elems(B, H, L, differential ? 2 : 1, &n)) return 0;
-  return 2 * align256(n * 2) + split_bytes(B, H, L, differential != 0);
+  return align256(sa_rope_table_bytes(L)) + align256(n * 2) + split_bytes(B, H, L, differential != 0);
 }
 
 size_t sa_attn_fwd_workspace_size(int B, int H, int L, int d, int differential) {
@@ -395,6 +406,41 @@ sa_status sa_attn_fwd(sa_attn_t h, const void* q_rot, const void* k_rot, const v
   return launch_attn(h, q_rot, k_rot, v, out, B, H, L, window, lambda, dtype, workspace, stream);
 }
 
+sa_status sa_rope_k(sa_attn_t h, const void* k, const int32_t* positions, void* k_rot, void* cs_table,
+                    int B, int H, int L, int d, int nmaps, sa_dtype dtype, sa_stream_t stream) {
+  const char* fn = "sa_rope_k";
+  if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
+  if (!k || !k_rot || !cs_table)
+    return fail(SA_ERR_INVALID_ARG, "%s: k, k_rot and cs_table must be non-NULL", fn);
+  if (!aligned16(k) || !aligned16(k_rot) || !aligned16(cs_table))
+    return fail(SA_ERR_INVALID_ARG, "%s: k, k_rot and cs_table must be 16-byte aligned", fn);
+  if (nmaps != 1 && nmaps != 2) return fail(SA_ERR_INVALID_ARG, "%s: nmaps must be 1 or 2", fn);
+  sa_status st = check_shape(fn, B, H, L, d, dtype, nmaps == 2);
+  if (st != SA_OK) return st;
+  return launch_rope(h, nullptr, k, positions, nullptr, k_rot, B, H, L, nmaps, dtype, stream, cs_table);
+}
+
+sa_status sa_attn_fwd_rope_q(sa_attn_t h, const void* q, const void* k_rot, const void* cs_table,
+                             const void* v, void* out, int B, int H, int L, int d, int window,
+                             const float* lambda, sa_dtype dtype, void* workspace,
+                             size_t workspace_bytes, sa_stream_t stream) {
+  const char* fn = "sa_attn_fwd_rope_q";
+  if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
+  if (!q || !k_rot || !cs_table || !v || !out)
+    return fail(SA_ERR_INVALID_ARG, "%s: q, k_rot, cs_table, v and out must be non-NULL", fn);
+  if (!aligned16(q) || !aligned16(k_rot) || !aligned16(cs_table) || !aligned16(v) || !aligned16(out) ||
+      (workspace && !aligned16(workspace)))
+    return fail(SA_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);
+  const bool diff = lambda != nullptr;
+  sa_status st = check_shape(fn, B, H, L, d, dtype, diff);
+  if (st != SA_OK) return st;
+  if ((st = check_lambda(fn, lambda, H)) != SA_OK) return st;
+  if (workspace && workspace_bytes < split_bytes(B, H, L, diff))
+    return fail(SA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn,
+                split_bytes(B, H, L, diff), workspace_bytes);
+  return launch_attn(h, q, k_rot, v, out, B, H, L, window, lambda, dtype, workspace, stream, cs_table);
+}
+
 sa_status sa_rope_attn(sa_attn_t h, const void* q, const void* k, const void* v,
                        const int32_t* positions, void* out, int B, int H, int L, int d, int window,
                        const float* lambda, sa_dtype dtype, void* workspace,
@@ -414,14 +460,16 @@ sa_status sa_rope_attn(sa_attn_t h, const void* q, const void* k, const void* v,
   if (!workspace || workspace_bytes < need)
     return fail(SA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given%s", fn, need,
                 workspace_bytes, workspace ? "" : " (NULL)");
+  // workspace: the (cos, sin) table, k', the split region.  The RoPE pass rotates k and writes
+  // the table; the attention kernel rotates q in its prologue.
   const size_t nqk = static_cast<size_t>(B) * H * (diff ? 2 : 1) * L * sa::kHeadDim;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  void* q_rot = ws;
-  void* k_rot = ws + align256(nqk * 2);
-  void* split_ws = ws + 2 * align256(nqk * 2);
-  st = launch_rope(h, q, k, positions, q_rot, k_rot, B, H, L, diff ? 2 : 1, dtype, stream);
+  void* cs = ws;
+  void* k_rot = ws + align256(sa_rope_table_bytes(L));
+  void* split_ws = static_cast<uint8_t*>(k_rot) + align256(nqk * 2);
+  st = launch_rope(h, nullptr, k, positions, nullptr, k_rot, B, H, L, diff ? 2 : 1, dtype, stream, cs);
   if (st != SA_OK) return st;
-  return launch_attn(h, q_rot, k_rot, v, out, B, H, L, window, lambda, dtype, split_ws, stream);
+  return launch_attn(h, q, k_rot, v, out, B, H, L, window, lambda, dtype, split_ws, stream, cs);
 }
 
 sa_status sa_attn_set_timeout(sa_attn_t h, unsigned long long timeout_ns) {

@@ -59,9 +59,9 @@ struct Cfg {
   static constexpr int P_BYTES = DIFF ? 4 * kTile : 0;
   static constexpr int OFF_P = OFF_V + NSV * V_STAGE;
   static constexpr int OFF_BAR = OFF_P + P_BYTES;
-  // barriers: q_full, k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2],
+  // barriers: q_full, q_ready[2], k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2],
   //           p_full[2], pv_done[2], s_free[2], o_full[2], drain[2], turn[2][4]
-  static constexpr int NBAR = 1 + 2 * NSK + 2 * NSV + 2 + 2 + 2 + 2 + 2 + 2 + 8;
+  static constexpr int NBAR = 1 + 2 + 2 * NSK + 2 * NSV + 2 + 2 + 2 + 2 + 2 + 2 + 8;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;           // tmem base, abort flag, ticket
   static constexpr int OFF_LSUM = OFF_MISC + 16;                // float [2][128]
   static constexpr int SMEM_USED = OFF_LSUM + 2 * kBlockM * 4;
@@ -76,8 +76,9 @@ static_assert(Cfg<true>::SMEM_ALLOC <= 227 * 1024, "smem budget");
 static_assert(Cfg<false>::SMEM_USED > 114 * 1024, "one CTA per SM keeps TMEM allocation uncontended");
 
 struct Barriers {
-  uint32_t q_full, k_full0, k_empty0, v_full0, v_empty0, s_full0, p_full0, pv_done0, s_free0, o_full0,
+  uint32_t q_full, q_ready0, k_full0, k_empty0, v_full0, v_empty0, s_full0, p_full0, pv_done0, s_free0, o_full0,
       drain0, turn0;
+  __device__ uint32_t q_ready(int s) const { return q_ready0 + 8 * s; }
   __device__ uint32_t k_full(int i) const { return k_full0 + 8 * i; }
   __device__ uint32_t k_empty(int i) const { return k_empty0 + 8 * i; }
   __device__ uint32_t v_full(int i) const { return v_full0 + 8 * i; }
@@ -144,6 +145,47 @@ __device__ __forceinline__ bool pwait_w(uint32_t bar, uint32_t parity, volatile 
   return __all_sync(0xffffffffu, pwait(bar, parity, abort_flag, err, err_bit, timeout_ns));
 }
 
+// RoPE prologue of one Q row (thread r of a softmax warpgroup): the TMA brought the tile in
+// raw; the row is rotated in place (128-byte-swizzled smem: 16-byte chunk c of row r sits at
+// c ^ (r & 7)), pairs [8g, 8g + 8) from chunks g and g + 4, with the RoPE pass's FP32
+// (cos, sin) of the row's position and the pre-pass's arithmetic.  Kept out of line so that its
+// registers do not weigh on the softmax loop's.  Returns the warp-uniform wait outcome.
+template <bool BF16>
+__device__ __noinline__ bool q_rope_prologue(const float2* cs, int L, int grow, uint32_t row, int r,
+                                             uint32_t q_full, volatile int* abort_flag, int* err,
+                                             uint64_t tmo) {
+  // the table is the RoPE pass's output: wait for that grid (programmatic dependent launch)
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the row's (cos, sin) pairs ([16][L] float4 table: a warp's loads are contiguous), loaded
+  // while the TMA brings Q
+  float4 t[16];
+  const float4* cs4 = reinterpret_cast<const float4*>(cs) + min(grow, L - 1);
+#pragma unroll
+  for (int m = 0; m < 16; ++m) t[m] = __ldg(cs4 + static_cast<size_t>(m) * L);
+  bool ok = pwait(q_full, 0, abort_flag, err, kErrSoftmax, tmo);
+  ok = __all_sync(0xffffffffu, ok);
+  if (ok && grow < L) {
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      float cg[8], sg[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        cg[2 * i] = t[4 * g + i].x;
+        sg[2 * i] = t[4 * g + i].y;
+        cg[2 * i + 1] = t[4 * g + i].z;
+        sg[2 * i + 1] = t[4 * g + i].w;
+      }
+      const uint32_t a_lo = row + ((g ^ (r & 7)) << 4), a_hi = row + (((g + 4) ^ (r & 7)) << 4);
+      const uint4 lo = ld_shared_v4(a_lo), hi = ld_shared_v4(a_hi);
+      uint4 olo, ohi;
+      rope_rotate8<BF16>(lo, hi, cg, sg, olo, ohi);
+      st_shared_v4(a_lo, olo.x, olo.y, olo.z, olo.w);
+      st_shared_v4(a_hi, ohi.x, ohi.y, ohi.z, ohi.w);
+    }
+  }
+  return ok;
+}
+
 template <bool DIFF, bool BF16>
 __global__ void __launch_bounds__(kFmhaThreads, 1)
     fmha_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -157,7 +199,8 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
 
   Barriers bar;
   bar.q_full = sb + C::OFF_BAR;
-  bar.k_full0 = bar.q_full + 8;
+  bar.q_ready0 = bar.q_full + 8;
+  bar.k_full0 = bar.q_ready0 + 16;
   bar.k_empty0 = bar.k_full0 + 8 * C::NSK;
   bar.v_full0 = bar.k_empty0 + 8 * C::NSK;
   bar.v_empty0 = bar.v_full0 + 8 * C::NSV;
@@ -207,6 +250,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(bar.q_full, 1);
+    for (int s = 0; s < 2; ++s) mbar_init(bar.q_ready(s), 4);   // one arrival per softmax warp
     for (int i = 0; i < C::NSK; ++i) {
       mbar_init(bar.k_full(i), 1);
       mbar_init(bar.k_empty(i), 2);    // one commit from each MMA issuer
@@ -252,7 +296,10 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     // This grid may have been started early (programmatic dependent launch) while the kernel
     // before it on the stream (the RoPE pass, which writes q', k') is still running: wait for
     // it before the first load.
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Raw q (the Q prologue case) is not written by the RoPE pass: load it, and warm L2 with the
+    // Q tiles of the CTA one wave later, before that wait.
+    const bool raw_q = a.cs != nullptr;
+    if (!raw_q) asm volatile("griddepcontrol.wait;" ::: "memory");
     const int plane_q = DIFF ? 2 * bh : bh;
     mbar_arrive_expect_tx_w(bar.q_full, C::Q_BYTES);
     if (DIFF) {
@@ -261,6 +308,17 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     } else {
       tma_load_3d_w(sQ, &tm_q, bar.q_full, 0, q0, plane_q);
       tma_load_3d_w(sQ + kTile, &tm_q, bar.q_full, 0, q0 + kBlockM, plane_q);
+    }
+    if (raw_q) {
+      const int c2 = static_cast<int>(blockIdx.x) + a.wave;
+      if (a.wave > 0 && c2 < static_cast<int>(gridDim.x) && lane == 0) {
+        const int u2 = c2 >= a.whole_ctas ? a.whole_ctas + (c2 - a.whole_ctas) / a.tail_k : c2;
+        const int bh2 = u2 / a.n_qblocks, q02 = (u2 % a.n_qblocks) * C::ROWS;
+        tma_prefetch_l2_3d(&tm_q, 0, q02, DIFF ? 2 * bh2 : bh2);
+        tma_prefetch_l2_3d(&tm_q, 0, DIFF ? q02 : q02 + kBlockM, DIFF ? 2 * bh2 + 1 : bh2);
+      }
+      __syncwarp();
+      asm volatile("griddepcontrol.wait;" ::: "memory");
     }
     int issued = 0;
     for (int it = 0; it < n_tiles; ++it) {
@@ -286,7 +344,8 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     __syncwarp();
   } else if (warp == kTmaWarpV) {
     // ------------------------------------------------------------------ V producer
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // v is not written by the RoPE pass, and the work before that pass on the stream has
+    // completed once this grid runs: no wait on the grid dependency.
     int issued = 0;
     for (int it = 0; it < n_tiles; ++it) {
       const int st = it % C::NSV;
@@ -333,7 +392,9 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         umma_commit_w(bar.s_full(s));
         umma_commit_w(bar.k_empty(st));
       };
-      bool ok = pwait_w(bar.q_full, 0, abort_flag, a.err, eb, tmo) && wait_k(0);
+      // Q tile s as the MMA reads it: straight from the TMA, or after the softmax warps' RoPE
+      const uint32_t q_bar = a.cs != nullptr ? bar.q_ready(s) : bar.q_full;
+      bool ok = pwait_w(q_bar, 0, abort_flag, a.err, eb, tmo) && wait_k(0);
       if (ok) {
         tc_fence_after();
         issue_s(0);
@@ -402,6 +463,14 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     // exponentials are issued, so one warp's max / TMEM / barrier work overlaps the other's
     // exponentials without waiting for the slowest warp of the other group.
     if (s == 1 && lane == 0) mbar_arrive(bar.turn(0, quarter));
+
+    if (a.cs != nullptr) {
+      // RoPE prologue on this warpgroup's Q tile, then the tile goes to its MMA issuer.
+      ok = q_rope_prologue<BF16>(a.cs, L, grow, sQ + s * kTile + r * 128, r, bar.q_full, abort_flag, a.err, tmo);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.q_ready(s));
+    }
 
     for (int it = 0; it < n_tiles; ++it) {
       ok = pwait(bar.s_full(s), it & 1, abort_flag, a.err, kErrSoftmax, tmo);

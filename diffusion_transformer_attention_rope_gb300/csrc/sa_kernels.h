@@ -33,10 +33,11 @@ constexpr int kErrSoftmax = 4;        // softmax / epilogue warps gave up on a w
 
 // RoPE pre-pass: rotate q and k (all planes) in FP32 and cast back to the storage dtype.
 struct RopeArgs {
-  const uint16_t* q;
+  const uint16_t* q;          // nullptr: k only (the attention kernel rotates q)
   const uint16_t* k;
   uint16_t* q_out;
   uint16_t* k_out;
+  float2* cs;                 // nullptr, or [L][32] (cos, sin) pairs written for the Q prologue
   const int32_t* positions;   // [L] or nullptr for 0..L-1
   long long planes;           // B * H * nmaps rows-of-L planes in q (and in k)
   int L;
@@ -62,7 +63,10 @@ struct FmhaArgs {
   float scale_log2;           // log2(e) / sqrt(d)
   int whole_ctas;             // CTAs that take a whole unit (the first ones)
   int tail_k;                 // pieces per tail unit (1: no pieces)
+  int wave;                   // CTAs resident at once (one per SM): the Q-prefetch distance
   unsigned epoch;             // nonzero, distinct for every launch (tags the unit counters)
+  const float2* cs;           // nullptr: q is already rotated; else q is raw and is rotated in the
+                              // prologue with this [L][32] (cos, sin) table of the RoPE pass
   unsigned long long* counters;  // tail_k > 1: [units] epoch-tagged piece counts
   float* partials;            // tail_k > 1: one slot of fmha_partial_floats per piece CTA
   unsigned long long timeout_ns;

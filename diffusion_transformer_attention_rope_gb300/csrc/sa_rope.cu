@@ -7,6 +7,9 @@
 // FP32 product and sin/cos are the full-precision single-precision functions: the sa3_trt
 // README ("Retired: bf16") shows what a low-precision angle does at long sequence lengths.
 //
+// With a table pointer the pass also writes each position's 32 (cos, sin) pairs (FP32), which
+// the attention kernel uses to rotate q in its prologue; q is then not touched here.
+//
 // One block rotates 32 positions of every plane in its slice of planes (a plane is one
 // (batch, head, map) sequence of L rows).  A thread owns 8 rotation pairs of one position
 // (two 16-byte chunks per row) and up to kPlaneBatch planes at a time: it issues all the loads
@@ -38,26 +41,8 @@ __device__ __forceinline__ void st_v4(uint16_t* p, uint4 v) {
                : "memory");
 }
 
-// Rotate 8 pairs: lo = x[8g .. 8g+8), hi = x[32+8g .. 32+8g+8).
-template <bool BF16>
-__device__ __forceinline__ void rotate(const uint4& lo, const uint4& hi, const float (&c)[8],
-                                       const float (&s)[8], uint4& out_lo, uint4& out_hi) {
-  const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w};
-  const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w};
-  uint32_t ol[4], oh[4];
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const float2 a = unpack2<BF16>(lw[j]);  // x_i, x_{i+1}
-    const float2 b = unpack2<BF16>(hw[j]);  // x_{i+32}, x_{i+33}
-    const int i0 = 2 * j, i1 = 2 * j + 1;
-    ol[j] = pack2<BF16>(fmaf(a.x, c[i0], -(b.x * s[i0])), fmaf(a.y, c[i1], -(b.y * s[i1])));
-    oh[j] = pack2<BF16>(fmaf(b.x, c[i0], a.x * s[i0]), fmaf(b.y, c[i1], a.y * s[i1]));
-  }
-  out_lo = make_uint4(ol[0], ol[1], ol[2], ol[3]);
-  out_hi = make_uint4(oh[0], oh[1], oh[2], oh[3]);
-}
-
-template <bool BF16>
+// WITH_Q: rotate q as well as k (false when the attention kernel rotates q in its prologue).
+template <bool BF16, bool WITH_Q>
 __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constant__ RopeArgs a) {
   // Let the dependent attention grid begin its prologue while this grid streams.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -80,8 +65,10 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constan
     for (int i = 0; i < kPlaneBatch; ++i) {
       if (i < n) {
         const size_t off = static_cast<size_t>(p0 + i) * row_stride + base;
-        qlo[i] = ld_stream(a.q + off);
-        qhi[i] = ld_stream(a.q + off + 32);
+        if (WITH_Q) {
+          qlo[i] = ld_stream(a.q + off);
+          qhi[i] = ld_stream(a.q + off + 32);
+        }
         klo[i] = ld_stream(a.k + off);
         khi[i] = ld_stream(a.k + off + 32);
       }
@@ -95,16 +82,27 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constan
         sincosf(theta, &s[i], &c[i]);
       }
       have_cs = true;
+      if (a.cs != nullptr && blockIdx.y == 0) {
+        // this position's pairs [8g, 8g + 8) of the (cos, sin) table for the Q prologue; the
+        // table is [16][L] float4 (pairs 2m and 2m + 1 of position l at [m][l]), so that the
+        // prologue's loads of consecutive rows are contiguous
+        float4* t = reinterpret_cast<float4*>(a.cs);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          t[static_cast<size_t>(4 * g + i) * a.L + l] = make_float4(c[2 * i], s[2 * i], c[2 * i + 1], s[2 * i + 1]);
+      }
     }
 #pragma unroll
     for (int i = 0; i < kPlaneBatch; ++i) {
       if (i < n) {
         const size_t off = static_cast<size_t>(p0 + i) * row_stride + base;
         uint4 lo, hi;
-        rotate<BF16>(qlo[i], qhi[i], c, s, lo, hi);
-        st_v4(a.q_out + off, lo);
-        st_v4(a.q_out + off + 32, hi);
-        rotate<BF16>(klo[i], khi[i], c, s, lo, hi);
+        if (WITH_Q) {
+          rope_rotate8<BF16>(qlo[i], qhi[i], c, s, lo, hi);
+          st_v4(a.q_out + off, lo);
+          st_v4(a.q_out + off + 32, hi);
+        }
+        rope_rotate8<BF16>(klo[i], khi[i], c, s, lo, hi);
         st_v4(a.k_out + off, lo);
         st_v4(a.k_out + off + 32, hi);
       }
@@ -115,14 +113,17 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constan
 }  // namespace
 
 int rope_blocks_per_sm() {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, rope_kernel<false>, kRopeThreads, 0) != cudaSuccess)
-    return 1;
-  int m = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&m, rope_kernel<true>, kRopeThreads, 0) != cudaSuccess)
-    return 1;
-  n = n < m ? n : m;
-  return n > 0 ? n : 1;
+  const void* fns[4] = {reinterpret_cast<const void*>(rope_kernel<false, true>),
+                        reinterpret_cast<const void*>(rope_kernel<true, true>),
+                        reinterpret_cast<const void*>(rope_kernel<false, false>),
+                        reinterpret_cast<const void*>(rope_kernel<true, false>)};
+  int least = 1 << 30;
+  for (const void* f : fns) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, f, kRopeThreads, 0) != cudaSuccess) return 1;
+    least = n < least ? n : least;
+  }
+  return least > 0 ? least : 1;
 }
 
 cudaError_t rope_launch(const RopeArgs& a_in, bool bf16, int num_sms, int blocks_per_sm,
@@ -145,10 +146,14 @@ cudaError_t rope_launch(const RopeArgs& a_in, bool bf16, int num_sms, int blocks
   }
   a.planes_per_block = static_cast<int>(ppb);
   const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(by));
-  if (bf16)
-    rope_kernel<true><<<grid, kRopeThreads, 0, stream>>>(a);
-  else
-    rope_kernel<false><<<grid, kRopeThreads, 0, stream>>>(a);
+  const bool with_q = a.q != nullptr;
+  if (bf16) {
+    if (with_q) rope_kernel<true, true><<<grid, kRopeThreads, 0, stream>>>(a);
+    else rope_kernel<true, false><<<grid, kRopeThreads, 0, stream>>>(a);
+  } else {
+    if (with_q) rope_kernel<false, true><<<grid, kRopeThreads, 0, stream>>>(a);
+    else rope_kernel<false, false><<<grid, kRopeThreads, 0, stream>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -85,11 +85,11 @@ SA_API sa_status sa_attn_create(sa_attn_t* handle, int device, float rope_base);
 SA_API sa_status sa_attn_destroy(sa_attn_t handle);
 
 /*
- * Bytes of device workspace sa_rope_attn needs for this shape: the rotated
- * and cast-back q and k (two buffers of B*H*nmaps*L*d elements of 2 bytes,
- * each rounded up to 256 bytes), followed by the split region of
- * sa_attn_fwd_workspace_size bytes.  differential != 0 selects nmaps = 2.
- * Returns 0 for invalid sizes.
+ * Bytes of device workspace sa_rope_attn needs for this shape: the FP32
+ * (cos, sin) table of sa_rope_table_bytes(L), the rotated and cast-back k
+ * (B*H*nmaps*L*d elements of 2 bytes), each rounded up to 256 bytes, followed
+ * by the split region of sa_attn_fwd_workspace_size bytes.  differential != 0
+ * selects nmaps = 2.  Returns 0 for invalid sizes.
  */
 SA_API size_t sa_rope_attn_workspace_size(int B, int H, int L, int d, int differential);
 
@@ -162,6 +162,42 @@ SA_API sa_status sa_rope_qk(sa_attn_t handle,
                             void* q_rot, void* k_rot,
                             int B, int H, int L, int d, int nmaps,
                             sa_dtype dtype, sa_stream_t stream);
+
+/*
+ * The two stages as sa_rope_attn runs them: the pre-pass rotates k only and
+ * the attention kernel rotates q in its prologue, as each Q tile arrives in
+ * shared memory.
+ *
+ * sa_rope_table_bytes: bytes of cs_table, L * 32 (cos, sin) pairs of FP32
+ *   (256 * L); 0 for invalid L.
+ * sa_rope_k: k_rot = cast(RoPE_fp32(k)) (the layout of k) and the table of
+ *   (cos, sin) of the FP32 angle fl(fl(p_l) * inv_freq[i]), i < 32,
+ *   p_l = positions[l] or l, as float4 cs_table[m][l] = (cos_2m, sin_2m,
+ *   cos_2m+1, sin_2m+1), m < 16 (rows of one pair-pair contiguous).
+ *   cs_table: device, 16-byte aligned.
+ * sa_attn_fwd_rope_q: attention (as sa_attn_fwd) on the raw q, rotated in the
+ *   kernel's prologue with cs_table in the pre-pass's arithmetic, so the output
+ *   has the same bits as sa_rope_qk followed by sa_attn_fwd; k_rot rotated
+ *   already; workspace the optional split region of sa_attn_fwd.
+ */
+SA_API size_t sa_rope_table_bytes(int L);
+
+SA_API sa_status sa_rope_k(sa_attn_t handle,
+                           const void* k,
+                           const int32_t* positions,
+                           void* k_rot, void* cs_table,
+                           int B, int H, int L, int d, int nmaps,
+                           sa_dtype dtype, sa_stream_t stream);
+
+SA_API sa_status sa_attn_fwd_rope_q(sa_attn_t handle,
+                                    const void* q, const void* k_rot, const void* cs_table,
+                                    const void* v, void* out,
+                                    int B, int H, int L, int d,
+                                    int window,
+                                    const float* lambda,
+                                    sa_dtype dtype,
+                                    void* workspace, size_t workspace_bytes,
+                                    sa_stream_t stream);
 
 /*
  * sa_attn_fwd: scaled-dot-product attention (softmax in FP32; differential

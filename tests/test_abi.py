@@ -65,11 +65,15 @@ def _split_bytes(B, H, L, diff):
 
 
 def test_workspace_size():
-    # two 256-byte-aligned buffers of B*H*nmaps*L*64 two-byte elements, then the split region
+    # the (cos, sin) table of L * 32 FP32 pairs, k' (B*H*nmaps*L*64 two-byte elements), each
+    # rounded up to 256 bytes, then the split region
+    assert sa.sa_rope_table_bytes(1292) == 1292 * 32 * 8
+    assert sa.sa_rope_table_bytes(0) == 0
     n = 1 * 16 * 1292 * 64 * 2
-    assert sa.sa_rope_attn_workspace_size(1, 16, 1292, 64, False) == 2 * _a256(n) + _split_bytes(1, 16, 1292, False)
+    assert sa.sa_rope_attn_workspace_size(1, 16, 1292, 64, False) == \
+        _a256(1292 * 256) + _a256(n) + _split_bytes(1, 16, 1292, False)
     n = 1 * 16 * 2 * 4096 * 64 * 2
-    assert sa.sa_rope_attn_workspace_size(1, 16, 4096, 64, True) == 2 * n + _split_bytes(1, 16, 4096, True)
+    assert sa.sa_rope_attn_workspace_size(1, 16, 4096, 64, True) == 4096 * 256 + n + _split_bytes(1, 16, 4096, True)
     assert sa.sa_attn_fwd_workspace_size(1, 24, 4096, 64, False) == _split_bytes(1, 24, 4096, False)
     assert sa.sa_attn_fwd_workspace_size(2, 3, 777, 64, True) == _split_bytes(2, 3, 777, True)
     assert sa.sa_rope_attn_workspace_size(1, 16, 4096, 128, True) == 0

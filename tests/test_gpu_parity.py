@@ -94,11 +94,14 @@ def test_rope_prepass_matches_oracle(attn, dtype):
     w = small("rope", B=2, H=3, L=300, dtype=dtype, seed=11)
     x = synth.make_inputs(w)
     pos = (np.arange(w.L) * 7 + 1000).astype(np.int32)
-    run_gpu(attn, x, positions=pos)
-    n = x["q"].size
-    ws = attn._ws[: 2 * ((n * 2 + 255) // 256 * 256)].cpu().numpy()
-    q_rot = ws[: n * 2].view(np.uint16)
-    k_rot = ws[(n * 2 + 255) // 256 * 256:][: n * 2].view(np.uint16)
+    q, k = dev(x["q"], dtype), dev(x["k"], dtype)
+    qr, kr = torch.empty_like(q), torch.empty_like(k)
+    sa.sa_rope_qk(attn.handle, q.data_ptr(), k.data_ptr(), torch.from_numpy(pos).cuda().data_ptr(),
+                  qr.data_ptr(), kr.data_ptr(), w.B, w.H, w.L, 64, 1,
+                  sa.SA_BF16 if dtype == "bf16" else sa.SA_FP16, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    q_rot = qr.view(torch.int16).cpu().numpy().view(np.uint16).ravel()
+    k_rot = kr.view(torch.int16).cpu().numpy().view(np.uint16).ravel()
     freq = oracle.rope(np.eye(64)[:32], np.ones(32, dtype=np.int32))
     omega = np.arctan2(freq[np.arange(32), np.arange(32) + 32], freq[np.arange(32), np.arange(32)])
     theta = np.abs(pos.astype(np.float64)[:, None] * omega[None, :])          # [L, 32]
@@ -113,6 +116,47 @@ def test_rope_prepass_matches_oracle(attn, dtype):
         assert np.all(np.abs(got - exact) <= bound)
         cast = oracle.round_to(exact, dtype)
         assert (got == cast).mean() > 0.95
+
+
+@pytest.mark.parametrize("diff,dtype,window", [(False, "fp16", -1), (True, "bf16", 129)])
+def test_q_rope_prologue_matches_prepass(attn, diff, dtype, window):
+    # sa_rope_attn rotates k in the pre-pass and q in the attention kernel's prologue, from the
+    # pass's FP32 (cos, sin) table: k' and the output must have the bits of the two-pass path
+    # (sa_rope_qk, then sa_attn_fwd on q'), and the table the FP32 angle's cos and sin.
+    w = small("qrope", B=1, H=3, L=777, window=window, nmaps=2 if diff else 1, dv=128 if diff else 64,
+              dtype=dtype, seed=33, lam=("uniform", 0.2, 0.8) if diff else None)
+    x = synth.make_inputs(w)
+    B, H, L, nm = w.B, w.H, w.L, w.nmaps
+    q, k, v = dev(x["q"], dtype), dev(x["k"], dtype), dev(x["v"], dtype)
+    pos = torch.from_numpy(((np.arange(L) * 5) % 3001 + 17).astype(np.int32)).cuda()
+    lam = None if x["lam"] is None else [float(t) for t in x["lam"]]
+    dt = sa.SA_BF16 if dtype == "bf16" else sa.SA_FP16
+    s = torch.cuda.current_stream().cuda_stream
+    h = attn.handle
+    qr, kr, kr2 = torch.empty_like(q), torch.empty_like(k), torch.empty_like(k)
+    cs = torch.empty(sa.sa_rope_table_bytes(L) // 4, dtype=torch.float32, device="cuda")
+    split = torch.empty(sa.sa_attn_fwd_workspace_size(B, H, L, 64, diff), dtype=torch.uint8, device="cuda")
+    o1 = torch.empty((B, H, L, w.dv), dtype=TDT[dtype], device="cuda")
+    o2 = torch.empty_like(o1)
+    sa.sa_rope_qk(h, q.data_ptr(), k.data_ptr(), pos.data_ptr(), qr.data_ptr(), kr.data_ptr(), B, H, L, 64, nm, dt, s)
+    sa.sa_attn_fwd(h, qr.data_ptr(), kr.data_ptr(), v.data_ptr(), o1.data_ptr(), B, H, L, 64, window, lam, dt, s,
+                   split.data_ptr(), split.numel())
+    sa.sa_rope_k(h, k.data_ptr(), pos.data_ptr(), kr2.data_ptr(), cs.data_ptr(), B, H, L, 64, nm, dt, s)
+    sa.sa_attn_fwd_rope_q(h, q.data_ptr(), kr2.data_ptr(), cs.data_ptr(), v.data_ptr(), o2.data_ptr(),
+                          B, H, L, 64, window, lam, dt, s, split.data_ptr(), split.numel())
+    torch.cuda.synchronize()
+    attn.check()
+    assert torch.equal(kr.view(torch.int16), kr2.view(torch.int16))
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    # the table: cos and sin of the FP32 angle fl(fl(p) * inv_freq_i), to a few ulp
+    inv = (10000.0 ** (-2.0 * np.arange(32) / 64.0)).astype(np.float32)
+    ang = (pos.cpu().numpy().astype(np.float32)[:, None] * inv[None, :]).astype(np.float64)
+    # [16][L] float4 (cos_2m, sin_2m, cos_2m+1, sin_2m+1) -> [L][32][2]
+    t = cs.cpu().numpy().reshape(16, L, 2, 2).transpose(1, 0, 2, 3).reshape(L, 32, 2).astype(np.float64)
+    assert np.abs(t[..., 0] - np.cos(ang)).max() < 1e-6
+    assert np.abs(t[..., 1] - np.sin(ang)).max() < 1e-6
+    x["positions"] = pos.cpu().numpy()
+    compare(o2.float().cpu().numpy(), oracle.rope_attn_workload(x), "q prologue", dtype=dtype)
 
 
 # ----------------------------------------------------------------------------- full outputs
