@@ -143,14 +143,11 @@ sa_status launch_rope(const sa_attn_s* h, const void* q, const void* k, const in
 
 // Key tiles visited by query block qb (the kernel's own rule).
 int block_tiles_host(int L, int window, int rows, int qb) {
-  int lo = 0, hi = (L - 1) / sa::kBlockN;
-  if (window >= 0) {
-    const int q0 = qb * rows;
-    const int q_last = std::min(L, q0 + rows) - 1;
-    lo = std::max(0, q0 - window) / sa::kBlockN;
-    hi = std::min(L - 1, q_last + window) / sa::kBlockN;
-  }
-  return hi - lo + 1;
+  if (window < 0) return (L - 1) / sa::kBlockN + 1;
+  const int q0 = qb * rows;
+  const int q_last = std::min(L, q0 + rows) - 1;
+  const int first = std::max(0, q0 - window);
+  return (std::min(L - 1, q_last + window) - first) / sa::kBlockN + 1;
 }
 
 // Every launch gets its own epoch: it tags the unit counters of the split region, so they

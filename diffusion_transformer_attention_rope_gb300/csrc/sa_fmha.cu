@@ -230,10 +230,13 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
   const int w = a.window;
 
   // K/V tiles this CTA visits.
-  int t_lo = 0, t_hi = (L - 1) / kBlockN;
+  // Keys [k_first, k_first + 128 n) in 128-key tiles: all keys, or the unit's window span
+  // [q0 - w, q_last + w] clipped to [0, L - 1], tiled from its first key (a TMA box may start at
+  // any row), which visits ceil(span / 128) tiles rather than every 128-aligned tile it touches.
+  int k_first = 0, t_lo = 0, t_hi = (L - 1) / kBlockN;
   if (w >= 0) {
-    t_lo = max(0, q0 - w) / kBlockN;
-    t_hi = min(L - 1, q_last + w) / kBlockN;
+    k_first = max(0, q0 - w);
+    t_hi = (min(L - 1, q_last + w) - k_first) / kBlockN;
   }
   if (piece) {
     // piece k of tail_k: tiles [t_lo + k nt / tail_k, t_lo + (k + 1) nt / tail_k), never empty
@@ -325,7 +328,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       const int st = it % C::NSK;
       if (!pwait_w(bar.k_empty(st), ((it / C::NSK) & 1) ^ 1, abort_flag, a.err, kErrProducer, tmo))
         break;
-      const int key0 = (t_lo + it) * kBlockN;
+      const int key0 = k_first + (t_lo + it) * kBlockN;
       const uint32_t k_dst = sK + st * C::K_STAGE;
       mbar_arrive_expect_tx_w(bar.k_full(st), C::K_STAGE);
       if (DIFF) {
@@ -351,7 +354,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       const int st = it % C::NSV;
       if (!pwait_w(bar.v_empty(st), ((it / C::NSV) & 1) ^ 1, abort_flag, a.err, kErrProducer, tmo))
         break;
-      const int key0 = (t_lo + it) * kBlockN;
+      const int key0 = k_first + (t_lo + it) * kBlockN;
       const uint32_t v_dst = sV + st * C::V_STAGE;
       mbar_arrive_expect_tx_w(bar.v_full(st), C::V_STAGE);
       tma_load_3d_w(v_dst, &tm_v, bar.v_full(st), 0, key0, bh);
@@ -490,7 +493,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         if (lane == 0) mbar_arrive(bar.s_free(s));
       }
 
-      const int key0 = (t_lo + it) * kBlockN;
+      const int key0 = k_first + (t_lo + it) * kBlockN;
       const bool need_mask =
           (key0 + kBlockN > L) ||
           (w >= 0 && !(key0 >= rows_hi - w && key0 + kBlockN - 1 <= rows_lo + w));

@@ -67,6 +67,10 @@ WORKLOADS = {
                  seed=3, lam=("const", 0.8)),
         Workload("swa_diff_l8192", B=1, H=16, L=8192, nmaps=2, dv=128, dtype="bf16",
                  window=256, seed=4, lam=("uniform", 0.2, 0.8)),
+        # SAME-L's own window, +-17 (HF discussion #6 "sm_120 SAME-L", "Three gotchas"), on the
+        # shape of the window workload above: a measurement case beyond the five configurations
+        Workload("swa17_diff_l8192", B=1, H=16, L=8192, nmaps=2, dv=128, dtype="bf16",
+                 window=17, seed=5, lam=("uniform", 0.2, 0.8)),
     ]
 }
 

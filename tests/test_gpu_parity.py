@@ -228,14 +228,17 @@ def sample_rows(w, rng, per_head_random=6):
     return np.array(rows, dtype=np.int64)
 
 
-@pytest.mark.parametrize("name", ["dit_l1292", "dit_l4096_outliers", "diff_l4096", "swa_diff_l8192"])
+@pytest.mark.parametrize("name", ["dit_l1292", "dit_l4096_outliers", "diff_l4096", "swa_diff_l8192",
+                                  "swa17_diff_l8192"])
 def test_full_size_workload(attn, name):
     w = synth.WORKLOADS[name]
     x = synth.make_inputs(w)
     got = run_gpu(attn, x)
     rows = sample_rows(w, np.random.default_rng(700))
     ref = oracle.rope_attn_workload(x, rows=rows)
-    compare(got.reshape(-1, w.dv)[rows], ref, name)
+    # the five target workloads take the strict bar; the +-17 window case (outputs averaged over
+    # 35 keys reach |o| >= 1, where bf16's own rounding is up to 2^-8) the edge cases' form
+    compare(got.reshape(-1, w.dv)[rows], ref, name, dtype=w.dtype if name == "swa17_diff_l8192" else None)
     # property at every row: out is a convex combination of v rows (standard), or a
     # difference of two such (differential), so |out| <= (1 + lambda) max |v| per column.
     g = got.reshape(w.B, w.H, w.L, w.dv)
@@ -357,11 +360,13 @@ def pieces_per_tail_unit(B, H, L, window, diff):
     w = -1 if window < 0 or window >= L - 1 else window
     nts = []
     for qb in range(nqb):
-        lo, hi = 0, (L - 1) // 128
-        if w >= 0:
+        if w < 0:
+            nts.append((L - 1) // 128 + 1)
+        else:
+            # the block's window span, tiled from its first key
             q0 = qb * rows
-            lo, hi = max(0, q0 - w) // 128, min(L - 1, min(L, q0 + rows) - 1 + w) // 128
-        nts.append(hi - lo + 1)
+            first = max(0, q0 - w)
+            nts.append((min(L - 1, min(L, q0 + rows) - 1 + w) - first) // 128 + 1)
     return min(sms // tail, min(nts), 4)
 
 
@@ -369,7 +374,7 @@ def pieces_per_tail_unit(B, H, L, window, diff):
     (1, 3, 1000, -1, False, "fp16"),    # 12 units, 4 pieces of two key tiles each
     (2, 2, 777, 129, False, "bf16"),    # window: pieces whose tiles miss some rows' windows
     (1, 2, 900, -1, True, "bf16"),      # differential: merged O of both maps
-    (1, 1, 1200, 17, True, "bf16"),     # differential, narrow window
+    (1, 1, 1280, 17, True, "bf16"),     # differential, narrow window (every block 2 tiles)
     (1, 2, 4096, -1, False, "fp16"),    # long rows: 4 pieces of 8 key tiles
     (1, 1, 700, 0, False, "fp16"),      # window 0: units of one key tile are never cut
 ])
