@@ -13,10 +13,14 @@ Functions and what they follow:
                      casts back; here FP64 without a cast).
 * ``round_to``    -- round-to-nearest-even cast to fp16 / bf16 (the cast-back of
                      ``t.to(out_dtype)`` in the same section).
+* ``rmsnorm``     -- FP64 RMSNorm of a row over the head dim with a learned
+                     gamma (the FP32 "RMSNorm islands" kept around attention,
+                     sa3_trt README "Notes on the design").
 * ``rope_attn``   -- the full core: RoPE, cast-back, exact two-pass softmax
                      attention, the differential subtraction (HF discussion #6,
                      "How the kernels differ") and the symmetric sliding window
-                     (same page, "Three gotchas").
+                     (same page, "Three gotchas"); optionally RMSNorm of every
+                     q and k row before RoPE.
 
 Every function is pinned by ``tests/test_oracle_pins.py`` against library
 routines (numpy fp16 casts, torch float64 SDPA), closed forms and invariants.
@@ -76,6 +80,16 @@ def _load():
                 ctypes.c_int, P(ctypes.c_double), ctypes.c_int, ctypes.c_int, ctypes.c_double,
                 P(ctypes.c_int64), ctypes.c_int64, P(ctypes.c_double), ctypes.c_int]
             lib.sa_oracle_rope_attn.restype = ctypes.c_int
+            lib.sa_oracle_rope_attn_qknorm.argtypes = [
+                P(ctypes.c_uint16), P(ctypes.c_uint16), P(ctypes.c_uint16), P(ctypes.c_int32),
+                ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                ctypes.c_int, P(ctypes.c_double), ctypes.c_int, ctypes.c_int, ctypes.c_double,
+                ctypes.c_int, P(ctypes.c_double), P(ctypes.c_double), ctypes.c_double,
+                P(ctypes.c_int64), ctypes.c_int64, P(ctypes.c_double), ctypes.c_int]
+            lib.sa_oracle_rope_attn_qknorm.restype = ctypes.c_int
+            lib.sa_oracle_rmsnorm.argtypes = [P(ctypes.c_double), ctypes.c_int64, ctypes.c_int,
+                                              P(ctypes.c_double), ctypes.c_double, P(ctypes.c_double)]
+            lib.sa_oracle_rmsnorm.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -107,6 +121,23 @@ def rope(x: np.ndarray, positions: Optional[np.ndarray] = None, base: float = 10
     return y.reshape(x.shape)
 
 
+def rmsnorm(x: np.ndarray, gamma: Optional[np.ndarray] = None, eps: float = 1e-6) -> np.ndarray:
+    """FP64 RMSNorm of rows x[..., d]: x * gamma / sqrt(mean(x^2) + eps) (gamma None: ones)."""
+    lib = _load()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    flat = x.reshape(-1, d)
+    g = None if gamma is None else np.ascontiguousarray(gamma, dtype=np.float64).reshape(-1)
+    if g is not None and g.shape[0] != d:
+        raise ValueError("gamma must have d entries")
+    y = np.empty_like(flat)
+    rc = lib.sa_oracle_rmsnorm(_ptr(flat, ctypes.c_double), flat.shape[0], d, _ptr(g, ctypes.c_double),
+                               float(eps), _ptr(y, ctypes.c_double))
+    if rc != 0:
+        raise ValueError(f"sa_oracle_rmsnorm failed ({rc})")
+    return y.reshape(x.shape)
+
+
 def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
     """Round doubles to the nearest fp16/bf16 value (ties to even), returned as double."""
     lib = _load()
@@ -127,12 +158,14 @@ def rope_attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, B: int, H: int, L:
               nmaps: int = 1, dv: int = 64, dtype: str = "fp16", window: int = -1,
               lam: Optional[np.ndarray] = None, positions: Optional[np.ndarray] = None,
               cast: str = "method", base: float = 10000.0, rows: Optional[np.ndarray] = None,
-              threads: Optional[int] = None) -> np.ndarray:
+              threads: Optional[int] = None, qk_norm: Optional[tuple] = None) -> np.ndarray:
     """RoPE + attention core in FP64.
 
     q, k: uint16 bits, [B, H, L, d] (nmaps=1) or [B, H, 2, L, d] (nmaps=2);
     v: uint16 bits [B, H, L, dv].  rows: flattened ids (b*H + h)*L + i, or None
-    for every row.  Returns double [len(rows), dv] (or [B, H, L, dv] for None).
+    for every row.  qk_norm: None, or (gamma_q, gamma_k, eps) to RMSNorm every q
+    and k row before RoPE (a gamma of None means ones).  Returns double
+    [len(rows), dv] (or [B, H, L, dv] for None).
     """
     lib = _load()
     q = np.ascontiguousarray(q, dtype=np.uint16)
@@ -151,10 +184,19 @@ def rope_attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, B: int, H: int, L:
     r = None if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
     nrows = B * H * L if r is None else r.shape[0]
     out = np.empty((nrows, dv), dtype=np.float64)
-    rc = lib.sa_oracle_rope_attn(
+    gq = gk = None
+    eps = 0.0
+    if qk_norm is not None:
+        gq, gk, eps = qk_norm
+        gq = None if gq is None else np.ascontiguousarray(gq, dtype=np.float64).reshape(-1)
+        gk = None if gk is None else np.ascontiguousarray(gk, dtype=np.float64).reshape(-1)
+        if (gq is not None and gq.shape[0] != d) or (gk is not None and gk.shape[0] != d):
+            raise ValueError("gamma must have d entries")
+    rc = lib.sa_oracle_rope_attn_qknorm(
         _ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16),
         _ptr(pos, ctypes.c_int32), B, H, L, d, nmaps, dv, int(window), _ptr(lam64, ctypes.c_double),
-        DTYPES[dtype], CASTS[cast], float(base), _ptr(r, ctypes.c_int64), nrows,
+        DTYPES[dtype], CASTS[cast], float(base), int(qk_norm is not None), _ptr(gq, ctypes.c_double),
+        _ptr(gk, ctypes.c_double), float(eps), _ptr(r, ctypes.c_int64), nrows,
         _ptr(out, ctypes.c_double), int(threads or default_threads()))
     if rc != 0:
         raise ValueError(f"sa_oracle_rope_attn failed ({rc})")
@@ -164,9 +206,10 @@ def rope_attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, B: int, H: int, L:
 
 
 def rope_attn_workload(inputs: dict, rows: Optional[np.ndarray] = None, cast: str = "method",
-                       threads: Optional[int] = None) -> np.ndarray:
+                       threads: Optional[int] = None, qk_norm: Optional[tuple] = None) -> np.ndarray:
     """Convenience: run the oracle on a ``synth.make_inputs`` dict."""
     w = inputs["workload"]
     return rope_attn(inputs["q"], inputs["k"], inputs["v"], B=w.B, H=w.H, L=w.L, d=w.d,
                      nmaps=w.nmaps, dv=w.dv, dtype=w.dtype, window=w.window, lam=inputs["lam"],
-                     positions=inputs["positions"], cast=cast, rows=rows, threads=threads)
+                     positions=inputs["positions"], cast=cast, rows=rows, threads=threads,
+                     qk_norm=qk_norm)

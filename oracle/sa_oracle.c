@@ -31,6 +31,12 @@
  *      symmetric); window < 0 means full attention.  Only keys in
  *      [max(0, i-w), min(L-1, i+w)] are visited; masked keys contribute
  *      exp(-inf) = 0, so this is exact.
+ *   6. Optional QK-RMSNorm before RoPE (the pages keep "RMSNorm + RoPE
+ *      around attention" as FP32 islands that guard variance overflow; sa3_trt
+ *      README "Notes on the design" and the encoder/decoder page's "Where the
+ *      quantization goes, per tier"): every q and k row of d values becomes
+ *      x_c * gamma_c / sqrt(mean_c(x_c^2) + eps), with one learned gamma[d]
+ *      for q and one for k, then RoPE, then the single cast-back of step 2.
  *
  * Layouts (C order): q, k [B][H][nmaps][L][d]; v [B][H][L][dv];
  * output rows [nrows][dv] in double.
@@ -135,6 +141,30 @@ static void rope_row(const double* x, double* y, int d, double p, double base)
     }
 }
 
+/* ---------------------------------------------------------------- RMSNorm (FP64) */
+
+/* y = x * gamma / sqrt(mean(x^2) + eps) over one row of d values (gamma NULL: all ones).
+ * y may alias x. */
+static void rmsnorm_row(const double* x, double* y, int d, const double* gamma, double eps)
+{
+    double ss = 0.0;
+    for (int c = 0; c < d; ++c)
+        ss += x[c] * x[c];
+    double inv = 1.0 / sqrt(ss / (double)d + eps);
+    for (int c = 0; c < d; ++c)
+        y[c] = x[c] * inv * (gamma ? gamma[c] : 1.0);
+}
+
+/* Public: RMSNorm of n rows of x[n][d]. */
+int sa_oracle_rmsnorm(const double* x, int64_t n, int d, const double* gamma, double eps, double* y)
+{
+    if (d <= 0 || !(eps >= 0.0))
+        return -1;
+    for (int64_t r = 0; r < n; ++r)
+        rmsnorm_row(x + r * d, y + r * d, d, gamma, eps);
+    return 0;
+}
+
 /* Public: rotate n rows of x[n][d] at positions pos[n] (NULL: 0..n-1). */
 int sa_oracle_rope(const double* x, const int32_t* pos, int64_t n, int d, double base, double* y)
 {
@@ -154,6 +184,9 @@ typedef struct {
     int B, H, L, d, nmaps, dv, window, dtype, cast_mode;
     const double* lambda;
     double base;
+    int qk_norm;                    /* 1: RMSNorm of q and k rows before RoPE */
+    const double *gamma_q, *gamma_k;
+    double eps;
     const int64_t* rows;
     int64_t nrows;
     double* out;
@@ -199,6 +232,8 @@ static int prepare_head(job_t* J, int64_t bh)
         for (int l = 0; l < L; ++l) {
             for (int c = 0; c < d; ++c)
                 row[c] = bits_to_double(ksrc[(size_t)l * d + c], J->dtype);
+            if (J->qk_norm)
+                rmsnorm_row(row, row, d, J->gamma_k, J->eps);
             double* dst = kr + ((size_t)m * L + l) * d;
             rope_row(row, dst, d, pos_of(J, l), J->base);
             for (int c = 0; c < d; ++c)
@@ -283,6 +318,8 @@ static void* worker(void* arg)
             const uint16_t* qsrc = J->q + ((((size_t)bh * nm + m) * L) + i) * d;
             for (int c = 0; c < d; ++c)
                 qraw[c] = bits_to_double(qsrc[c], J->dtype);
+            if (J->qk_norm)
+                rmsnorm_row(qraw, qraw, d, J->gamma_q, J->eps);
             rope_row(qraw, qr, d, pos_of(J, i), J->base);
             for (int c = 0; c < d; ++c)
                 qr[c] = cast_back(qr[c], J);
@@ -300,18 +337,23 @@ static void* worker(void* arg)
 }
 
 /*
- * Public entry.  rows: flattened row ids (b*H + h)*L + i, or NULL for all
- * B*H*L rows in order.  lambda: [H] (required when nmaps == 2).
+ * Public entry with the optional QK-RMSNorm.  rows: flattened row ids
+ * (b*H + h)*L + i, or NULL for all B*H*L rows in order.  lambda: [H] (required
+ * when nmaps == 2).  qk_norm != 0: gamma_q, gamma_k [d] (NULL: all ones) and
+ * eps >= 0 normalise every q and k row before RoPE.
  * Returns 0 on success, a negative code on bad arguments or allocation failure.
  */
-int sa_oracle_rope_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
-                        const int32_t* positions, int B, int H, int L, int d, int nmaps,
-                        int dv, int window, const double* lambda, int dtype, int cast_mode,
-                        double base, const int64_t* rows, int64_t nrows, double* out,
-                        int nthreads)
+int sa_oracle_rope_attn_qknorm(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                               const int32_t* positions, int B, int H, int L, int d, int nmaps,
+                               int dv, int window, const double* lambda, int dtype, int cast_mode,
+                               double base, int qk_norm, const double* gamma_q,
+                               const double* gamma_k, double eps, const int64_t* rows,
+                               int64_t nrows, double* out, int nthreads)
 {
     if (!q || !k || !v || !out || B <= 0 || H <= 0 || L <= 0 || d <= 0 || (d & 1) || dv <= 0)
         return -1;
+    if (qk_norm && !(eps >= 0.0))
+        return -8;
     if (nmaps != 1 && nmaps != 2)
         return -2;
     if (nmaps == 2 && !lambda)
@@ -333,6 +375,7 @@ int sa_oracle_rope_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     J.B = B; J.H = H; J.L = L; J.d = d; J.nmaps = nmaps; J.dv = dv;
     J.window = window; J.dtype = dtype; J.cast_mode = cast_mode; J.lambda = lambda;
     J.base = base; J.rows = rows; J.nrows = nrows; J.out = out;
+    J.qk_norm = qk_norm != 0; J.gamma_q = gamma_q; J.gamma_k = gamma_k; J.eps = eps;
     int64_t nbh = (int64_t)B * H;
     J.kr = (double**)calloc((size_t)nbh, sizeof(double*));
     J.vd = (double**)calloc((size_t)nbh, sizeof(double*));
@@ -364,4 +407,16 @@ int sa_oracle_rope_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
     free(J.kr); free(J.vd); free(J.head_lock);
     pthread_mutex_destroy(&J.lock);
     return J.failed ? -7 : 0;
+}
+
+/* Public entry without the QK-RMSNorm (the attention core as the pages describe it). */
+int sa_oracle_rope_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+                        const int32_t* positions, int B, int H, int L, int d, int nmaps,
+                        int dv, int window, const double* lambda, int dtype, int cast_mode,
+                        double base, const int64_t* rows, int64_t nrows, double* out,
+                        int nthreads)
+{
+    return sa_oracle_rope_attn_qknorm(q, k, v, positions, B, H, L, d, nmaps, dv, window, lambda,
+                                      dtype, cast_mode, base, 0, NULL, NULL, 0.0, rows, nrows,
+                                      out, nthreads);
 }

@@ -420,6 +420,95 @@ def test_window_at_least_l_minus_one_is_full(oracle_mod):
 
 # ----------------------------------------------------------------------------- plumbing
 
+# ----------------------------------------------------------------------------- QK-RMSNorm
+
+def test_rmsnorm_matches_torch_rms_norm(oracle_mod):
+    # library routine: torch's float64 rms_norm with a weight.  catches: sum
+    # instead of mean, eps outside the square root, a missing weight.
+    rng = np.random.default_rng(40)
+    x = rng.standard_normal((33, 64)) * np.exp(rng.uniform(-6, 6, (33, 1)))
+    g = rng.uniform(0.5, 1.5, 64)
+    for eps in (0.0, 1e-6, 1e-2):
+        got = oracle_mod.rmsnorm(x, g, eps)
+        ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (64,), weight=torch.from_numpy(g),
+                                           eps=eps).numpy()
+        np.testing.assert_allclose(got, ref, rtol=1e-13, atol=0)
+
+
+def test_rmsnorm_closed_forms(oracle_mod):
+    # eps = 0, gamma = 1: unit mean square and invariance to a positive row scale;
+    # a constant row c gives c / sqrt(c^2 + eps) in every entry; a zero row stays 0.
+    rng = np.random.default_rng(41)
+    x = rng.standard_normal((9, 64))
+    y = oracle_mod.rmsnorm(x, None, 0.0)
+    np.testing.assert_allclose(np.mean(y * y, axis=1), 1.0, rtol=1e-14)
+    np.testing.assert_allclose(oracle_mod.rmsnorm(x * 1234.5, None, 0.0), y, rtol=1e-13, atol=1e-15)
+    for c in (3.0, -0.25, 6.0e4):
+        row = np.full((1, 64), c)
+        np.testing.assert_allclose(oracle_mod.rmsnorm(row, None, 1e-6), c / math.sqrt(c * c + 1e-6),
+                                   rtol=1e-15)
+    assert np.all(oracle_mod.rmsnorm(np.zeros((1, 64)), None, 1e-6) == 0.0)
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_qknorm_then_rope_then_cast_then_sdpa(oracle_mod, dtype):
+    # composition: RMSNorm (pinned above) -> RoPE (pinned) -> RNE cast (library
+    # casts) -> torch SDPA equals the oracle's pipeline with qk_norm.  Distinct,
+    # non-uniform gammas for q and k make the order (norm before RoPE), the
+    # tensor each gamma belongs to, and eps (small-magnitude rows) all matter;
+    # fp16 rows near 6e4 would overflow a 16-bit sum of squares.
+    rng = np.random.default_rng(42)
+    B, H, L = 1, 2, 40
+    q, k, v = _std_case(rng, B, H, L, dtype)
+    scale = np.exp(rng.uniform(-9, 10, (B, H, L, 1)))
+    qd = np.clip(_decode64(q, dtype) * scale, -6.0e4, 6.0e4)
+    q = synth.encode(qd.astype(np.float32), dtype)
+    pos = np.arange(L, dtype=np.int32) * 13 + 2
+    gq = rng.uniform(0.25, 2.0, 64)
+    gk = rng.uniform(0.25, 2.0, 64)
+    eps = 1e-6
+    cast = (lambda a: a.astype(np.float16).astype(np.float64)) if dtype == "fp16" else \
+        (lambda a: oracle_mod.round_to(a, "bf16"))
+
+    def prep(bits, g):
+        n = oracle_mod.rmsnorm(_decode64(bits, dtype).reshape(-1, 64), g, eps)
+        return cast(oracle_mod.rope(n, np.tile(pos, B * H)).reshape(bits.shape))
+
+    ref = _sdpa64(prep(q, gq), prep(k, gk), _decode64(v, dtype))
+    got = oracle_mod.rope_attn(q, k, v, B=B, H=H, L=L, dtype=dtype, positions=pos, qk_norm=(gq, gk, eps))
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+    swapped = oracle_mod.rope_attn(q, k, v, B=B, H=H, L=L, dtype=dtype, positions=pos,
+                                   qk_norm=(gk, gq, eps))
+    assert np.abs(swapped - got).max() > 1e-3
+    plain = oracle_mod.rope_attn(q, k, v, B=B, H=H, L=L, dtype=dtype, positions=pos)
+    assert np.abs(plain - got).max() > 1e-2
+
+
+def test_qknorm_differential_and_window(oracle_mod):
+    # the norm applies to both maps of q and k; windowed rows agree with a
+    # masked torch SDPA on the normalised, rotated, cast operands.
+    rng = np.random.default_rng(43)
+    B, H, L, w = 1, 2, 33, 5
+    q, k, v = _diff_case(rng, B, H, L)
+    lam = rng.uniform(0.2, 0.8, H)
+    gq, gk, eps = rng.uniform(0.5, 1.5, 64), rng.uniform(0.5, 1.5, 64), 1e-6
+    cast = lambda a: oracle_mod.round_to(a, "bf16")
+
+    def prep(bits, g):
+        n = oracle_mod.rmsnorm(_decode64(bits, "bf16").reshape(-1, 64), g, eps)
+        return cast(oracle_mod.rope(n, np.tile(np.arange(L, dtype=np.int32), B * H * 2)).reshape(bits.shape))
+
+    qn, kn = prep(q, gq), prep(k, gk)
+    vd = _decode64(v, "bf16")
+    mask = _window_mask(L, w)
+    o1 = _sdpa64(qn[:, :, 0], kn[:, :, 0], vd, mask)
+    o2 = _sdpa64(qn[:, :, 1], kn[:, :, 1], vd, mask)
+    ref = o1 - np.asarray(lam).reshape(1, H, 1, 1) * o2
+    got = oracle_mod.rope_attn(q, k, v, B=B, H=H, L=L, nmaps=2, dv=128, dtype="bf16", window=w,
+                               lam=lam, qk_norm=(gq, gk, eps))
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-13)
+
+
 def test_row_subset_and_threads_are_consistent(oracle_mod):
     rng = np.random.default_rng(32)
     B, H, L = 2, 2, 30
