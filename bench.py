@@ -253,7 +253,16 @@ def row_flops(w, rows: np.ndarray) -> int:
     return int(keys.sum()) * w.nmaps * (2 * w.d + 2 * w.dv)
 
 
-def oracle_sample(w, x, budget_s: float, rng, threads=None):
+def qk_norm_params(enabled: bool):
+    """The QK-RMSNorm of --qk-norm: seeded gammas ~ U(0.5, 1.5) for q and k, eps 1e-6 (the
+    pages give no values; these stand in for learned weights)."""
+    if not enabled:
+        return None
+    rng = np.random.default_rng(60)
+    return (rng.uniform(0.5, 1.5, 64).astype(np.float32), rng.uniform(0.5, 1.5, 64).astype(np.float32), 1e-6)
+
+
+def oracle_sample(w, x, budget_s: float, rng, threads=None, qk_norm=None):
     """Time the FP64 oracle on a random row sample sized to ~budget_s of work.
     Returns (tflops, seconds, rows_done, threads)."""
     import oracle
@@ -261,14 +270,15 @@ def oracle_sample(w, x, budget_s: float, rng, threads=None):
     oracle.build()
     threads = threads or oracle.default_threads()
     total = w.B * w.H * w.L
+    nrm = None if qk_norm is None else (qk_norm[0].astype(np.float64), qk_norm[1].astype(np.float64), qk_norm[2])
     probe = rng.choice(total, size=min(total, max(64, total // 200)), replace=False)
     t0 = time.perf_counter()
-    oracle.rope_attn_workload(x, rows=probe, threads=threads)
+    oracle.rope_attn_workload(x, rows=probe, threads=threads, qk_norm=nrm)
     dt = max(time.perf_counter() - t0, 1e-3)
     n = int(min(total, max(len(probe), len(probe) * budget_s / dt)))
     rows = rng.choice(total, size=n, replace=False)
     t0 = time.perf_counter()
-    oracle.rope_attn_workload(x, rows=rows, threads=threads)
+    oracle.rope_attn_workload(x, rows=rows, threads=threads, qk_norm=nrm)
     dt = time.perf_counter() - t0
     return row_flops(w, rows) / dt / 1e12, dt, n, threads
 
@@ -318,18 +328,38 @@ def run_ours(args):
     stream = torch.cuda.current_stream(device)
     s = stream.cuda_stream
 
-    def rope():
-        sa.sa_rope_k(h, k.data_ptr(), None, k_rot.data_ptr(), cs_table.data_ptr(),
-                     w.B, w.H, w.L, w.d, w.nmaps, dtype, s)
+    nrm = qk_norm_params(args.qk_norm)
+    if nrm is None:
+        def rope():
+            sa.sa_rope_k(h, k.data_ptr(), None, k_rot.data_ptr(), cs_table.data_ptr(),
+                         w.B, w.H, w.L, w.d, w.nmaps, dtype, s)
 
-    def attn():
-        sa.sa_attn_fwd_rope_q(h, q.data_ptr(), k_rot.data_ptr(), cs_table.data_ptr(), v.data_ptr(),
-                              out.data_ptr(), w.B, w.H, w.L, w.d, w.window, lam, dtype, s,
-                              split.data_ptr(), split.numel())
+        def attn():
+            sa.sa_attn_fwd_rope_q(h, q.data_ptr(), k_rot.data_ptr(), cs_table.data_ptr(), v.data_ptr(),
+                                  out.data_ptr(), w.B, w.H, w.L, w.d, w.window, lam, dtype, s,
+                                  split.data_ptr(), split.numel())
 
-    def full():
-        sa.sa_rope_attn(h, q.data_ptr(), k.data_ptr(), v.data_ptr(), None, out.data_ptr(), w.B, w.H,
-                        w.L, w.d, w.window, lam, dtype, ws.data_ptr(), ws_bytes, s)
+        def full():
+            sa.sa_rope_attn(h, q.data_ptr(), k.data_ptr(), v.data_ptr(), None, out.data_ptr(), w.B, w.H,
+                            w.L, w.d, w.window, lam, dtype, ws.data_ptr(), ws_bytes, s)
+    else:
+        # QK-RMSNorm: region 2 times the two-stage form (normalised, rotated q' and k' from the
+        # pre-pass, then the attention kernel on them), the only split form this variant has
+        gq, gk, eps = nrm[0].tolist(), nrm[1].tolist(), nrm[2]
+        q_rot = torch.empty_like(q)
+
+        def rope():
+            sa.sa_qknorm_rope_qk(h, q.data_ptr(), k.data_ptr(), None, gq, gk, eps, q_rot.data_ptr(),
+                                 k_rot.data_ptr(), w.B, w.H, w.L, w.d, w.nmaps, dtype, s)
+
+        def attn():
+            sa.sa_attn_fwd(h, q_rot.data_ptr(), k_rot.data_ptr(), v.data_ptr(), out.data_ptr(), w.B, w.H,
+                           w.L, w.d, w.window, lam, dtype, s, split.data_ptr(), split.numel())
+
+        def full():
+            sa.sa_rope_attn_qknorm(h, q.data_ptr(), k.data_ptr(), v.data_ptr(), None, gq, gk, eps,
+                                   out.data_ptr(), w.B, w.H, w.L, w.d, w.window, lam, dtype,
+                                   ws.data_ptr(), ws_bytes, s)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -384,8 +414,7 @@ def run_ours(args):
         q.copy_(qh, non_blocking=True)
         k.copy_(kh, non_blocking=True)
         v.copy_(vh, non_blocking=True)
-        sa.sa_rope_attn(h, q.data_ptr(), k.data_ptr(), v.data_ptr(), None, out.data_ptr(), w.B, w.H,
-                        w.L, w.d, w.window, lam, dtype, ws.data_ptr(), ws_bytes, s)
+        full()
         oh.copy_(out, non_blocking=True)
         if e is not None:
             e[1].record(stream)
@@ -415,7 +444,7 @@ def run_ours(args):
     achieved = fl / attn_avg_s / 1e12
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        tfl, dt, n, th = oracle_sample(w, x, args.cpu_budget, np.random.default_rng(0))
+        tfl, dt, n, th = oracle_sample(w, x, args.cpu_budget, np.random.default_rng(0), qk_norm=nrm)
         cpu = {"value": tfl, "unit": "TFLOP/s", "cores": th, "kind": "oracle",
                "sample": f"{n} of {w.B * w.H * w.L} query rows (random, all heads), {dt:.1f} s, FP64 C oracle"}
     return {
@@ -434,11 +463,13 @@ def run_ours(args):
         "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "d_v": w.dv,
                    "maps": w.nmaps, "window": w.window, "flops_per_step_per_gpu": fl,
                    "l2": "flushed before every step (256 MiB write, outside the events)",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}", "qk_norm": nrm is not None},
         "frac_of_peak": value / world / peaks["tflops"],
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["tflops"], "traffic": load_traffic(w.name),
-                     "kernel": "attention (sa_attn_fwd_rope_q)", "kernel_sha": kernel_sha(),
+                     "frac": achieved / peaks["tflops"],
+                     "traffic": load_traffic(w.name) if nrm is None else None,
+                     "kernel": "attention (sa_attn_fwd_rope_q)" if nrm is None else
+                               "attention (sa_attn_fwd on sa_qknorm_rope_qk output)", "kernel_sha": kernel_sha(),
                      "peak_source": peaks["source"] + " bf16 burst",
                      "avg_ms": attn_avg_s * 1e3},
         "stages_ms": {"rope": statistics.mean(rope_ms), "attention": statistics.mean(attn_ms)},
@@ -461,12 +492,13 @@ def run_reference(args):
     x = synth.make_inputs(w)
     rng = np.random.default_rng(1)
     per_step = max(0.2, min(2.0, 150.0 / max(1, args.steps + args.warmup)))
+    nrm = qk_norm_params(args.qk_norm)
     for _ in range(args.warmup):
-        oracle_sample(w, x, per_step / 4, rng)
+        oracle_sample(w, x, per_step / 4, rng, qk_norm=nrm)
     vals, secs, rows = [], [], 0
     th = None
     for _ in range(args.steps):
-        tfl, dt, n, th = oracle_sample(w, x, per_step, rng)
+        tfl, dt, n, th = oracle_sample(w, x, per_step, rng, qk_norm=nrm)
         vals.append(tfl)
         secs.append(dt)
         rows += n
@@ -486,7 +518,7 @@ def run_reference(args):
         "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "L": w.L, "d": w.d, "d_v": w.dv,
-                   "maps": w.nmaps, "window": w.window},
+                   "maps": w.nmaps, "window": w.window, "qk_norm": nrm is not None},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": th, "kind": "oracle",
                          "sample": f"{rows} query rows over {args.steps} steps (random rows of "
                                    f"{w.B * w.H * w.L}), FP64 C oracle"},
@@ -504,6 +536,8 @@ def main():
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size B")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--qk-norm", action="store_true",
+                    help="QK-RMSNorm (FP32, seeded gammas, eps 1e-6) before RoPE: sa_rope_attn_qknorm")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         ap.error("--warmup must be >= 3")

@@ -19,7 +19,7 @@ from typing import Optional, Sequence
 __all__ = [
     "SA_FP16", "SA_BF16", "SaAttnError", "library_path", "load_library",
     "sa_attn_create", "sa_attn_destroy", "sa_rope_attn_workspace_size", "sa_attn_fwd_workspace_size", "sa_rope_table_bytes", "sa_rope_k", "sa_attn_fwd_rope_q", "sa_rope_attn",
-    "sa_rope_qk", "sa_attn_fwd", "sa_rope_attn_noalloc", "sa_attn_check", "sa_attn_set_timeout", "sa_last_error", "sa_status_string", "RopeAttention",
+    "sa_rope_qk", "sa_rope_attn_qknorm", "sa_qknorm_rope_qk", "sa_attn_fwd", "sa_rope_attn_noalloc", "sa_attn_check", "sa_attn_set_timeout", "sa_last_error", "sa_status_string", "RopeAttention",
 ]
 
 SA_FP16 = 0
@@ -66,6 +66,12 @@ def load_library():
         lib.sa_rope_attn.restype = i
         lib.sa_rope_qk.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
         lib.sa_rope_qk.restype = i
+        lib.sa_rope_attn_qknorm.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(f), ctypes.POINTER(f), f,
+                                            vp, i, i, i, i, i, ctypes.POINTER(f), i, vp, sz, vp]
+        lib.sa_rope_attn_qknorm.restype = i
+        lib.sa_qknorm_rope_qk.argtypes = [vp, vp, vp, vp, ctypes.POINTER(f), ctypes.POINTER(f), f,
+                                          vp, vp, i, i, i, i, i, i, vp]
+        lib.sa_qknorm_rope_qk.restype = i
         lib.sa_rope_table_bytes.argtypes = [i]
         lib.sa_rope_table_bytes.restype = sz
         lib.sa_rope_k.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
@@ -173,6 +179,44 @@ def sa_rope_qk(handle: int, q: int, k: int, positions: Optional[int], q_rot: int
         ctypes.c_void_p(handle), ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(positions),
         ctypes.c_void_p(q_rot), ctypes.c_void_p(k_rot), int(B), int(H), int(L), int(d), int(nmaps),
         int(dtype), ctypes.c_void_p(stream)))
+
+
+def _gamma(g):
+    if g is None:
+        return None
+    vals = [float(x) for x in g]
+    return (ctypes.c_float * len(vals))(*vals)
+
+
+def sa_rope_attn_qknorm(handle: int, q: int, k: int, v: int, positions: Optional[int],
+                        gamma_q: Optional[Sequence[float]], gamma_k: Optional[Sequence[float]],
+                        eps: float, out: int, B: int, H: int, L: int, d: int, window: int,
+                        lam: Optional[Sequence[float]], dtype: int, workspace: Optional[int],
+                        workspace_bytes: int, stream: Optional[int]) -> None:
+    """Enqueue QK-RMSNorm (FP32, gamma per tensor, eps) + RoPE + attention; gammas are host lists."""
+    for g in (gamma_q, gamma_k):
+        if g is not None and len(g) != d:
+            raise ValueError("gamma must have d entries")
+    _check(load_library().sa_rope_attn_qknorm(
+        ctypes.c_void_p(handle), ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v),
+        ctypes.c_void_p(positions), _gamma(gamma_q), _gamma(gamma_k), ctypes.c_float(eps),
+        ctypes.c_void_p(out), int(B), int(H), int(L), int(d), int(window), _lam(lam), int(dtype),
+        ctypes.c_void_p(workspace), ctypes.c_size_t(workspace_bytes), ctypes.c_void_p(stream)))
+
+
+def sa_qknorm_rope_qk(handle: int, q: int, k: int, positions: Optional[int],
+                      gamma_q: Optional[Sequence[float]], gamma_k: Optional[Sequence[float]], eps: float,
+                      q_rot: int, k_rot: int, B: int, H: int, L: int, d: int, nmaps: int, dtype: int,
+                      stream: Optional[int]) -> None:
+    """Enqueue the QK-RMSNorm + RoPE stage alone (q_rot/k_rot: normalised, rotated, cast-back)."""
+    for g in (gamma_q, gamma_k):
+        if g is not None and len(g) != d:
+            raise ValueError("gamma must have d entries")
+    _check(load_library().sa_qknorm_rope_qk(
+        ctypes.c_void_p(handle), ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(positions),
+        _gamma(gamma_q), _gamma(gamma_k), ctypes.c_float(eps), ctypes.c_void_p(q_rot),
+        ctypes.c_void_p(k_rot), int(B), int(H), int(L), int(d), int(nmaps), int(dtype),
+        ctypes.c_void_p(stream)))
 
 
 def sa_attn_fwd(handle: int, q_rot: int, k_rot: int, v: int, out: int, B: int, H: int, L: int,

@@ -18,7 +18,8 @@
 struct sa_attn_s {
   int device;
   int num_sms;
-  int rope_blocks_per_sm;
+  int rope_blocks_per_sm;       // RoPE pass, without / with the QK-RMSNorm
+  int rope_blocks_per_sm_norm;
   float rope_base;
   float inv_freq[sa::kHeadDim / 2];
   int* d_err;  // 4-byte device error word
@@ -118,10 +119,31 @@ sa_status check_lambda(const char* fn, const float* lambda, int H) {
   return SA_OK;
 }
 
+// QK-RMSNorm parameters as the kernels take them (gamma NULL: all ones).
+struct QkNorm {
+  float eps;
+  float gamma_q[sa::kHeadDim];
+  float gamma_k[sa::kHeadDim];
+};
+
+sa_status make_qknorm(const char* fn, const float* gamma_q, const float* gamma_k, float eps, QkNorm* n) {
+  if (!std::isfinite(eps) || eps < 0.0f)
+    return fail(SA_ERR_INVALID_ARG, "%s: eps must be finite and >= 0 (got %g)", fn, static_cast<double>(eps));
+  n->eps = eps;
+  for (int i = 0; i < sa::kHeadDim; ++i) {
+    n->gamma_q[i] = gamma_q ? gamma_q[i] : 1.0f;
+    n->gamma_k[i] = gamma_k ? gamma_k[i] : 1.0f;
+    if (!std::isfinite(n->gamma_q[i]) || !std::isfinite(n->gamma_k[i]))
+      return fail(SA_ERR_INVALID_ARG, "%s: gamma_q[%d] or gamma_k[%d] is not finite", fn, i, i);
+  }
+  return SA_OK;
+}
+
 // q == nullptr: rotate k only and write the (cos, sin) table cs (for the Q prologue).
+// nrm: QK-RMSNorm before the rotation, or nullptr.
 sa_status launch_rope(const sa_attn_s* h, const void* q, const void* k, const int32_t* positions,
                       void* q_rot, void* k_rot, int B, int H, int L, int nmaps, sa_dtype dtype,
-                      sa_stream_t stream, void* cs = nullptr) {
+                      sa_stream_t stream, void* cs = nullptr, const QkNorm* nrm = nullptr) {
   DeviceGuard guard(h->device);
   if (!guard.ok) return fail(SA_ERR_CUDA, "cannot select device %d", h->device);
   sa::RopeArgs ra;
@@ -135,7 +157,14 @@ sa_status launch_rope(const sa_attn_s* h, const void* q, const void* k, const in
   ra.L = L;
   ra.planes_per_block = 1;
   std::memcpy(ra.inv_freq, h->inv_freq, sizeof(ra.inv_freq));
-  cudaError_t e = sa::rope_launch(ra, dtype == SA_BF16, h->num_sms, h->rope_blocks_per_sm,
+  ra.qk_norm = nrm != nullptr;
+  ra.eps = nrm ? nrm->eps : 0.0f;
+  for (int i = 0; i < sa::kHeadDim; ++i) {
+    ra.gamma_q[i] = nrm ? nrm->gamma_q[i] : 1.0f;
+    ra.gamma_k[i] = nrm ? nrm->gamma_k[i] : 1.0f;
+  }
+  cudaError_t e = sa::rope_launch(ra, dtype == SA_BF16, h->num_sms,
+                                  nrm ? h->rope_blocks_per_sm_norm : h->rope_blocks_per_sm,
                                   reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(SA_ERR_CUDA, "RoPE launch: %s", cudaGetErrorString(e));
   return ok();
@@ -167,7 +196,8 @@ size_t split_bytes(int B, int H, int L, bool diff) {
 // in its prologue with the (cos, sin) table cs.
 sa_status launch_attn(const sa_attn_s* h, const void* q_rot, const void* k_rot, const void* v,
                       void* out, int B, int H, int L, int window, const float* lambda,
-                      sa_dtype dtype, void* split_ws, sa_stream_t stream, const void* cs = nullptr) {
+                      sa_dtype dtype, void* split_ws, sa_stream_t stream, const void* cs = nullptr,
+                      const QkNorm* nrm = nullptr) {
   const bool diff = lambda != nullptr;
   const bool bf16 = dtype == SA_BF16;
   const int d = sa::kHeadDim;
@@ -193,6 +223,9 @@ sa_status launch_attn(const sa_attn_s* h, const void* q_rot, const void* k_rot, 
   fa.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   fa.timeout_ns = h->timeout_ns;
   fa.cs = static_cast<const float2*>(cs);
+  fa.qk_norm = nrm != nullptr;   // (with cs: the Q prologue normalises each raw q row)
+  fa.eps = nrm ? nrm->eps : 0.0f;
+  for (int i = 0; i < sa::kHeadDim; ++i) fa.gamma_q[i] = nrm ? nrm->gamma_q[i] : 1.0f;
   if (diff)
     for (int i = 0; i < H; ++i) fa.lambda[i] = lambda[i];
   // One CTA per unit, except that when the units leave the GPU's last wave partly empty and a
@@ -320,7 +353,8 @@ sa_status sa_attn_create(sa_attn_t* handle, int device, float rope_base) {
     delete h;
     return fail(SA_ERR_CUDA, "sa_attn_create: cudaMalloc: %s", cudaGetErrorString(e));
   }
-  h->rope_blocks_per_sm = sa::rope_blocks_per_sm();
+  h->rope_blocks_per_sm = sa::rope_blocks_per_sm(false);
+  h->rope_blocks_per_sm_norm = sa::rope_blocks_per_sm(true);
   if ((e = cudaMemset(h->d_err, 0, sizeof(int))) != cudaSuccess ||
       (e = sa::fmha_set_attributes()) != cudaSuccess) {
     cudaFree(h->d_err);
@@ -438,11 +472,16 @@ sa_status sa_attn_fwd_rope_q(sa_attn_t h, const void* q, const void* k_rot, cons
   return launch_attn(h, q, k_rot, v, out, B, H, L, window, lambda, dtype, workspace, stream, cs_table);
 }
 
-sa_status sa_rope_attn(sa_attn_t h, const void* q, const void* k, const void* v,
+}  // extern "C"
+
+namespace {
+
+// sa_rope_attn and sa_rope_attn_qknorm: checks, then the K pass (with the table) and the
+// attention kernel (with the Q prologue), both on the caller's workspace.
+sa_status rope_attn_ws(const char* fn, sa_attn_t h, const void* q, const void* k, const void* v,
                        const int32_t* positions, void* out, int B, int H, int L, int d, int window,
-                       const float* lambda, sa_dtype dtype, void* workspace,
-                       size_t workspace_bytes, sa_stream_t stream) {
-  const char* fn = "sa_rope_attn";
+                       const float* lambda, sa_dtype dtype, void* workspace, size_t workspace_bytes,
+                       sa_stream_t stream, const QkNorm* nrm) {
   if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
   if (!q || !k || !v || !out)
     return fail(SA_ERR_INVALID_ARG, "%s: q, k, v and out must be non-NULL", fn);
@@ -464,9 +503,52 @@ sa_status sa_rope_attn(sa_attn_t h, const void* q, const void* k, const void* v,
   void* cs = ws;
   void* k_rot = ws + align256(sa_rope_table_bytes(L));
   void* split_ws = static_cast<uint8_t*>(k_rot) + align256(nqk * 2);
-  st = launch_rope(h, nullptr, k, positions, nullptr, k_rot, B, H, L, diff ? 2 : 1, dtype, stream, cs);
+  st = launch_rope(h, nullptr, k, positions, nullptr, k_rot, B, H, L, diff ? 2 : 1, dtype, stream, cs, nrm);
   if (st != SA_OK) return st;
-  return launch_attn(h, q, k_rot, v, out, B, H, L, window, lambda, dtype, split_ws, stream, cs);
+  return launch_attn(h, q, k_rot, v, out, B, H, L, window, lambda, dtype, split_ws, stream, cs, nrm);
+}
+
+}  // namespace
+
+extern "C" {
+
+sa_status sa_rope_attn(sa_attn_t h, const void* q, const void* k, const void* v,
+                       const int32_t* positions, void* out, int B, int H, int L, int d, int window,
+                       const float* lambda, sa_dtype dtype, void* workspace,
+                       size_t workspace_bytes, sa_stream_t stream) {
+  return rope_attn_ws("sa_rope_attn", h, q, k, v, positions, out, B, H, L, d, window, lambda, dtype,
+                      workspace, workspace_bytes, stream, nullptr);
+}
+
+sa_status sa_rope_attn_qknorm(sa_attn_t h, const void* q, const void* k, const void* v,
+                              const int32_t* positions, const float* gamma_q, const float* gamma_k,
+                              float eps, void* out, int B, int H, int L, int d, int window,
+                              const float* lambda, sa_dtype dtype, void* workspace,
+                              size_t workspace_bytes, sa_stream_t stream) {
+  const char* fn = "sa_rope_attn_qknorm";
+  QkNorm nrm;
+  sa_status st = make_qknorm(fn, gamma_q, gamma_k, eps, &nrm);
+  if (st != SA_OK) return st;
+  return rope_attn_ws(fn, h, q, k, v, positions, out, B, H, L, d, window, lambda, dtype, workspace,
+                      workspace_bytes, stream, &nrm);
+}
+
+sa_status sa_qknorm_rope_qk(sa_attn_t h, const void* q, const void* k, const int32_t* positions,
+                            const float* gamma_q, const float* gamma_k, float eps, void* q_rot,
+                            void* k_rot, int B, int H, int L, int d, int nmaps, sa_dtype dtype,
+                            sa_stream_t stream) {
+  const char* fn = "sa_qknorm_rope_qk";
+  if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
+  if (!q || !k || !q_rot || !k_rot)
+    return fail(SA_ERR_INVALID_ARG, "%s: q, k, q_rot and k_rot must be non-NULL", fn);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(q_rot) || !aligned16(k_rot))
+    return fail(SA_ERR_INVALID_ARG, "%s: q, k, q_rot and k_rot must be 16-byte aligned", fn);
+  if (nmaps != 1 && nmaps != 2) return fail(SA_ERR_INVALID_ARG, "%s: nmaps must be 1 or 2", fn);
+  sa_status st = check_shape(fn, B, H, L, d, dtype, nmaps == 2);
+  if (st != SA_OK) return st;
+  QkNorm nrm;
+  if ((st = make_qknorm(fn, gamma_q, gamma_k, eps, &nrm)) != SA_OK) return st;
+  return launch_rope(h, q, k, positions, q_rot, k_rot, B, H, L, nmaps, dtype, stream, nullptr, &nrm);
 }
 
 sa_status sa_attn_set_timeout(sa_attn_t h, unsigned long long timeout_ns) {

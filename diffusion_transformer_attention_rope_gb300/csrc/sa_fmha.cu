@@ -148,12 +148,14 @@ __device__ __forceinline__ bool pwait_w(uint32_t bar, uint32_t parity, volatile 
 // RoPE prologue of one Q row (thread r of a softmax warpgroup): the TMA brought the tile in
 // raw; the row is rotated in place (128-byte-swizzled smem: 16-byte chunk c of row r sits at
 // c ^ (r & 7)), pairs [8g, 8g + 8) from chunks g and g + 4, with the RoPE pass's FP32
-// (cos, sin) of the row's position and the pre-pass's arithmetic.  Kept out of line so that its
-// registers do not weigh on the softmax loop's.  Returns the warp-uniform wait outcome.
-template <bool BF16>
+// (cos, sin) of the row's position and the pre-pass's arithmetic.  With gamma (NORM) the row is
+// QK-RMS-normalised first, with the pre-pass's sum order and scaling, so its bits again equal
+// the pre-pass's.  Kept out of line so that its registers do not weigh on the softmax loop's.
+// Returns the warp-uniform wait outcome.
+template <bool BF16, bool NORM>
 __device__ __noinline__ bool q_rope_prologue(const float2* cs, int L, int grow, uint32_t row, int r,
                                              uint32_t q_full, volatile int* abort_flag, int* err,
-                                             uint64_t tmo) {
+                                             uint64_t tmo, const float* gamma, float eps) {
   // the table is the RoPE pass's output: wait for that grid (programmatic dependent launch)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   // the row's (cos, sin) pairs ([16][L] float4 table: a warp's loads are contiguous), loaded
@@ -165,6 +167,19 @@ __device__ __noinline__ bool q_rope_prologue(const float2* cs, int L, int grow, 
   bool ok = pwait(q_full, 0, abort_flag, err, kErrSoftmax, tmo);
   ok = __all_sync(0xffffffffu, ok);
   if (ok && grow < L) {
+    uint4 lo[4], hi[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) {
+      lo[g] = ld_shared_v4(row + ((g ^ (r & 7)) << 4));
+      hi[g] = ld_shared_v4(row + (((g + 4) ^ (r & 7)) << 4));
+    }
+    float inv = 1.0f;
+    if (NORM) {
+      float tg[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) tg[g] = sumsq8<BF16>(lo[g]) + sumsq8<BF16>(hi[g]);
+      inv = qknorm_inv_rms((tg[0] + tg[1]) + (tg[2] + tg[3]), eps);
+    }
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
       float cg[8], sg[8];
@@ -175,10 +190,19 @@ __device__ __noinline__ bool q_rope_prologue(const float2* cs, int L, int grow, 
         cg[2 * i + 1] = t[4 * g + i].z;
         sg[2 * i + 1] = t[4 * g + i].w;
       }
-      const uint32_t a_lo = row + ((g ^ (r & 7)) << 4), a_hi = row + (((g + 4) ^ (r & 7)) << 4);
-      const uint4 lo = ld_shared_v4(a_lo), hi = ld_shared_v4(a_hi);
       uint4 olo, ohi;
-      rope_rotate8<BF16>(lo, hi, cg, sg, olo, ohi);
+      if (NORM) {
+        float sl[8], sh[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          sl[i] = __fmul_rn(inv, gamma[8 * g + i]);
+          sh[i] = __fmul_rn(inv, gamma[32 + 8 * g + i]);
+        }
+        rope_rotate8_scaled<BF16>(lo[g], hi[g], cg, sg, sl, sh, olo, ohi);
+      } else {
+        rope_rotate8<BF16>(lo[g], hi[g], cg, sg, olo, ohi);
+      }
+      const uint32_t a_lo = row + ((g ^ (r & 7)) << 4), a_hi = row + (((g + 4) ^ (r & 7)) << 4);
       st_shared_v4(a_lo, olo.x, olo.y, olo.z, olo.w);
       st_shared_v4(a_hi, ohi.x, ohi.y, ohi.z, ohi.w);
     }
@@ -469,7 +493,12 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
 
     if (a.cs != nullptr) {
       // RoPE prologue on this warpgroup's Q tile, then the tile goes to its MMA issuer.
-      ok = q_rope_prologue<BF16>(a.cs, L, grow, sQ + s * kTile + r * 128, r, bar.q_full, abort_flag, a.err, tmo);
+      if (a.qk_norm)
+        ok = q_rope_prologue<BF16, true>(a.cs, L, grow, sQ + s * kTile + r * 128, r, bar.q_full, abort_flag,
+                                         a.err, tmo, a.gamma_q, a.eps);
+      else
+        ok = q_rope_prologue<BF16, false>(a.cs, L, grow, sQ + s * kTile + r * 128, r, bar.q_full, abort_flag,
+                                          a.err, tmo, nullptr, 0.0f);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.q_ready(s));

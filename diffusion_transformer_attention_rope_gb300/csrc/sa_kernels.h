@@ -43,6 +43,11 @@ struct RopeArgs {
   int L;
   int planes_per_block;
   float inv_freq[kHeadDim / 2];
+  // QK-RMSNorm before the rotation (qk_norm != 0): x * gamma / sqrt(mean(x^2) + eps) per row
+  int qk_norm;
+  float eps;
+  float gamma_q[kHeadDim];
+  float gamma_k[kHeadDim];
 };
 
 // Attention kernel arguments (tensor maps are passed separately as __grid_constant__).
@@ -71,6 +76,10 @@ struct FmhaArgs {
   float* partials;            // tail_k > 1: one slot of fmha_partial_floats per piece CTA
   unsigned long long timeout_ns;
   float lambda[kMaxDiffHeads];
+  // Q prologue only (cs != nullptr): QK-RMSNorm of each raw q row before its rotation
+  int qk_norm;
+  float eps;
+  float gamma_q[kHeadDim];
 };
 
 // Rows of queries in one unit: two 128-row tiles (standard) or one tile with two maps.
@@ -83,8 +92,9 @@ constexpr int fmha_partial_floats(bool diff) { return 2 * kBlockM * ((diff ? 2 *
 constexpr int kMaxPieces = 160;
 constexpr int kMaxTailK = 4;
 
-// Blocks of the RoPE kernel resident per SM (from the occupancy calculator).
-int rope_blocks_per_sm();
+// Blocks of the RoPE kernel resident per SM (from the occupancy calculator), without and with
+// the QK-RMSNorm.
+int rope_blocks_per_sm(bool qk_norm);
 cudaError_t rope_launch(const RopeArgs& a, bool bf16, int num_sms, int blocks_per_sm, cudaStream_t stream);
 
 cudaError_t fmha_set_attributes();

@@ -381,5 +381,53 @@ __device__ __forceinline__ void rope_rotate8(const uint4& lo, const uint4& hi, c
   out_hi = make_uint4(oh[0], oh[1], oh[2], oh[3]);
 }
 
+// QK-RMSNorm pieces shared by the pre-pass and the Q prologue, so that a row normalised by
+// either has the same bits.  Sum of squares of one 16-byte chunk (8 values) in FP32, in a fixed
+// order; a row's total is ((t0 + t1) + (t2 + t3)) where t_g = sumsq8(chunk g) + sumsq8(chunk
+// g + 4), which is also what a 4-lane butterfly over t_g gives every lane (FP32 addition is
+// commutative).  FP32 holds the square of every fp16 value; bf16 rows with |x| >= 2^63 are
+// outside its range.
+template <bool BF16>
+__device__ __forceinline__ float sumsq8(const uint4& v) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+  float acc = 0.0f;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 a = unpack2<BF16>(w[j]);
+    acc = __fmaf_rn(a.x, a.x, acc);
+    acc = __fmaf_rn(a.y, a.y, acc);
+  }
+  return acc;
+}
+
+// 1 / sqrt(mean of squares + eps) of a 64-value row from its sum of squares.
+__device__ __forceinline__ float qknorm_inv_rms(float sumsq, float eps) {
+  return 1.0f / sqrtf(__fmaf_rn(sumsq, 1.0f / 64.0f, eps));
+}
+
+// rope_rotate8 of the normalised row: each value is first multiplied by its scale
+// (1 / rms times the value's gamma), glo for the lo chunk, ghi for the hi chunk.
+template <bool BF16>
+__device__ __forceinline__ void rope_rotate8_scaled(const uint4& lo, const uint4& hi, const float (&c)[8],
+                                              const float (&s)[8], const float (&glo)[8],
+                                              const float (&ghi)[8], uint4& out_lo, uint4& out_hi) {
+  const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w};
+  const uint32_t hw[4] = {hi.x, hi.y, hi.z, hi.w};
+  uint32_t ol[4], oh[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i0 = 2 * j, i1 = 2 * j + 1;
+    float2 a = unpack2<BF16>(lw[j]);
+    float2 b = unpack2<BF16>(hw[j]);
+    a.x = __fmul_rn(a.x, glo[i0]);
+    a.y = __fmul_rn(a.y, glo[i1]);
+    b.x = __fmul_rn(b.x, ghi[i0]);
+    b.y = __fmul_rn(b.y, ghi[i1]);
+    ol[j] = pack2<BF16>(fmaf(a.x, c[i0], -(b.x * s[i0])), fmaf(a.y, c[i1], -(b.y * s[i1])));
+    oh[j] = pack2<BF16>(fmaf(b.x, c[i0], a.x * s[i0]), fmaf(b.y, c[i1], a.y * s[i1]));
+  }
+  out_lo = make_uint4(ol[0], ol[1], ol[2], ol[3]);
+  out_hi = make_uint4(oh[0], oh[1], oh[2], oh[3]);
+}
 
 }  // namespace sa

@@ -10,6 +10,11 @@
 // With a table pointer the pass also writes each position's 32 (cos, sin) pairs (FP32), which
 // the attention kernel uses to rotate q in its prologue; q is then not touched here.
 //
+// Optional QK-RMSNorm (the pages keep "RMSNorm + RoPE around attention" as FP32 islands that
+// guard variance overflow): each row is first scaled by gamma / sqrt(mean(x^2) + eps) in FP32,
+// then rotated, then cast once.  The 4 threads of a row (consecutive lanes) add their partial
+// sums of squares with a 2-step butterfly.
+//
 // One block rotates 32 positions of every plane in its slice of planes (a plane is one
 // (batch, head, map) sequence of L rows).  A thread owns 8 rotation pairs of one position
 // (two 16-byte chunks per row) and up to kPlaneBatch planes at a time: it issues all the loads
@@ -41,15 +46,32 @@ __device__ __forceinline__ void st_v4(uint16_t* p, uint4 v) {
                : "memory");
 }
 
+// The row's inverse RMS from this thread's partial sum of squares (lanes of a row: gmask).
+__device__ __forceinline__ float row_inv_rms(float t, unsigned gmask, float eps) {
+  const float u = t + __shfl_xor_sync(gmask, t, 1);
+  return qknorm_inv_rms(u + __shfl_xor_sync(gmask, u, 2), eps);
+}
+
 // WITH_Q: rotate q as well as k (false when the attention kernel rotates q in its prologue).
-template <bool BF16, bool WITH_Q>
-__global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constant__ RopeArgs a) {
+// NORM: QK-RMSNorm of every row before its rotation.
+template <bool BF16, bool WITH_Q, bool NORM>
+__device__ __forceinline__ void rope_body(const RopeArgs& a) {
   // Let the dependent attention grid begin its prologue while this grid streams.
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int r = threadIdx.x >> 2;  // position within the block
   const int g = threadIdx.x & 3;   // group of 8 pairs: pairs [8g, 8g + 8)
   const int l = blockIdx.x * kRopeRows + r;
-  if (l >= a.L) return;
+  // gammas in shared memory (q then k; registers are what limits this pass's occupancy); a
+  // thread reads those of its 16 values, [8g, 8g + 8) and [32 + 8g, 32 + 8g + 8)
+  __shared__ float s_gamma[2][kHeadDim];
+  if (NORM) {
+    static_assert(kRopeThreads == 2 * kHeadDim, "one gamma per thread");
+    s_gamma[threadIdx.x >> 6][threadIdx.x & 63] =
+        threadIdx.x < kHeadDim ? a.gamma_q[threadIdx.x] : a.gamma_k[threadIdx.x - kHeadDim];
+    __syncthreads();
+  }
+  if (l >= a.L) return;            // (all 4 lanes of a row leave together)
+  const unsigned gmask = 0xFu << (threadIdx.x & 28);
   const long long first = static_cast<long long>(blockIdx.y) * a.planes_per_block;
   long long last = first + a.planes_per_block;
   if (last > a.planes) last = a.planes;
@@ -97,12 +119,34 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constan
       if (i < n) {
         const size_t off = static_cast<size_t>(p0 + i) * row_stride + base;
         uint4 lo, hi;
-        if (WITH_Q) {
-          rope_rotate8<BF16>(qlo[i], qhi[i], c, s, lo, hi);
-          st_v4(a.q_out + off, lo);
-          st_v4(a.q_out + off + 32, hi);
+        if (NORM) {
+          float sl[8], sh[8];
+          if (WITH_Q) {
+            const float inv = row_inv_rms(sumsq8<BF16>(qlo[i]) + sumsq8<BF16>(qhi[i]), gmask, a.eps);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              sl[j] = __fmul_rn(inv, s_gamma[0][8 * g + j]);
+              sh[j] = __fmul_rn(inv, s_gamma[0][32 + 8 * g + j]);
+            }
+            rope_rotate8_scaled<BF16>(qlo[i], qhi[i], c, s, sl, sh, lo, hi);
+            st_v4(a.q_out + off, lo);
+            st_v4(a.q_out + off + 32, hi);
+          }
+          const float inv = row_inv_rms(sumsq8<BF16>(klo[i]) + sumsq8<BF16>(khi[i]), gmask, a.eps);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            sl[j] = __fmul_rn(inv, s_gamma[1][8 * g + j]);
+            sh[j] = __fmul_rn(inv, s_gamma[1][32 + 8 * g + j]);
+          }
+          rope_rotate8_scaled<BF16>(klo[i], khi[i], c, s, sl, sh, lo, hi);
+        } else {
+          if (WITH_Q) {
+            rope_rotate8<BF16>(qlo[i], qhi[i], c, s, lo, hi);
+            st_v4(a.q_out + off, lo);
+            st_v4(a.q_out + off + 32, hi);
+          }
+          rope_rotate8<BF16>(klo[i], khi[i], c, s, lo, hi);
         }
-        rope_rotate8<BF16>(klo[i], khi[i], c, s, lo, hi);
         st_v4(a.k_out + off, lo);
         st_v4(a.k_out + off + 32, hi);
       }
@@ -110,13 +154,23 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constan
   }
 }
 
-}  // namespace
+template <bool BF16, bool WITH_Q>
+__global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constant__ RopeArgs a) {
+  rope_body<BF16, WITH_Q, false>(a);
+}
 
-int rope_blocks_per_sm() {
-  const void* fns[4] = {reinterpret_cast<const void*>(rope_kernel<false, true>),
-                        reinterpret_cast<const void*>(rope_kernel<true, true>),
-                        reinterpret_cast<const void*>(rope_kernel<false, false>),
-                        reinterpret_cast<const void*>(rope_kernel<true, false>)};
+template <bool BF16, bool WITH_Q>
+__global__ void __launch_bounds__(kRopeThreads) rope_norm_kernel(const __grid_constant__ RopeArgs a) {
+  rope_body<BF16, WITH_Q, true>(a);
+}
+
+template <bool NORM>
+int blocks_per_sm() {
+  const void* fns[4] = {
+      NORM ? reinterpret_cast<const void*>(rope_norm_kernel<false, true>) : reinterpret_cast<const void*>(rope_kernel<false, true>),
+      NORM ? reinterpret_cast<const void*>(rope_norm_kernel<true, true>) : reinterpret_cast<const void*>(rope_kernel<true, true>),
+      NORM ? reinterpret_cast<const void*>(rope_norm_kernel<false, false>) : reinterpret_cast<const void*>(rope_kernel<false, false>),
+      NORM ? reinterpret_cast<const void*>(rope_norm_kernel<true, false>) : reinterpret_cast<const void*>(rope_kernel<true, false>)};
   int least = 1 << 30;
   for (const void* f : fns) {
     int n = 0;
@@ -125,6 +179,16 @@ int rope_blocks_per_sm() {
   }
   return least > 0 ? least : 1;
 }
+
+template <bool BF16, bool WITH_Q>
+void launch_variant(const RopeArgs& a, dim3 grid, cudaStream_t stream) {
+  if (a.qk_norm) rope_norm_kernel<BF16, WITH_Q><<<grid, kRopeThreads, 0, stream>>>(a);
+  else rope_kernel<BF16, WITH_Q><<<grid, kRopeThreads, 0, stream>>>(a);
+}
+
+}  // namespace
+
+int rope_blocks_per_sm(bool qk_norm) { return qk_norm ? blocks_per_sm<true>() : blocks_per_sm<false>(); }
 
 cudaError_t rope_launch(const RopeArgs& a_in, bool bf16, int num_sms, int blocks_per_sm,
                         cudaStream_t stream) {
@@ -148,11 +212,11 @@ cudaError_t rope_launch(const RopeArgs& a_in, bool bf16, int num_sms, int blocks
   const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(by));
   const bool with_q = a.q != nullptr;
   if (bf16) {
-    if (with_q) rope_kernel<true, true><<<grid, kRopeThreads, 0, stream>>>(a);
-    else rope_kernel<true, false><<<grid, kRopeThreads, 0, stream>>>(a);
+    if (with_q) launch_variant<true, true>(a, grid, stream);
+    else launch_variant<true, false>(a, grid, stream);
   } else {
-    if (with_q) rope_kernel<false, true><<<grid, kRopeThreads, 0, stream>>>(a);
-    else rope_kernel<false, false><<<grid, kRopeThreads, 0, stream>>>(a);
+    if (with_q) launch_variant<false, true>(a, grid, stream);
+    else launch_variant<false, false>(a, grid, stream);
   }
   return cudaGetLastError();
 }

@@ -148,6 +148,38 @@ SA_API sa_status sa_rope_attn(sa_attn_t handle,
                        sa_stream_t stream);
 
 /*
+ * sa_rope_attn with a QK-RMSNorm in front of RoPE.  The pages keep "RMSNorm +
+ * RoPE around attention" as FP32 islands that guard against variance overflow
+ * (sa3_trt README, "Notes on the design"; the encoder/decoder tiers page,
+ * "Where the quantization goes, per tier").  Here every row x of q and k (d
+ * values, each map of the differential form alike) becomes, in FP32,
+ *
+ *   x_c * gamma_c / sqrt(mean_c(x_c^2) + eps),
+ *
+ * is then rotated as in sa_rope_attn and cast once to dtype; attention follows
+ * unchanged.  The sum of squares is FP32, which holds every fp16 row; bf16
+ * rows with a value of magnitude >= 2^63 overflow it (result undefined).
+ *
+ *   gamma_q, gamma_k  host float[d] (NULL: all ones), finite.  Read during the
+ *                     call only (copied into the kernel arguments).
+ *   eps               finite, >= 0.
+ *
+ * Everything else (arguments, workspace, errors) as sa_rope_attn; a bad gamma
+ * or eps is SA_ERR_INVALID_ARG with nothing enqueued.
+ */
+SA_API sa_status sa_rope_attn_qknorm(sa_attn_t handle,
+                                     const void* q, const void* k, const void* v,
+                                     const int32_t* positions,
+                                     const float* gamma_q, const float* gamma_k, float eps,
+                                     void* out,
+                                     int B, int H, int L, int d,
+                                     int window,
+                                     const float* lambda,
+                                     sa_dtype dtype,
+                                     void* workspace, size_t workspace_bytes,
+                                     sa_stream_t stream);
+
+/*
  * The two stages sa_rope_attn is made of, for callers that want them apart
  * (for instance to time the attention kernel alone, or to feed q/k that are
  * already rotated).  Same conventions, layouts and errors as sa_rope_attn.
@@ -162,6 +194,20 @@ SA_API sa_status sa_rope_qk(sa_attn_t handle,
                             void* q_rot, void* k_rot,
                             int B, int H, int L, int d, int nmaps,
                             sa_dtype dtype, sa_stream_t stream);
+
+/*
+ * sa_qknorm_rope_qk: sa_rope_qk with the QK-RMSNorm of sa_rope_attn_qknorm in
+ *   front of the rotation (same gamma_q, gamma_k, eps rules).  Its q_rot, k_rot
+ *   have the bits the normalised, rotated q and k have inside
+ *   sa_rope_attn_qknorm.
+ */
+SA_API sa_status sa_qknorm_rope_qk(sa_attn_t handle,
+                                   const void* q, const void* k,
+                                   const int32_t* positions,
+                                   const float* gamma_q, const float* gamma_k, float eps,
+                                   void* q_rot, void* k_rot,
+                                   int B, int H, int L, int d, int nmaps,
+                                   sa_dtype dtype, sa_stream_t stream);
 
 /*
  * The two stages as sa_rope_attn runs them: the pre-pass rotates k only and

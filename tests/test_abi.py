@@ -96,6 +96,25 @@ def test_null_handle_is_rejected_on_the_host():
     assert "handle" in sa.sa_last_error()
 
 
+def test_qknorm_parameters_are_checked_on_the_host():
+    # eps and gamma are validated before anything else; nothing is enqueued
+    args = (256, 256, 256, None)
+    for gq, eps, word in (([1.0] * 64, -1.0, "eps"), ([1.0] * 64, float("nan"), "eps"),
+                          ([1.0] * 63 + [float("inf")], 1e-6, "gamma")):
+        with pytest.raises(sa.SaAttnError) as e:
+            sa.sa_rope_attn_qknorm(0, *args, gq, None, eps, 256, 1, 1, 64, 64, -1, None, sa.SA_FP16,
+                                   256, 1 << 20, None)
+        assert e.value.status == 1
+        assert word in sa.sa_last_error()
+    with pytest.raises(sa.SaAttnError) as e:
+        sa.sa_rope_attn_qknorm(0, *args, None, None, 1e-6, 256, 1, 1, 64, 64, -1, None, sa.SA_FP16,
+                               256, 1 << 20, None)
+    assert e.value.status == 1 and "handle" in sa.sa_last_error()
+    with pytest.raises(ValueError):
+        sa.sa_qknorm_rope_qk(0, 256, 256, None, [1.0] * 32, None, 1e-6, 256, 256, 1, 1, 64, 64, 1,
+                             sa.SA_FP16, None)
+
+
 def test_create_without_a_gpu_reports_no_device():
     import torch
 

@@ -422,3 +422,148 @@ def test_split_region_too_small_is_refused(attn):
     assert e.value.status == 6
     torch.cuda.synchronize()
     assert torch.all(out == 3.0)
+
+
+# ----------------------------------------------------------------------------- QK-RMSNorm
+
+def _gammas(seed):
+    rng = np.random.default_rng(seed)
+    return rng.uniform(0.5, 1.5, 64).astype(np.float32), rng.uniform(0.5, 1.5, 64).astype(np.float32)
+
+
+def run_qknorm(attn, x, gq, gk, eps, positions=None):
+    """sa_rope_attn_qknorm on a synth input dict; returns the output as float64."""
+    w = x["workload"]
+    q, k, v = dev(x["q"], w.dtype), dev(x["k"], w.dtype), dev(x["v"], w.dtype)
+    diff = w.nmaps == 2
+    n = sa.sa_rope_attn_workspace_size(w.B, w.H, w.L, 64, diff)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    out = torch.empty((w.B, w.H, w.L, w.dv), dtype=TDT[w.dtype], device="cuda")
+    pos = None if positions is None else torch.from_numpy(positions.astype(np.int32)).cuda()
+    lam = None if x["lam"] is None else [float(t) for t in x["lam"]]
+    sa.sa_rope_attn_qknorm(attn.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                           None if pos is None else pos.data_ptr(),
+                           None if gq is None else gq.tolist(), None if gk is None else gk.tolist(), eps,
+                           out.data_ptr(), w.B, w.H, w.L, 64, w.window, lam,
+                           sa.SA_BF16 if w.dtype == "bf16" else sa.SA_FP16, ws.data_ptr(), n,
+                           torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    attn.check()
+    return out.float().cpu().numpy().astype(np.float64)
+
+
+def _oracle_qknorm(x, gq, gk, eps, positions=None, rows=None):
+    if positions is not None:
+        x = dict(x, positions=positions.astype(np.int32))
+    return oracle.rope_attn_workload(
+        x, rows=rows, qk_norm=(None if gq is None else gq.astype(np.float64),
+                               None if gk is None else gk.astype(np.float64), eps))
+
+
+@pytest.mark.parametrize("dtype", ["fp16", "bf16"])
+def test_qknorm_prepass_matches_oracle(attn, dtype):
+    # sa_qknorm_rope_qk's q', k' against the FP64 RMSNorm then rotation.  On top of the RoPE
+    # bound of test_rope_prepass_matches_oracle, the FP32 normalisation (a 64-term FP32 sum of
+    # squares, sqrt, divide and two products) adds a relative error below 2^-16 of each pair.
+    # Rows of very different magnitudes (1e-3 .. 3e4 for fp16) exercise eps and the FP32 sum.
+    w = small("qkn", B=1, H=3, L=300, dtype=dtype, seed=51)
+    x = synth.make_inputs(w)
+    rng = np.random.default_rng(52)
+    top = 3.0e4 if dtype == "fp16" else 1.0e6
+    for key in ("q", "k"):
+        xd = synth.decode(x[key], dtype).astype(np.float64)
+        xd = xd * np.exp(rng.uniform(np.log(1e-3), np.log(top / 4), (w.B, w.H, w.L, 1)))
+        x[key] = synth.encode(np.clip(xd, -top, top).astype(np.float32), dtype)
+    gq, gk = _gammas(53)
+    eps = 1e-6
+    pos = (np.arange(w.L) * 11 + 3).astype(np.int32)
+    q, k = dev(x["q"], dtype), dev(x["k"], dtype)
+    qr, kr = torch.empty_like(q), torch.empty_like(k)
+    sa.sa_qknorm_rope_qk(attn.handle, q.data_ptr(), k.data_ptr(), torch.from_numpy(pos).cuda().data_ptr(),
+                         gq.tolist(), gk.tolist(), eps, qr.data_ptr(), kr.data_ptr(), w.B, w.H, w.L, 64, 1,
+                         sa.SA_BF16 if dtype == "bf16" else sa.SA_FP16, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    attn.check()
+    theta = np.abs(pos.astype(np.float64)[:, None] * (10000.0 ** (-2.0 * np.arange(32) / 64.0))[None, :])
+    theta = np.concatenate([theta, theta], axis=1)
+    for bits, g, rot in ((x["q"], gq, qr), (x["k"], gk, kr)):
+        xin = synth.decode(bits, dtype).astype(np.float64).reshape(-1, w.L, 64)
+        nrm = oracle.rmsnorm(xin, g.astype(np.float64), eps)
+        exact = oracle.rope(nrm.reshape(-1, 64), np.tile(pos, w.B * w.H)).reshape(xin.shape)
+        pair = np.sqrt(nrm[..., :32] ** 2 + nrm[..., 32:] ** 2)
+        pair = np.concatenate([pair, pair], axis=-1)
+        got = synth.decode(rot.view(torch.int16).cpu().numpy().view(np.uint16), dtype).astype(np.float64)
+        got = got.reshape(xin.shape)
+        bound = half_ulp(exact, dtype) + pair * (theta[None] * 2.0 ** -22 + 2.0 ** -16)
+        assert np.all(np.abs(got - exact) <= bound)
+        assert (got == oracle.round_to(exact, dtype)).mean() > 0.95
+
+
+@pytest.mark.parametrize("diff,dtype,window", [(False, "fp16", -1), (True, "bf16", 129)])
+def test_qknorm_prologue_matches_prepass(attn, diff, dtype, window):
+    # the fused path (K pass with the norm, q normalised in the attention kernel's prologue)
+    # has the bits of sa_qknorm_rope_qk followed by sa_attn_fwd
+    w = small("qknf", B=1, H=3, L=777, window=window, nmaps=2 if diff else 1, dv=128 if diff else 64,
+              dtype=dtype, seed=54, lam=("uniform", 0.2, 0.8) if diff else None)
+    x = synth.make_inputs(w)
+    B, H, L, nm = w.B, w.H, w.L, w.nmaps
+    q, k, v = dev(x["q"], dtype), dev(x["k"], dtype), dev(x["v"], dtype)
+    gq, gk = _gammas(55)
+    eps = 1e-5
+    lam = None if x["lam"] is None else [float(t) for t in x["lam"]]
+    dt = sa.SA_BF16 if dtype == "bf16" else sa.SA_FP16
+    s = torch.cuda.current_stream().cuda_stream
+    qr, kr = torch.empty_like(q), torch.empty_like(k)
+    split = torch.empty(sa.sa_attn_fwd_workspace_size(B, H, L, 64, diff), dtype=torch.uint8, device="cuda")
+    o1 = torch.empty((B, H, L, w.dv), dtype=TDT[dtype], device="cuda")
+    sa.sa_qknorm_rope_qk(attn.handle, q.data_ptr(), k.data_ptr(), None, gq.tolist(), gk.tolist(), eps,
+                         qr.data_ptr(), kr.data_ptr(), B, H, L, 64, nm, dt, s)
+    sa.sa_attn_fwd(attn.handle, qr.data_ptr(), kr.data_ptr(), v.data_ptr(), o1.data_ptr(), B, H, L, 64,
+                   window, lam, dt, s, split.data_ptr(), split.numel())
+    torch.cuda.synchronize()
+    o2 = run_qknorm(attn, x, gq, gk, eps)
+    assert np.array_equal(o1.float().cpu().numpy().astype(np.float64), o2)
+    compare(o2, _oracle_qknorm(x, gq, gk, eps), "qk-norm prologue", dtype=dtype)
+
+
+@pytest.mark.parametrize("B,H,L,window,diff,dtype,ones", [
+    (1, 3, 300, -1, False, "fp16", False),
+    (2, 2, 129, -1, False, "bf16", True),     # gamma NULL (ones)
+    (1, 2, 260, -1, True, "bf16", False),
+    (1, 2, 700, 17, False, "bf16", False),
+    (1, 2, 640, 17, True, "bf16", False),
+    (1, 1, 1, -1, False, "fp16", False),      # one row: out = v_0 whatever the norm
+])
+def test_qknorm_matches_oracle(attn, B, H, L, window, diff, dtype, ones):
+    w = small("qkn", B=B, H=H, L=L, window=window, nmaps=2 if diff else 1, dv=128 if diff else 64,
+              dtype=dtype, seed=560 + L, lam=("uniform", 0.2, 0.8) if diff else None)
+    x = synth.make_inputs(w)
+    gq, gk = (None, None) if ones else _gammas(57 + L)
+    pos = (np.arange(L) * 3 + 40).astype(np.int32)
+    got = run_qknorm(attn, x, gq, gk, 1e-6, positions=pos)
+    compare(got, _oracle_qknorm(x, gq, gk, 1e-6, positions=pos), f"qk-norm L={L}", dtype=dtype)
+
+
+def test_qknorm_large_fp16_rows(attn):
+    # rows near the fp16 maximum: a 16-bit sum of squares would overflow; the FP32 island
+    # (the pages' reason for keeping RMSNorm in FP32) gives the same result as unit rows
+    w = small("qknbig", B=1, H=2, L=200, dtype="fp16", seed=58)
+    x = synth.make_inputs(w)
+    for key in ("q", "k"):
+        xd = synth.decode(x[key], "fp16").astype(np.float64)
+        x[key] = synth.encode(np.clip(xd * 2.0e4, -6.0e4, 6.0e4).astype(np.float32), "fp16")
+    gq, gk = _gammas(59)
+    got = run_qknorm(attn, x, gq, gk, 1e-6)
+    assert np.all(np.isfinite(got))
+    compare(got, _oracle_qknorm(x, gq, gk, 1e-6), "qk-norm large rows", dtype="fp16")
+
+
+@pytest.mark.parametrize("name", ["dit_l1292", "dit_l4096_outliers"])
+def test_qknorm_full_size(attn, name):
+    w = synth.WORKLOADS[name]
+    x = synth.make_inputs(w)
+    gq, gk = _gammas(60)
+    got = run_qknorm(attn, x, gq, gk, 1e-6)
+    rows = sample_rows(w, np.random.default_rng(701))
+    ref = _oracle_qknorm(x, gq, gk, 1e-6, rows=rows)
+    compare(got.reshape(-1, w.dv)[rows], ref, f"qk-norm {name}")
