@@ -19,7 +19,8 @@ from typing import Optional, Sequence
 __all__ = [
     "SA_FP16", "SA_BF16", "SaAttnError", "library_path", "load_library",
     "sa_attn_create", "sa_attn_destroy", "sa_rope_attn_workspace_size", "sa_attn_fwd_workspace_size", "sa_rope_table_bytes", "sa_rope_k", "sa_attn_fwd_rope_q", "sa_rope_attn",
-    "sa_rope_qk", "sa_rope_attn_qknorm", "sa_qknorm_rope_qk", "sa_attn_fwd", "sa_rope_attn_noalloc", "sa_attn_check", "sa_attn_set_timeout", "sa_last_error", "sa_status_string", "RopeAttention",
+    "sa_rope_qk", "sa_rope_attn_qknorm", "sa_qknorm_rope_qk", "sa_rope_attn_host",
+    "sa_rope_attn_host_workspace_size", "sa_attn_fwd", "sa_rope_attn_noalloc", "sa_attn_check", "sa_attn_set_timeout", "sa_last_error", "sa_status_string", "RopeAttention",
 ]
 
 SA_FP16 = 0
@@ -66,6 +67,10 @@ def load_library():
         lib.sa_rope_attn.restype = i
         lib.sa_rope_qk.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, i, vp]
         lib.sa_rope_qk.restype = i
+        lib.sa_rope_attn_host_workspace_size.argtypes = [i, i, i, i, i]
+        lib.sa_rope_attn_host_workspace_size.restype = sz
+        lib.sa_rope_attn_host.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(f), i, vp, sz, vp]
+        lib.sa_rope_attn_host.restype = i
         lib.sa_rope_attn_qknorm.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(f), ctypes.POINTER(f), f,
                                             vp, i, i, i, i, i, ctypes.POINTER(f), i, vp, sz, vp]
         lib.sa_rope_attn_qknorm.restype = i
@@ -179,6 +184,23 @@ def sa_rope_qk(handle: int, q: int, k: int, positions: Optional[int], q_rot: int
         ctypes.c_void_p(handle), ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(positions),
         ctypes.c_void_p(q_rot), ctypes.c_void_p(k_rot), int(B), int(H), int(L), int(d), int(nmaps),
         int(dtype), ctypes.c_void_p(stream)))
+
+
+def sa_rope_attn_host_workspace_size(B: int, H: int, L: int, d: int, differential: bool) -> int:
+    return int(load_library().sa_rope_attn_host_workspace_size(int(B), int(H), int(L), int(d), int(bool(differential))))
+
+
+def sa_rope_attn_host(handle: int, q: int, k: int, v: int, positions: Optional[int], out: int,
+                      B: int, H: int, L: int, d: int, window: int, lam: Optional[Sequence[float]],
+                      dtype: int, workspace: Optional[int], workspace_bytes: int,
+                      stream: Optional[int]) -> None:
+    """Enqueue RoPE + attention on HOST q, k, v, out (ints: host addresses; page-locked memory
+    overlaps the copies); positions and workspace are device addresses."""
+    _check(load_library().sa_rope_attn_host(
+        ctypes.c_void_p(handle), ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v),
+        ctypes.c_void_p(positions), ctypes.c_void_p(out), int(B), int(H), int(L), int(d),
+        int(window), _lam(lam), int(dtype), ctypes.c_void_p(workspace), ctypes.c_size_t(workspace_bytes),
+        ctypes.c_void_p(stream)))
 
 
 def _gamma(g):

@@ -25,6 +25,10 @@ struct sa_attn_s {
   int* d_err;  // 4-byte device error word
   PFN_cuTensorMapEncodeTiled_v12000 encode;
   unsigned long long timeout_ns;
+  // sa_rope_attn_host: copy-in, copy-out and per-chunk compute streams, and their events
+  cudaStream_t hs_in, hs_out, hs_comp[sa::kHostChunks];
+  cudaEvent_t he_entry, he_in[sa::kHostChunks], he_done[sa::kHostChunks], he_exit;
+  bool host_ready;
 };
 
 namespace {
@@ -86,6 +90,34 @@ bool qk_elems(int B, int H, int L, int nmaps, size_t* out) {
   return true;
 }
 
+
+// Streams and events of sa_rope_attn_host, created with the handle (false if any failed; the
+// host entry then reports SA_ERR_CUDA).
+bool create_host_streams(sa_attn_s* h) {
+  bool good = cudaStreamCreateWithFlags(&h->hs_in, cudaStreamNonBlocking) == cudaSuccess;
+  good = good && cudaStreamCreateWithFlags(&h->hs_out, cudaStreamNonBlocking) == cudaSuccess;
+  for (int c = 0; c < sa::kHostChunks; ++c) {
+    good = good && cudaStreamCreateWithFlags(&h->hs_comp[c], cudaStreamNonBlocking) == cudaSuccess;
+    good = good && cudaEventCreateWithFlags(&h->he_in[c], cudaEventDisableTiming) == cudaSuccess;
+    good = good && cudaEventCreateWithFlags(&h->he_done[c], cudaEventDisableTiming) == cudaSuccess;
+  }
+  good = good && cudaEventCreateWithFlags(&h->he_entry, cudaEventDisableTiming) == cudaSuccess;
+  good = good && cudaEventCreateWithFlags(&h->he_exit, cudaEventDisableTiming) == cudaSuccess;
+  return good;
+}
+
+void destroy_host_streams(sa_attn_s* h) {
+  // (destroying a null stream or event handle is harmless)
+  if (h->hs_in) cudaStreamDestroy(h->hs_in);
+  if (h->hs_out) cudaStreamDestroy(h->hs_out);
+  for (int c = 0; c < sa::kHostChunks; ++c) {
+    if (h->hs_comp[c]) cudaStreamDestroy(h->hs_comp[c]);
+    if (h->he_in[c]) cudaEventDestroy(h->he_in[c]);
+    if (h->he_done[c]) cudaEventDestroy(h->he_done[c]);
+  }
+  if (h->he_entry) cudaEventDestroy(h->he_entry);
+  if (h->he_exit) cudaEventDestroy(h->he_exit);
+}
 
 // Shape / dtype checks shared by the entry points.
 sa_status check_shape(const char* fn, int B, int H, int L, int d, sa_dtype dtype, bool diff) {
@@ -355,9 +387,11 @@ sa_status sa_attn_create(sa_attn_t* handle, int device, float rope_base) {
   }
   h->rope_blocks_per_sm = sa::rope_blocks_per_sm(false);
   h->rope_blocks_per_sm_norm = sa::rope_blocks_per_sm(true);
+  h->host_ready = create_host_streams(h);
   if ((e = cudaMemset(h->d_err, 0, sizeof(int))) != cudaSuccess ||
       (e = sa::fmha_set_attributes()) != cudaSuccess) {
     cudaFree(h->d_err);
+    destroy_host_streams(h);
     delete h;
     return fail(SA_ERR_CUDA, "sa_attn_create: %s", cudaGetErrorString(e));
   }
@@ -366,6 +400,7 @@ sa_status sa_attn_create(sa_attn_t* handle, int device, float rope_base) {
     // The warpgroup register split (setmaxnreg) is sized for this launch allocation; any
     // other value could make the register grow wait forever, so refuse to run.
     cudaFree(h->d_err);
+    destroy_host_streams(h);
     delete h;
     return fail(SA_ERR_UNSUPPORTED, "sa_attn_create: attention kernel built with %d registers per "
                 "thread, expected %d", regs, sa::kFmhaLaunchRegs);
@@ -380,6 +415,7 @@ sa_status sa_attn_destroy(sa_attn_t h) {
     DeviceGuard guard(h->device);
     cudaDeviceSynchronize();
     cudaFree(h->d_err);
+    destroy_host_streams(h);
   }
   delete h;
   return ok();
@@ -532,6 +568,152 @@ sa_status sa_rope_attn_qknorm(sa_attn_t h, const void* q, const void* k, const v
   return rope_attn_ws(fn, h, q, k, v, positions, out, B, H, L, d, window, lambda, dtype, workspace,
                       workspace_bytes, stream, &nrm);
 }
+
+}  // extern "C"
+
+// ---------------------------------------------------------------- host buffers
+
+namespace {
+
+// Chunks of sa_rope_attn_host: contiguous ranges of the B*H (batch, head) planes, at most
+// kHostChunks at a time in flight and at most kMaxDiffHeads planes each.  Every copy has a
+// fixed cost, so a chunk carries at least kHostChunkBytes of copies where the sizes allow.
+constexpr double kHostChunkBytes = 16.0 * 1024 * 1024;
+
+struct HostChunks {
+  long long planes;
+  int n;          // chunks
+  int max_len;    // planes in the largest chunk
+  long long first(int c) const { return c * planes / n; }
+  int len(int c) const { return static_cast<int>(first(c + 1) - first(c)); }
+};
+
+HostChunks host_chunks(int B, int H, int L, bool diff) {
+  HostChunks hc;
+  hc.planes = static_cast<long long>(B) * H;
+  // bytes copied per plane: q, k (both maps), v in and out out
+  const double plane_bytes = 2.0 * L * sa::kHeadDim * (diff ? 2 : 1) * 4;
+  const long long by_size = std::max<long long>(1, static_cast<long long>(hc.planes * plane_bytes / kHostChunkBytes));
+  long long n = std::min<long long>(std::min<long long>(sa::kHostChunks, by_size), hc.planes);
+  n = std::max<long long>(n, (hc.planes + sa::kMaxDiffHeads - 1) / sa::kMaxDiffHeads);
+  hc.n = static_cast<int>(n);
+  hc.max_len = static_cast<int>((hc.planes + n - 1) / n);
+  return hc;
+}
+
+// Device bytes of sa_rope_attn_host: q, k, v, out, then one sa_rope_attn workspace per compute
+// stream (for its largest chunk).
+size_t host_ws_bytes(int B, int H, int L, int d, bool diff, size_t* per_chunk) {
+  size_t nqk = 0;
+  if (d != sa::kHeadDim || !qk_elems(B, H, L, diff ? 2 : 1, &nqk)) return 0;
+  const HostChunks hc = host_chunks(B, H, L, diff);
+  const size_t nv = static_cast<size_t>(B) * H * L * (diff ? 2 : 1) * sa::kHeadDim;
+  const size_t chunk = sa_rope_attn_workspace_size(1, hc.max_len, L, d, diff);
+  if (chunk == 0) return 0;
+  if (per_chunk) *per_chunk = chunk;
+  return 2 * align256(nqk * 2) + 2 * align256(nv * 2) +
+         static_cast<size_t>(std::min(hc.n, sa::kHostChunks)) * chunk;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t sa_rope_attn_host_workspace_size(int B, int H, int L, int d, int differential) {
+  if (B <= 0 || H <= 0 || L <= 0 || L >= sa::kMaxL) return 0;
+  return host_ws_bytes(B, H, L, d, differential != 0, nullptr);
+}
+
+sa_status sa_rope_attn_host(sa_attn_t h, const void* q, const void* k, const void* v,
+                            const int32_t* positions, void* out, int B, int H, int L, int d,
+                            int window, const float* lambda, sa_dtype dtype, void* workspace,
+                            size_t workspace_bytes, sa_stream_t stream) {
+  const char* fn = "sa_rope_attn_host";
+  if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
+  if (!q || !k || !v || !out)
+    return fail(SA_ERR_INVALID_ARG, "%s: q, k, v and out must be non-NULL", fn);
+  if (!workspace || !aligned16(workspace))
+    return fail(SA_ERR_INVALID_ARG, "%s: workspace must be a 16-byte aligned device pointer", fn);
+  const bool diff = lambda != nullptr;
+  sa_status st = check_shape(fn, B, H, L, d, dtype, diff);
+  if (st != SA_OK) return st;
+  if ((st = check_lambda(fn, lambda, H)) != SA_OK) return st;
+  size_t per_chunk = 0;
+  const size_t need = host_ws_bytes(B, H, L, d, diff, &per_chunk);
+  if (workspace_bytes < need)
+    return fail(SA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn, need, workspace_bytes);
+  if (!h->host_ready) return fail(SA_ERR_CUDA, "%s: the handle's copy streams could not be created", fn);
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return fail(SA_ERR_CUDA, "cannot select device %d", h->device);
+
+  // per plane: q/k elements (both maps for the differential form) and v/out elements
+  const size_t pqk = static_cast<size_t>(diff ? 2 : 1) * L * sa::kHeadDim;
+  const size_t pv = static_cast<size_t>(L) * (diff ? 2 : 1) * sa::kHeadDim;
+  const size_t nqk = static_cast<size_t>(B) * H * pqk, nv = static_cast<size_t>(B) * H * pv;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  uint8_t* dq = ws;
+  uint8_t* dk = dq + align256(nqk * 2);
+  uint8_t* dv = dk + align256(nqk * 2);
+  uint8_t* dout = dv + align256(nv * 2);
+  uint8_t* regions = dout + align256(nv * 2);
+  const cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+
+  const HostChunks hc = host_chunks(B, H, L, diff);
+  if (hc.n == 1) {
+    // one chunk: nothing to overlap, so everything goes on `stream` in order
+    cudaError_t e = cudaMemcpyAsync(dq, q, nqk * 2, cudaMemcpyHostToDevice, cs);
+    e = e != cudaSuccess ? e : cudaMemcpyAsync(dk, k, nqk * 2, cudaMemcpyHostToDevice, cs);
+    e = e != cudaSuccess ? e : cudaMemcpyAsync(dv, v, nv * 2, cudaMemcpyHostToDevice, cs);
+    if (e != cudaSuccess) return fail(SA_ERR_CUDA, "%s: copy in: %s", fn, cudaGetErrorString(e));
+    st = rope_attn_ws(fn, h, dq, dk, dv, positions, dout, B, H, L, d, window, lambda, dtype, regions,
+                      per_chunk, stream, nullptr);
+    if (st != SA_OK) return st;
+    e = cudaMemcpyAsync(out, dout, nv * 2, cudaMemcpyDeviceToHost, cs);
+    if (e != cudaSuccess) return fail(SA_ERR_CUDA, "%s: copy out: %s", fn, cudaGetErrorString(e));
+    return ok();
+  }
+  // The caller's earlier work on `stream` comes first; every internal stream starts after it.
+  cudaError_t e = cudaEventRecord(h->he_entry, cs);
+  e = e != cudaSuccess ? e : cudaStreamWaitEvent(h->hs_in, h->he_entry, 0);
+  e = e != cudaSuccess ? e : cudaStreamWaitEvent(h->hs_out, h->he_entry, 0);
+  for (int c = 0; c < sa::kHostChunks && e == cudaSuccess; ++c) e = cudaStreamWaitEvent(h->hs_comp[c], h->he_entry, 0);
+  if (e != cudaSuccess) return fail(SA_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+
+  // Chunk c: copy its planes in (copy stream), RoPE + attention on compute stream c % kHostChunks
+  // (chunks on different streams run side by side), copy its output back (output stream).
+  for (int c = 0; c < hc.n; ++c) {
+    const long long p0 = hc.first(c);
+    const int len = hc.len(c);
+    const int slot = c % sa::kHostChunks;
+    const size_t oqk = static_cast<size_t>(p0) * pqk * 2, ov = static_cast<size_t>(p0) * pv * 2;
+    const size_t bqk = static_cast<size_t>(len) * pqk * 2, bv = static_cast<size_t>(len) * pv * 2;
+    e = cudaMemcpyAsync(dq + oqk, static_cast<const uint8_t*>(q) + oqk, bqk, cudaMemcpyHostToDevice, h->hs_in);
+    e = e != cudaSuccess ? e : cudaMemcpyAsync(dk + oqk, static_cast<const uint8_t*>(k) + oqk, bqk, cudaMemcpyHostToDevice, h->hs_in);
+    e = e != cudaSuccess ? e : cudaMemcpyAsync(dv + ov, static_cast<const uint8_t*>(v) + ov, bv, cudaMemcpyHostToDevice, h->hs_in);
+    e = e != cudaSuccess ? e : cudaEventRecord(h->he_in[slot], h->hs_in);
+    e = e != cudaSuccess ? e : cudaStreamWaitEvent(h->hs_comp[slot], h->he_in[slot], 0);
+    if (e != cudaSuccess) return fail(SA_ERR_CUDA, "%s: copy in: %s", fn, cudaGetErrorString(e));
+    float lam[sa::kMaxDiffHeads];
+    if (diff)
+      for (int i = 0; i < len; ++i) lam[i] = lambda[(p0 + i) % H];
+    st = rope_attn_ws(fn, h, dq + oqk, dk + oqk, dv + ov, positions, dout + ov, 1, len, L, d, window,
+                      diff ? lam : nullptr, dtype, regions + slot * per_chunk, per_chunk, h->hs_comp[slot], nullptr);
+    if (st != SA_OK) return st;
+    e = cudaEventRecord(h->he_done[slot], h->hs_comp[slot]);
+    e = e != cudaSuccess ? e : cudaStreamWaitEvent(h->hs_out, h->he_done[slot], 0);
+    e = e != cudaSuccess ? e : cudaMemcpyAsync(static_cast<uint8_t*>(out) + ov, dout + ov, bv, cudaMemcpyDeviceToHost, h->hs_out);
+    if (e != cudaSuccess) return fail(SA_ERR_CUDA, "%s: copy out: %s", fn, cudaGetErrorString(e));
+  }
+  // `stream` continues once the last output copy is done.
+  e = cudaEventRecord(h->he_exit, h->hs_out);
+  e = e != cudaSuccess ? e : cudaStreamWaitEvent(cs, h->he_exit, 0);
+  if (e != cudaSuccess) return fail(SA_ERR_CUDA, "%s: %s", fn, cudaGetErrorString(e));
+  return ok();
+}
+
+}  // extern "C"
+
+extern "C" {
 
 sa_status sa_qknorm_rope_qk(sa_attn_t h, const void* q, const void* k, const int32_t* positions,
                             const float* gamma_q, const float* gamma_k, float eps, void* q_rot,

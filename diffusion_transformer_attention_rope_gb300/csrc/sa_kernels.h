@@ -25,6 +25,7 @@ constexpr int kControlRegs = 56;
 static_assert(2 * 128 * kSoftmaxRegs + 128 * kControlRegs <= kFmhaThreads * kFmhaLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr int kMaxL = 1 << 24;        // positions and row indices stay exact in FP32 / int32
+constexpr int kHostChunks = 4;        // sa_rope_attn_host: planes are copied and computed in chunks
 
 // Bits of the device error word.
 constexpr int kErrProducer = 1;       // TMA warp gave up on a wait

@@ -148,6 +148,43 @@ SA_API sa_status sa_rope_attn(sa_attn_t handle,
                        sa_stream_t stream);
 
 /*
+ * sa_rope_attn on HOST buffers: q, k, v are copied to the device, the path runs, and out is
+ * copied back, all enqueued without blocking the host.  The (batch, head) planes are cut into
+ * chunks of about 16 MiB of copies, at most 4 (more when a chunk would exceed
+ * SA_MAX_DIFF_HEADS planes).  With one chunk everything runs on `stream` in order.  Otherwise
+ * chunk c is copied in on the handle's copy-in stream, computed on compute stream c mod 4
+ * (chunks on different streams run side by side on the GPU) and copied out on the copy-out
+ * stream, so copies overlap computation.  Work enqueued on `stream` before the call is
+ * ordered before it, and work enqueued on `stream` after it waits for the last output copy.
+ *
+ *   q, k, v, out  HOST memory, layouts as in sa_rope_attn.  Page-locked memory lets the
+ *                 copies run asynchronously and overlap; pageable memory works but the
+ *                 copies then serialise with the host.  out must stay valid (and unread)
+ *                 until `stream` reaches the point after the call.
+ *   positions     DEVICE int32 [L] or NULL, as in sa_rope_attn.
+ *   workspace     DEVICE scratch, 16-byte aligned, of at least
+ *                 sa_rope_attn_host_workspace_size bytes: device copies of q, k, v and out,
+ *                 then one sa_rope_attn workspace per compute stream.
+ *
+ * The results have the bits of sa_rope_attn run on each chunk's planes (a chunk is a
+ * contiguous range of the B*H planes, launched as B = 1 with its heads' lambdas).  Calls
+ * that share a handle share its internal streams and are ordered on them.  Errors as
+ * sa_rope_attn; SA_ERR_CUDA also when the handle's streams could not be created.
+ */
+SA_API size_t sa_rope_attn_host_workspace_size(int B, int H, int L, int d, int differential);
+
+SA_API sa_status sa_rope_attn_host(sa_attn_t handle,
+                                   const void* q, const void* k, const void* v,
+                                   const int32_t* positions,
+                                   void* out,
+                                   int B, int H, int L, int d,
+                                   int window,
+                                   const float* lambda,
+                                   sa_dtype dtype,
+                                   void* workspace, size_t workspace_bytes,
+                                   sa_stream_t stream);
+
+/*
  * sa_rope_attn with a QK-RMSNorm in front of RoPE.  The pages keep "RMSNorm +
  * RoPE around attention" as FP32 islands that guard against variance overflow
  * (sa3_trt README, "Notes on the design"; the encoder/decoder tiers page,

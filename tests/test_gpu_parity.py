@@ -567,3 +567,87 @@ def test_qknorm_full_size(attn, name):
     rows = sample_rows(w, np.random.default_rng(701))
     ref = _oracle_qknorm(x, gq, gk, 1e-6, rows=rows)
     compare(got.reshape(-1, w.dv)[rows], ref, f"qk-norm {name}")
+
+
+# ----------------------------------------------------------------------------- host buffers
+
+def host_chunks(B, H, L, diff):
+    """The host entry's chunks of the B*H planes (first plane, length): about one per 16 MiB of
+    copies, at most 4 (more when a chunk would exceed 128 planes)."""
+    P = B * H
+    plane_bytes = 2.0 * L * 64 * (2 if diff else 1) * 4
+    n = max(min(min(4, max(1, int(P * plane_bytes / (16 * 1024 * 1024)))), P), -(-P // 128))
+    return [(c * P // n, (c + 1) * P // n - c * P // n) for c in range(n)]
+
+
+@pytest.mark.parametrize("B,H,L,window,diff,dtype,pinned", [
+    (2, 3, 300, -1, False, "fp16", True),     # small: one chunk
+    (1, 12, 8192, 129, False, "fp16", True),  # 12 planes of 4 MiB of copies: 3 chunks of 4
+    (1, 6, 8192, 129, True, "bf16", True),    # differential: 3 chunks, each with its heads' lambdas
+    (1, 1, 129, -1, False, "fp16", False),    # one plane, pageable host memory
+])
+def test_host_buffers_match_device_chunks(attn, B, H, L, window, diff, dtype, pinned):
+    w = small("host", B=B, H=H, L=L, window=window, nmaps=2 if diff else 1, dv=128 if diff else 64,
+              dtype=dtype, seed=900 + L, lam=("uniform", 0.2, 0.8) if diff else None)
+    x = synth.make_inputs(w)
+    t = TDT[dtype]
+    host = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(t)
+    qh, kh, vh = host(x["q"]), host(x["k"]), host(x["v"])
+    oh = torch.full((B, H, L, w.dv), 7.0, dtype=t)
+    if pinned:
+        qh, kh, vh, oh = qh.pin_memory(), kh.pin_memory(), vh.pin_memory(), oh.pin_memory()
+    lam = None if x["lam"] is None else [float(v) for v in x["lam"]]
+    dt = sa.SA_BF16 if dtype == "bf16" else sa.SA_FP16
+    n = sa.sa_rope_attn_host_workspace_size(B, H, L, 64, diff)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    sa.sa_rope_attn_host(attn.handle, qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), None, oh.data_ptr(),
+                         B, H, L, 64, window, lam, dt, ws.data_ptr(), n, s)
+    torch.cuda.synchronize()
+    attn.check()
+    got = oh.float().numpy().astype(np.float64)
+    compare(got, oracle.rope_attn_workload(x), "host buffers", dtype=dtype)
+    # each chunk has the bits of the device path on that chunk's planes (B = 1, its heads' lambdas)
+    nm = 2 if diff else 1
+    qd = dev(x["q"], dtype).reshape(B * H, nm, L, 64)
+    kd = dev(x["k"], dtype).reshape(B * H, nm, L, 64)
+    vd = dev(x["v"], dtype).reshape(B * H, L, w.dv)
+    flat = got.reshape(B * H, L, w.dv)
+    for p0, ln in host_chunks(B, H, L, diff):
+        o = torch.empty((1, ln, L, w.dv), dtype=t, device="cuda")
+        wsc = torch.empty(sa.sa_rope_attn_workspace_size(1, ln, L, 64, diff), dtype=torch.uint8, device="cuda")
+        lc = None if lam is None else [lam[(p0 + i) % H] for i in range(ln)]
+        qc, kc, vc = (a[p0:p0 + ln].contiguous() for a in (qd, kd, vd))
+        sa.sa_rope_attn(attn.handle, qc.data_ptr(), kc.data_ptr(), vc.data_ptr(), None, o.data_ptr(), 1, ln, L,
+                        64, window, lc, dt, wsc.data_ptr(), wsc.numel(), s)
+        torch.cuda.synchronize()
+        assert np.array_equal(o.float().cpu().numpy().reshape(ln, L, w.dv), flat[p0:p0 + ln])
+
+
+def test_host_buffers_full_size(attn):
+    w = synth.WORKLOADS["dit_l4096_outliers"]     # 3 chunks of 8 planes
+    x = synth.make_inputs(w)
+    host = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.float16).pin_memory()
+    qh, kh, vh = host(x["q"]), host(x["k"]), host(x["v"])
+    oh = torch.empty((w.B, w.H, w.L, w.dv), dtype=torch.float16).pin_memory()
+    n = sa.sa_rope_attn_host_workspace_size(w.B, w.H, w.L, 64, False)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    for _ in range(2):     # the second call reuses the handle's streams and events
+        sa.sa_rope_attn_host(attn.handle, qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), None, oh.data_ptr(),
+                             w.B, w.H, w.L, 64, -1, None, sa.SA_FP16, ws.data_ptr(), n,
+                             torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    attn.check()
+    rows = sample_rows(w, np.random.default_rng(702))
+    compare(oh.float().numpy().astype(np.float64).reshape(-1, w.dv)[rows], oracle.rope_attn_workload(x, rows=rows),
+            "host buffers dit_l4096_outliers")
+
+
+def test_host_buffers_workspace_checked(attn):
+    q = torch.zeros((1, 2, 64, 64), dtype=torch.float16).pin_memory()
+    n = sa.sa_rope_attn_host_workspace_size(1, 2, 64, 64, False)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    with pytest.raises(sa.SaAttnError) as e:
+        sa.sa_rope_attn_host(attn.handle, q.data_ptr(), q.data_ptr(), q.data_ptr(), None, q.data_ptr(), 1, 2, 64, 64,
+                             -1, None, sa.SA_FP16, ws.data_ptr(), n - 1, None)
+    assert e.value.status == 6
