@@ -78,10 +78,14 @@ def load_peaks():
 
 
 def kernel_sha() -> str:
+    """Hash of the attention kernel's source with comments and blank lines removed, so that the
+    stored ncu counters stay valid across comment-only edits and no others."""
     import hashlib
+    import re
 
     path = os.path.join(ROOT, "diffusion_transformer_attention_rope_gb300", "csrc", "sa_fmha.cu")
-    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    code = [re.sub(r"\s*//.*$", "", ln).rstrip() for ln in open(path).read().splitlines()]
+    return hashlib.sha256("\n".join(ln for ln in code if ln).encode()).hexdigest()[:16]
 
 
 def load_traffic(workload: str):

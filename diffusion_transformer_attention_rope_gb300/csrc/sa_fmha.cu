@@ -7,22 +7,29 @@
 // accumulators (HF discussion #6 "sm_120 SAME-L", section "How the kernels differ"), and the
 // symmetric sliding window |i - j| <= w (same page, "Three gotchas").
 //
-// One CTA (320 threads, 1 per SM) owns 256 query rows of one (batch, head) as two 128-row
-// tiles (standard), or 128 rows with both maps (differential).  Warp roles:
-//   warps 0-3, 4-7  softmax warpgroups, one per tile / map: thread = query row = TMEM lane.
-//   warp 8          TMA producer: Q tiles once, then a ring of K/V stages (128 keys each).
-//   warp 9          TMEM allocator and the single-thread tcgen05.mma issuer.
-// Per K/V tile and warpgroup s:
+// One CTA (384 threads, 1 per SM) owns one unit: 256 query rows of one (batch, head) as two
+// 128-row tiles (standard), or 128 rows with both maps (differential).  Warp roles:
+//   warps 0-3, 4-7  softmax warpgroups, one per tile / map (stream s): thread = query row =
+//                   TMEM lane; with a raw q they first rotate their Q row in shared memory
+//                   (RoPE prologue, from the RoPE pass's FP32 (cos, sin) table).
+//   warp 8          TMA producer of Q and of the K ring (128 keys per stage).
+//   warp 9          TMEM allocator and the MMA issuer of stream 0.
+//   warp 10         the MMA issuer of stream 1.
+//   warp 11         TMA producer of the V ring.
+// Per K/V tile and stream s:
 //   S_s = Q_s K^T      tcgen05.mma, A and B from 128B-swizzled smem, fp32 into TMEM
 //   P_s = exp2(S_s*c - m)   softmax warps: tcgen05.ld S, row max, lazy rescale of O_s
 //                      (only when the running max grows by more than 2^8), fp16/bf16 P
-//                      written back to TMEM with tcgen05.st
-//   O_s += P_s V       tcgen05.mma, A = P from TMEM, B = V (MN-major) from smem
+//                      written to TMEM (standard) or to shared memory (differential)
+//   O_s += P_s V       tcgen05.mma, A = P from TMEM or smem, B = V (MN-major) from smem
+// The two warpgroups take turns on the exponential phase; each stream's S buffer is released
+// as soon as the softmax warps hold S in registers, so the next S MMA overlaps the softmax.
 // TMEM (512 columns): standard S0|S1|P0|P1|O0|O1 = 128|128|64|64|64|64;
-// differential S0|S1|O0|O1 = 128|128|128|128 with P_s written over the first 64 columns of
-// S_s (the issuer waits for P_s V to finish before it writes the next S_s there).
-// The sliding window visits only the K/V tiles that intersect [q0 - w, q_last + w]; element
-// masks are applied only on tiles that are not entirely inside every row's window.
+// differential S0|S1|O0|O1 = 128|128|128|128.
+// The sliding window visits only the key tiles of [q0 - w, q_last + w], tiled from its first
+// key; element masks are applied only on tiles that are not entirely inside every row's window.
+// When the units leave the GPU's last wave partly empty, the tail units are cut into key-range
+// pieces (one CTA each) whose FP32 partial results the last piece merges in a fixed order.
 // Every wait is bounded: on timeout a warp sets the device error word and a CTA-wide abort
 // flag, waits (bounded) for its own copies / MMAs in flight, and the CTA frees TMEM and exits.
 #include <type_traits>
@@ -36,7 +43,7 @@ namespace {
 constexpr int kTile = kBlockM * kHeadDim * 2;  // bytes of one 128 x 64 fp16/bf16 tile (16 KB)
 constexpr int kTmaWarp = 8;   // TMA producer of Q and the K ring
 constexpr int kMmaWarp = 9;    // first MMA issuer (stream 0); also allocates TMEM
-constexpr int kMmaWarp1 = 10;  // second MMA issuer (stream 1)
+                               // (warp 10: the MMA issuer of stream 1)
 constexpr int kTmaWarpV = 11;  // TMA producer of the V ring
 constexpr uint32_t kTmemCols = 512;
 
