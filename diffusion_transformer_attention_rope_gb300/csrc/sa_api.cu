@@ -18,8 +18,7 @@
 struct sa_attn_s {
   int device;
   int num_sms;
-  int rope_blocks_per_sm;       // RoPE pass, without / with the QK-RMSNorm
-  int rope_blocks_per_sm_norm;
+  int rope_blocks_per_sm[2][2];   // RoPE pass: [rotates q too][QK-RMSNorm]
   float rope_base;
   float inv_freq[sa::kHeadDim / 2];
   int* d_err;  // 4-byte device error word
@@ -196,7 +195,7 @@ sa_status launch_rope(const sa_attn_s* h, const void* q, const void* k, const in
     ra.gamma_k[i] = nrm ? nrm->gamma_k[i] : 1.0f;
   }
   cudaError_t e = sa::rope_launch(ra, dtype == SA_BF16, h->num_sms,
-                                  nrm ? h->rope_blocks_per_sm_norm : h->rope_blocks_per_sm,
+                                  h->rope_blocks_per_sm[q != nullptr][nrm != nullptr],
                                   reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(SA_ERR_CUDA, "RoPE launch: %s", cudaGetErrorString(e));
   return ok();
@@ -385,8 +384,8 @@ sa_status sa_attn_create(sa_attn_t* handle, int device, float rope_base) {
     delete h;
     return fail(SA_ERR_CUDA, "sa_attn_create: cudaMalloc: %s", cudaGetErrorString(e));
   }
-  h->rope_blocks_per_sm = sa::rope_blocks_per_sm(false);
-  h->rope_blocks_per_sm_norm = sa::rope_blocks_per_sm(true);
+  for (int wq = 0; wq < 2; ++wq)
+    for (int nm = 0; nm < 2; ++nm) h->rope_blocks_per_sm[wq][nm] = sa::rope_blocks_per_sm(wq != 0, nm != 0);
   h->host_ready = create_host_streams(h);
   if ((e = cudaMemset(h->d_err, 0, sizeof(int))) != cudaSuccess ||
       (e = sa::fmha_set_attributes()) != cudaSuccess) {

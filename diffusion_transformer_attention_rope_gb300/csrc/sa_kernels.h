@@ -93,9 +93,9 @@ constexpr int fmha_partial_floats(bool diff) { return 2 * kBlockM * ((diff ? 2 *
 constexpr int kMaxPieces = 160;
 constexpr int kMaxTailK = 4;
 
-// Blocks of the RoPE kernel resident per SM (from the occupancy calculator), without and with
-// the QK-RMSNorm.
-int rope_blocks_per_sm(bool qk_norm);
+// Blocks of the RoPE kernel resident per SM (from the occupancy calculator) for the variant
+// that rotates q as well as k (or k only), without or with the QK-RMSNorm.
+int rope_blocks_per_sm(bool with_q, bool qk_norm);
 cudaError_t rope_launch(const RopeArgs& a, bool bf16, int num_sms, int blocks_per_sm, cudaStream_t stream);
 
 cudaError_t fmha_set_attributes();

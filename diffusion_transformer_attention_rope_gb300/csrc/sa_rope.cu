@@ -164,13 +164,12 @@ __global__ void __launch_bounds__(kRopeThreads) rope_norm_kernel(const __grid_co
   rope_body<BF16, WITH_Q, true>(a);
 }
 
-template <bool NORM>
+// Resident blocks per SM of one variant (the fewer of its fp16 and bf16 forms).
+template <bool WITH_Q, bool NORM>
 int blocks_per_sm() {
-  const void* fns[4] = {
-      NORM ? reinterpret_cast<const void*>(rope_norm_kernel<false, true>) : reinterpret_cast<const void*>(rope_kernel<false, true>),
-      NORM ? reinterpret_cast<const void*>(rope_norm_kernel<true, true>) : reinterpret_cast<const void*>(rope_kernel<true, true>),
-      NORM ? reinterpret_cast<const void*>(rope_norm_kernel<false, false>) : reinterpret_cast<const void*>(rope_kernel<false, false>),
-      NORM ? reinterpret_cast<const void*>(rope_norm_kernel<true, false>) : reinterpret_cast<const void*>(rope_kernel<true, false>)};
+  const void* fns[2] = {
+      NORM ? reinterpret_cast<const void*>(rope_norm_kernel<false, WITH_Q>) : reinterpret_cast<const void*>(rope_kernel<false, WITH_Q>),
+      NORM ? reinterpret_cast<const void*>(rope_norm_kernel<true, WITH_Q>) : reinterpret_cast<const void*>(rope_kernel<true, WITH_Q>)};
   int least = 1 << 30;
   for (const void* f : fns) {
     int n = 0;
@@ -188,7 +187,10 @@ void launch_variant(const RopeArgs& a, dim3 grid, cudaStream_t stream) {
 
 }  // namespace
 
-int rope_blocks_per_sm(bool qk_norm) { return qk_norm ? blocks_per_sm<true>() : blocks_per_sm<false>(); }
+int rope_blocks_per_sm(bool with_q, bool qk_norm) {
+  if (with_q) return qk_norm ? blocks_per_sm<true, true>() : blocks_per_sm<true, false>();
+  return qk_norm ? blocks_per_sm<false, true>() : blocks_per_sm<false, false>();
+}
 
 cudaError_t rope_launch(const RopeArgs& a_in, bool bf16, int num_sms, int blocks_per_sm,
                         cudaStream_t stream) {
