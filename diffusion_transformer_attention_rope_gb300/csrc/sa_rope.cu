@@ -1,7 +1,8 @@
 // sa_rope.cu -- RoPE pre-pass: q' = RoPE(q), k' = RoPE(k) in FP32, cast back to fp16/bf16.
 //
 // HF discussion #3 "fp16mixed attention-core fix", section "The bug": apply_rotary_pos_emb
-// computes in FP32 and ends with t.to(out_dtype), so attention then runs on fp16/bf16 q, k.
+// computes in FP32 and finishes with a cast to the output dtype, so attention then runs on
+// fp16/bf16 q, k.
 // Rotate-half over the full head dim (d = 64): pair (i, i + 32) at position p turns by
 // theta = p * inv_freq[i], inv_freq[i] = base^(-2i/64) held as FP32.  The angle itself is an
 // FP32 product and sin/cos are the full-precision single-precision functions: the sa3_trt
@@ -10,8 +11,8 @@
 // With a table pointer the pass also writes each position's 32 (cos, sin) pairs (FP32), which
 // the attention kernel uses to rotate q in its prologue; q is then not touched here.
 //
-// Optional QK-RMSNorm (the pages keep "RMSNorm + RoPE around attention" as FP32 islands that
-// guard variance overflow): each row is first scaled by gamma / sqrt(mean(x^2) + eps) in FP32,
+// Optional QK-RMSNorm (the pages run RMSNorm and RoPE next to attention in FP32, so that
+// variances cannot overflow fp16): each row is first scaled by gamma / sqrt(mean(x^2) + eps) in FP32,
 // then rotated, then cast once.  The 4 threads of a row (consecutive lanes) add their partial
 // sums of squares with a 2-step butterfly.
 //

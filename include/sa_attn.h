@@ -6,8 +6,9 @@
  *
  *   RoPE on q and k, rotate-half over the full head dim, in FP32, then cast
  *   back to the storage dtype (HF discussion #3 "fp16mixed attention-core fix",
- *   section "The bug": apply_rotary_pos_emb computes in FP32 and ends with
- *   t.to(out_dtype); section "The fix": Mul(fp32) -> Cast(fp16)x2):
+ *   section "The bug": apply_rotary_pos_emb computes in FP32 and finishes
+ *   with a cast to the output dtype; section "The fix": the rotation is
+ *   multiplied out in FP32, then q and k are cast to fp16):
  *       theta_{p,i} = p * rope_base^(-2i/d),  i < d/2
  *       x'_i       = x_i cos(theta) - x_{i+d/2} sin(theta)
  *       x'_{i+d/2} = x_{i+d/2} cos(theta) + x_i sin(theta)
@@ -185,8 +186,8 @@ SA_API sa_status sa_rope_attn_host(sa_attn_t handle,
                                    sa_stream_t stream);
 
 /*
- * sa_rope_attn with a QK-RMSNorm in front of RoPE.  The pages keep "RMSNorm +
- * RoPE around attention" as FP32 islands that guard against variance overflow
+ * sa_rope_attn with a QK-RMSNorm in front of RoPE.  The pages run RMSNorm and
+ * RoPE next to attention in FP32, so that variances cannot overflow fp16
  * (sa3_trt README, "Notes on the design"; the encoder/decoder tiers page,
  * "Where the quantization goes, per tier").  Here every row x of q and k (d
  * values, each map of the differential form alike) becomes, in FP32,

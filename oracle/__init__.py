@@ -12,9 +12,9 @@ Functions and what they follow:
                      "The bug": ``apply_rotary_pos_emb`` computes in FP32 and
                      casts back; here FP64 without a cast).
 * ``round_to``    -- round-to-nearest-even cast to fp16 / bf16 (the cast-back of
-                     ``t.to(out_dtype)`` in the same section).
+                     the RoPE function's final cast, same section).
 * ``rmsnorm``     -- FP64 RMSNorm of a row over the head dim with a learned
-                     gamma (the FP32 "RMSNorm islands" kept around attention,
+                     gamma (the pages keep RMSNorm next to attention in FP32,
                      sa3_trt README "Notes on the design").
 * ``rope_attn``   -- the full core: RoPE, cast-back, exact two-pass softmax
                      attention, the differential subtraction (HF discussion #6,

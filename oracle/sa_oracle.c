@@ -13,9 +13,9 @@
  *      10000): theta_{p,i} = p * base^(-2i/d) for i < d/2, and
  *      x'_i = x_i cos - x_{i+d/2} sin,  x'_{i+d/2} = x_{i+d/2} cos + x_i sin.
  *      The pages say RoPE runs in FP32 and casts back to the autocast dtype
- *      ("apply_rotary_pos_emb ends with t.to(out_dtype)"; graph
- *      "Mul(fp32) -> Cast(fp16)x2", HF discussion #3 "fp16mixed attention-core
- *      fix", sections "The bug" and "The fix").  Here the rotation is FP64 and,
+ *      (apply_rotary_pos_emb finishes with a cast to the output dtype, and the
+ *      exported graph multiplies in FP32 before two casts to fp16; HF discussion
+ *      #3 "fp16mixed attention-core fix", sections "The bug" and "The fix").  Here the rotation is FP64 and,
  *      in the default "method" cast mode, the rotated q/k are rounded to the
  *      storage dtype (round to nearest even) and decoded back to double.
  *      Cast mode "exact" skips that rounding.
@@ -31,8 +31,8 @@
  *      symmetric); window < 0 means full attention.  Only keys in
  *      [max(0, i-w), min(L-1, i+w)] are visited; masked keys contribute
  *      exp(-inf) = 0, so this is exact.
- *   6. Optional QK-RMSNorm before RoPE (the pages keep "RMSNorm + RoPE
- *      around attention" as FP32 islands that guard variance overflow; sa3_trt
+ *   6. Optional QK-RMSNorm before RoPE (the pages run RMSNorm and RoPE next
+ *      to attention in FP32, so that variances cannot overflow fp16; sa3_trt
  *      README "Notes on the design" and the encoder/decoder page's "Where the
  *      quantization goes, per tier"): every q and k row of d values becomes
  *      x_c * gamma_c / sqrt(mean_c(x_c^2) + eps), with one learned gamma[d]

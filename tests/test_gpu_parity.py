@@ -251,7 +251,7 @@ def test_full_size_workload(attn, name):
 # ----------------------------------------------------------------------------- behaviour
 
 def test_bit_reproducible(attn):
-    # the pages' fp16 engine is "bit-reproducible run to run"
+    # the pages' fp16 engine gives the same bits on every run
     x = synth.make_inputs(synth.WORKLOADS["diff_l4096"])
     a = run_gpu(attn, x)
     b = run_gpu(attn, x)
