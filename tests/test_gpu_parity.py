@@ -585,6 +585,7 @@ def host_chunks(B, H, L, diff):
     (1, 12, 8192, 129, False, "fp16", True),  # 12 planes of 4 MiB of copies: 3 chunks of 4
     (1, 6, 8192, 129, True, "bf16", True),    # differential: 3 chunks, each with its heads' lambdas
     (1, 1, 129, -1, False, "fp16", False),    # one plane, pageable host memory
+    (5, 128, 64, -1, True, "bf16", True),     # 640 planes: 5 chunks of 128, streams reused
 ])
 def test_host_buffers_match_device_chunks(attn, B, H, L, window, diff, dtype, pinned):
     w = small("host", B=B, H=H, L=L, window=window, nmaps=2 if diff else 1, dv=128 if diff else 64,
