@@ -491,6 +491,7 @@ def run_ours(args):
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": total_ms / args.steps,
+        "step_ms": {"median": statistics.median(step_ms), "min": min(step_ms), "max": max(step_ms)},
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
