@@ -652,3 +652,30 @@ def test_host_buffers_workspace_checked(attn):
         sa.sa_rope_attn_host(attn.handle, q.data_ptr(), q.data_ptr(), q.data_ptr(), None, q.data_ptr(), 1, 2, 64, 64,
                              -1, None, sa.SA_FP16, ws.data_ptr(), n - 1, None)
     assert e.value.status == 6
+
+
+# ----------------------------------------------------------------------------- random shapes
+
+def _random_case(i):
+    rng = np.random.default_rng(5000 + i)
+    diff = bool(rng.integers(0, 2))
+    L = int(rng.integers(1, 700))
+    window = -1 if rng.random() < 0.4 else int(rng.integers(0, L + 6))
+    return dict(B=int(rng.integers(1, 4)), H=int(rng.integers(1, 5)), L=L, window=window, diff=diff,
+                dtype=["fp16", "bf16"][int(rng.integers(0, 2))],
+                positions=None if rng.random() < 0.5 else rng.integers(0, 20000, L).astype(np.int32))
+
+
+@pytest.mark.parametrize("i", range(16))
+def test_random_shapes_match_oracle(attn, i):
+    # seeded random batch, heads, length (ragged), window (including 0 and >= L - 1), maps, dtype
+    # and positions, through sa_rope_attn (with its split region), against the oracle
+    c = _random_case(i)
+    w = small("rand", B=c["B"], H=c["H"], L=c["L"], window=c["window"], nmaps=2 if c["diff"] else 1,
+              dv=128 if c["diff"] else 64, dtype=c["dtype"], seed=6000 + i,
+              lam=("uniform", 0.2, 0.8) if c["diff"] else None)
+    x = synth.make_inputs(w)
+    got = run_gpu(attn, x, positions=c["positions"])
+    if c["positions"] is not None:
+        x["positions"] = c["positions"]
+    compare(got, oracle.rope_attn_workload(x), f"random case {i}: {c}", dtype=c["dtype"])
