@@ -79,3 +79,40 @@ def test_set_timeout_rejects_bad_values():
         assert e.value.status == 1
     finally:
         sa.sa_attn_destroy(h)
+
+
+def test_timeout_through_the_host_entry_is_reported():
+    # the host-buffer entry runs its chunks on the handle's internal streams: a device-side
+    # timeout there reaches the same error word, and the handle stays usable
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    w = synth.Workload("fail_host", B=1, H=12, L=8192, window=129, seed=43)   # 3 chunks of 4 planes
+    x = synth.make_inputs(w)
+    host = lambda bits: torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.float16).pin_memory()
+    qh, kh, vh = host(x["q"]), host(x["k"]), host(x["v"])
+    oh = torch.zeros((w.B, w.H, w.L, w.dv), dtype=torch.float16).pin_memory()
+    n = sa.sa_rope_attn_host_workspace_size(w.B, w.H, w.L, w.d, False)
+    ws = torch.empty(n, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream().cuda_stream
+    h = sa.sa_attn_create(0)
+
+    def run():
+        sa.sa_rope_attn_host(h, qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), None, oh.data_ptr(), w.B, w.H, w.L,
+                             w.d, w.window, None, sa.SA_FP16, ws.data_ptr(), n, stream)
+        torch.cuda.synchronize()
+
+    try:
+        sa.sa_attn_set_timeout(h, 500)
+        run()
+        with pytest.raises(sa.SaAttnError) as e:
+            sa.sa_attn_check(h)
+        assert e.value.status == 4
+        sa.sa_attn_set_timeout(h, 1_000_000_000)
+        run()
+        sa.sa_attn_check(h)
+        rows = np.arange(0, w.B * w.H * w.L, 997)
+        ref = oracle.rope_attn_workload(x, rows=rows)
+        got = oh.float().numpy().astype(np.float64).reshape(-1, w.dv)[rows]
+        assert np.abs(got - ref).max() <= 4e-3
+    finally:
+        sa.sa_attn_destroy(h)
