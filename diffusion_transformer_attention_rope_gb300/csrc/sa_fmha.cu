@@ -217,7 +217,13 @@ __device__ __noinline__ bool q_rope_prologue(const float2* cs, int L, int grow, 
   return ok;
 }
 
-template <bool DIFF, bool BF16>
+// Key masking a launch needs, a template parameter because the softmax loop's speed depends on
+// its code size (the loop is close to the instruction cache's capacity): none (full attention,
+// L a multiple of 128), the sequence tail (full attention, the last key tile crosses L), or the
+// window (and the tail).
+constexpr int kMaskNone = 0, kMaskTail = 1, kMaskWindow = 2;
+
+template <bool DIFF, bool BF16, int MASK>
 __global__ void __launch_bounds__(kFmhaThreads, 1)
     fmha_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FmhaArgs a) {
@@ -529,17 +535,19 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         if (lane == 0) mbar_arrive(bar.s_free(s));
       }
 
-      const int key0 = k_first + (t_lo + it) * kBlockN;
-      const bool need_mask =
-          (key0 + kBlockN > L) ||
-          (w >= 0 && !(key0 >= rows_hi - w && key0 + kBlockN - 1 <= rows_lo + w));
-      if (need_mask) {
+      if (MASK != kMaskNone) {
+        const int key0 = k_first + (t_lo + it) * kBlockN;
+        const bool need_mask =
+            (key0 + kBlockN > L) ||
+            (MASK == kMaskWindow && !(key0 >= rows_hi - w && key0 + kBlockN - 1 <= rows_lo + w));
+        if (need_mask) {
 #pragma unroll
-        for (int j = 0; j < kBlockN; ++j) {
-          const int key = key0 + j;
-          bool valid = key < L;
-          if (w >= 0) valid = valid && key >= grow - w && key <= grow + w;
-          if (!valid) sr[j] = __float_as_uint(-INFINITY);
+          for (int j = 0; j < kBlockN; ++j) {
+            const int key = key0 + j;
+            bool valid = key < L;
+            if (MASK == kMaskWindow) valid = valid && key >= grow - w && key <= grow + w;
+            if (!valid) sr[j] = __float_as_uint(-INFINITY);
+          }
         }
       }
       // 8 independent chains; chain q covers elements q, q + 8, ..., q + 120.
@@ -808,13 +816,20 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
 
 template <bool DIFF, bool BF16>
 cudaError_t set_attr() {
-  return cudaFuncSetAttribute(fmha_kernel<DIFF, BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Cfg<DIFF>::SMEM_ALLOC);
+  cudaError_t e = cudaFuncSetAttribute(fmha_kernel<DIFF, BF16, kMaskNone>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<DIFF>::SMEM_ALLOC);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fmha_kernel<DIFF, BF16, kMaskTail>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<DIFF>::SMEM_ALLOC);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fmha_kernel<DIFF, BF16, kMaskWindow>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Cfg<DIFF>::SMEM_ALLOC);
+  return e;
 }
 
 // Launched with programmatic stream serialization: the CTAs may start while the previous
 // kernel on the stream (the RoPE pass) finishes; only the TMA warp waits for it.
-template <bool DIFF, bool BF16>
+template <bool DIFF, bool BF16, int MASK>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                    const FmhaArgs& a, long long num_ctas, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -827,16 +842,33 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fmha_kernel<DIFF, BF16>, tq, tk, tv, a);
+  return cudaLaunchKernelEx(&cfg, fmha_kernel<DIFF, BF16, MASK>, tq, tk, tv, a);
+}
+
+template <bool DIFF, bool BF16>
+cudaError_t launch_masked(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                          const FmhaArgs& a, long long num_ctas, cudaStream_t stream) {
+  if (a.window >= 0) return launch<DIFF, BF16, kMaskWindow>(tq, tk, tv, a, num_ctas, stream);
+  if (a.L % kBlockN != 0) return launch<DIFF, BF16, kMaskTail>(tq, tk, tv, a, num_ctas, stream);
+  return launch<DIFF, BF16, kMaskNone>(tq, tk, tv, a, num_ctas, stream);
 }
 
 }  // namespace
 
 bool fmha_check_registers(int* got) {
-  const void* fns[4] = {reinterpret_cast<const void*>(fmha_kernel<false, false>),
-                        reinterpret_cast<const void*>(fmha_kernel<false, true>),
-                        reinterpret_cast<const void*>(fmha_kernel<true, false>),
-                        reinterpret_cast<const void*>(fmha_kernel<true, true>)};
+  const void* fns[12] = {
+      reinterpret_cast<const void*>(fmha_kernel<false, false, kMaskNone>),
+      reinterpret_cast<const void*>(fmha_kernel<false, true, kMaskNone>),
+      reinterpret_cast<const void*>(fmha_kernel<true, false, kMaskNone>),
+      reinterpret_cast<const void*>(fmha_kernel<true, true, kMaskNone>),
+      reinterpret_cast<const void*>(fmha_kernel<false, false, kMaskTail>),
+      reinterpret_cast<const void*>(fmha_kernel<false, true, kMaskTail>),
+      reinterpret_cast<const void*>(fmha_kernel<true, false, kMaskTail>),
+      reinterpret_cast<const void*>(fmha_kernel<true, true, kMaskTail>),
+      reinterpret_cast<const void*>(fmha_kernel<false, false, kMaskWindow>),
+      reinterpret_cast<const void*>(fmha_kernel<false, true, kMaskWindow>),
+      reinterpret_cast<const void*>(fmha_kernel<true, false, kMaskWindow>),
+      reinterpret_cast<const void*>(fmha_kernel<true, true, kMaskWindow>)};
   for (const void* f : fns) {
     cudaFuncAttributes attr;
     if (cudaFuncGetAttributes(&attr, f) != cudaSuccess) return false;
@@ -857,10 +889,10 @@ cudaError_t fmha_set_attributes() {
 cudaError_t fmha_launch(bool diff, bool bf16, const CUtensorMap& tq, const CUtensorMap& tk,
                         const CUtensorMap& tv, const FmhaArgs& a, long long num_ctas,
                         cudaStream_t stream) {
-  if (diff) return bf16 ? launch<true, true>(tq, tk, tv, a, num_ctas, stream)
-                        : launch<true, false>(tq, tk, tv, a, num_ctas, stream);
-  return bf16 ? launch<false, true>(tq, tk, tv, a, num_ctas, stream)
-              : launch<false, false>(tq, tk, tv, a, num_ctas, stream);
+  if (diff) return bf16 ? launch_masked<true, true>(tq, tk, tv, a, num_ctas, stream)
+                        : launch_masked<true, false>(tq, tk, tv, a, num_ctas, stream);
+  return bf16 ? launch_masked<false, true>(tq, tk, tv, a, num_ctas, stream)
+              : launch_masked<false, false>(tq, tk, tv, a, num_ctas, stream);
 }
 
 }  // namespace sa
