@@ -217,6 +217,26 @@ __device__ __noinline__ bool q_rope_prologue(const float2* cs, int L, int grow, 
   return ok;
 }
 
+// O_s *= f in TMEM, the lazy rescale.  It is rare, and kept out of line it adds no code to the
+// softmax loop (whose speed depends on its size: the loop is close to the instruction cache's
+// capacity).
+template <int DV>
+__device__ __noinline__ void rescale_o(uint32_t taddr, float f) {
+#pragma unroll
+  for (int cc = 0; cc < DV / 32; ++cc) {
+    uint32_t o[32];
+    tmem_ld32_nowait(taddr + 32 * cc, o);
+    tmem_wait_ld_32(o);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const float2 v2 = fmul2(make_float2(__uint_as_float(o[j]), __uint_as_float(o[j + 1])), make_float2(f, f));
+      o[j] = __float_as_uint(v2.x);
+      o[j + 1] = __float_as_uint(v2.y);
+    }
+    tmem_st32(taddr + 32 * cc, o);
+  }
+}
+
 // Key masking a launch needs, a template parameter because the softmax loop's speed depends on
 // its code size (the loop is close to the instruction cache's capacity): none (full attention,
 // L a multiple of 128), the sequence tail (full attention, the last key tile crosses L), or the
@@ -622,24 +642,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         tmem_st32(tmem + C::p_col(s) + lane_off, pk);
         tmem_st32(tmem + C::p_col(s) + lane_off + 32, pk + 32);
       }
-      if (rescale) {
-        // O_s is stable here: P_s V of the previous tile has finished and P_s V of this
-        // tile waits for the arrive below.
-#pragma unroll
-        for (int cc = 0; cc < C::DV / 32; ++cc) {
-          uint32_t o[32];
-          tmem_ld32_nowait(tmem + C::o_col(s) + lane_off + 32 * cc, o);
-          tmem_wait_ld_32(o);
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const float2 v2 = fmul2(make_float2(__uint_as_float(o[j]), __uint_as_float(o[j + 1])),
-                                    make_float2(f, f));
-            o[j] = __float_as_uint(v2.x);
-            o[j + 1] = __float_as_uint(v2.y);
-          }
-          tmem_st32(tmem + C::o_col(s) + lane_off + 32 * cc, o);
-        }
-      }
+      if (rescale) rescale_o<C::DV>(tmem + C::o_col(s) + lane_off, f);
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
