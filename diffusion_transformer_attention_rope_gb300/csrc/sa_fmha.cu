@@ -561,13 +561,16 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
             (key0 + kBlockN > L) ||
             (MASK == kMaskWindow && !(key0 >= rows_hi - w && key0 + kBlockN - 1 <= rows_lo + w));
         if (need_mask) {
-#pragma unroll
-          for (int j = 0; j < kBlockN; ++j) {
-            const int key = key0 + j;
-            bool valid = key < L;
-            if (MASK == kMaskWindow) valid = valid && key >= grow - w && key <= grow + w;
-            if (!valid) sr[j] = __float_as_uint(-INFINITY);
+          // this row's valid keys are columns [j_lo, j_hi) of the tile (one compare per column
+          // against a bound computed once keeps the masking code short)
+          int j_hi = L - key0, j_lo = 0;
+          if (MASK == kMaskWindow) {
+            j_hi = min(j_hi, grow + w + 1 - key0);
+            j_lo = grow - w - key0;
           }
+#pragma unroll
+          for (int j = 0; j < kBlockN; ++j)
+            if (j >= j_hi || (MASK == kMaskWindow && j < j_lo)) sr[j] = __float_as_uint(-INFINITY);
         }
       }
       // 8 independent chains; chain q covers elements q, q + 8, ..., q + 120.
