@@ -243,6 +243,121 @@ __device__ __noinline__ void rescale_o(uint32_t taddr, float f) {
 // window (and the tail).
 constexpr int kMaskNone = 0, kMaskTail = 1, kMaskWindow = 2;
 
+// One key tile of a softmax warp (tile `it` of its unit, stream s): wait for S, load it and
+// release it, mask it (TMASK: none; the sequence tail, columns >= j_hi; or, when need_mask,
+// the window, columns outside [j_lo, j_hi)), row max and lazy rescale, exponentials on this
+// warp's turn, row sum, P stored for its P.V MMA.  Returns the warp-uniform wait outcome.
+template <bool DIFF, bool BF16, int TMASK>
+__device__ __forceinline__ bool softmax_tile(const Barriers& bar, int it, uint32_t tmem, uint32_t lane_off,
+                                             int s, int quarter, int lane, int r, uint32_t sP, float c,
+                                             float tau, bool need_mask, int j_lo, int j_hi, float& m_use,
+                                             float& l_sum, volatile int* abort_flag, int* err, uint64_t tmo) {
+  using C = Cfg<DIFF>;
+  bool ok;
+  ok = pwait(bar.s_full(s), it & 1, abort_flag, err, kErrSoftmax, tmo);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return false;
+  tc_fence_after();
+  uint32_t sr[kBlockN];
+#pragma unroll
+  for (int cc = 0; cc < kBlockN / 32; ++cc)
+    tmem_ld32_nowait(tmem + C::s_col(s) + lane_off + 32 * cc, sr + 32 * cc);
+  tmem_wait_ld_128(sr);
+  {
+    // S_s is in registers: the issuer may write the next S_s into these columns now.
+    // Every lane has waited for its own load; after the warp sync one lane arrives.
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar.s_free(s));
+  }
+
+  if (TMASK == kMaskTail || (TMASK == kMaskWindow && need_mask)) {
+    // this row's valid keys are columns [j_lo, j_hi) of the tile (one compare per column
+    // against bounds computed once keeps the masking code short)
+#pragma unroll
+    for (int j = 0; j < kBlockN; ++j)
+      if (j >= j_hi || (TMASK == kMaskWindow && j < j_lo)) sr[j] = __float_as_uint(-INFINITY);
+  }
+  // 8 independent chains; chain q covers elements q, q + 8, ..., q + 120.
+  float mx[8];
+#pragma unroll
+  for (int q = 0; q < 8; ++q) mx[q] = fmaxf(__uint_as_float(sr[q]), __uint_as_float(sr[q + 8]));
+#pragma unroll
+  for (int j = 16; j < kBlockN; j += 16) {
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+      mx[q] = fmax3(mx[q], __uint_as_float(sr[j + q]), __uint_as_float(sr[j + 8 + q]));
+  }
+  const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+
+  // Lazy rescale: keep the old running max unless this tile raises it by more than tau
+  // (P then stays <= 2^8).  The decision is warp-uniform because tcgen05.ld/st are.
+  float f = 1.0f;
+  bool rescale = false;
+  if (it == 0) {
+    m_use = mt;
+  } else if (__any_sync(0xffffffffu, mt > m_use + tau)) {
+    const float m_new = fmaxf(m_use, mt);
+    f = (m_new == m_use) ? 1.0f : ex2_approx((m_use - m_new) * c);
+    m_use = m_new;
+    rescale = true;
+  }
+  const float mb = (m_use == -INFINITY) ? 0.0f : m_use * c;
+  const float2 c2 = make_float2(c, c), nmb2 = make_float2(-mb, -mb);
+  ok = pwait(bar.turn(s, quarter), it & 1, abort_flag, err, kErrSoftmax, tmo);
+  ok = __all_sync(0xffffffffu, ok);
+  if (!ok) return false;
+  // Exponentials of the whole row into registers (packed pairs): P_s(it) is computed
+  // before the wait for P_s V(it - 1), which has the whole exponential phase to finish.
+  float2 sum0 = make_float2(0.0f, 0.0f), sum1 = make_float2(0.0f, 0.0f);
+  uint32_t pk[kBlockN / 2];
+#pragma unroll
+  for (int j = 0; j < kBlockN / 2; j += 2) {
+    const int e = 2 * j;
+    const float2 x0 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nmb2);
+    const float2 x1 = ffma2(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nmb2);
+    const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+    const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+    sum0 = fadd2(sum0, p0);
+    sum1 = fadd2(sum1, p1);
+    pk[j] = pack2<BF16>(p0.x, p0.y);
+    pk[j + 1] = pack2<BF16>(p1.x, p1.y);
+  }
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar.turn(1 - s, quarter));
+  const float2 sum = fadd2(sum0, sum1);
+  l_sum = fmaf(l_sum, f, sum.x + sum.y);
+  if (it > 0) {
+    // P_s and O_s are still read / written by P_s V of the previous tile until it is done.
+    ok = pwait(bar.pv_done(s), (it - 1) & 1, abort_flag, err, kErrSoftmax, tmo);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return false;
+    tc_fence_after();
+  }
+  if (DIFF) {
+    // row r of the K-major, 128-byte-swizzled P tile: atom h (keys 64h..64h+63),
+    // 16-byte chunk kq lands at chunk kq ^ (r & 7)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const uint32_t row_base = sP + s * 2 * kTile + h * kTile + r * 128;
+#pragma unroll
+      for (int kq = 0; kq < 8; ++kq)
+        st_shared_v4(row_base + ((kq ^ (r & 7)) << 4), pk[32 * h + 4 * kq], pk[32 * h + 4 * kq + 1],
+                     pk[32 * h + 4 * kq + 2], pk[32 * h + 4 * kq + 3]);
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  } else {
+    tmem_st32(tmem + C::p_col(s) + lane_off, pk);
+    tmem_st32(tmem + C::p_col(s) + lane_off + 32, pk + 32);
+  }
+  if (rescale) rescale_o<C::DV>(tmem + C::o_col(s) + lane_off, f);
+  tmem_wait_st();
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar.p_full(s));
+  return true;
+}
+
 template <bool DIFF, bool BF16, int MASK>
 __global__ void __launch_bounds__(kFmhaThreads, 1)
     fmha_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -537,120 +652,29 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       if (lane == 0) mbar_arrive(bar.q_ready(s));
     }
 
-    for (int it = 0; it < n_tiles; ++it) {
-      ok = pwait(bar.s_full(s), it & 1, abort_flag, a.err, kErrSoftmax, tmo);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
-      tc_fence_after();
-      uint32_t sr[kBlockN];
-#pragma unroll
-      for (int cc = 0; cc < kBlockN / 32; ++cc)
-        tmem_ld32_nowait(tmem + C::s_col(s) + lane_off + 32 * cc, sr + 32 * cc);
-      tmem_wait_ld_128(sr);
-      {
-        // S_s is in registers: the issuer may write the next S_s into these columns now.
-        // Every lane has waited for its own load; after the warp sync one lane arrives.
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar.s_free(s));
-      }
-
-      if (MASK != kMaskNone) {
+    // The tile that crosses the end of the sequence (the unit's last, if any) is peeled off the
+    // loop in the tail-masked kernel, so the loop body holds no masking code.
+    const bool peel_tail = MASK == kMaskTail && k_first + (t_lo + n_tiles) * kBlockN > L;
+    const int n_loop = n_tiles - (peel_tail ? 1 : 0);
+    for (int it = 0; it < n_loop; ++it) {
+      if (MASK != kMaskWindow) {
+        ok = softmax_tile<DIFF, BF16, kMaskNone>(bar, it, tmem, lane_off, s, quarter, lane, r, sP, c, tau, false,
+                                                 0, 0, m_use, l_sum, abort_flag, a.err, tmo);
+      } else {
         const int key0 = k_first + (t_lo + it) * kBlockN;
         const bool need_mask =
-            (key0 + kBlockN > L) ||
-            (MASK == kMaskWindow && !(key0 >= rows_hi - w && key0 + kBlockN - 1 <= rows_lo + w));
-        if (need_mask) {
-          // this row's valid keys are columns [j_lo, j_hi) of the tile (one compare per column
-          // against a bound computed once keeps the masking code short)
-          int j_hi = L - key0, j_lo = 0;
-          if (MASK == kMaskWindow) {
-            j_hi = min(j_hi, grow + w + 1 - key0);
-            j_lo = grow - w - key0;
-          }
-#pragma unroll
-          for (int j = 0; j < kBlockN; ++j)
-            if (j >= j_hi || (MASK == kMaskWindow && j < j_lo)) sr[j] = __float_as_uint(-INFINITY);
-        }
+            (key0 + kBlockN > L) || !(key0 >= rows_hi - w && key0 + kBlockN - 1 <= rows_lo + w);
+        ok = softmax_tile<DIFF, BF16, kMaskWindow>(bar, it, tmem, lane_off, s, quarter, lane, r, sP, c, tau,
+                                                   need_mask, grow - w - key0,
+                                                   min(L - key0, grow + w + 1 - key0), m_use, l_sum,
+                                                   abort_flag, a.err, tmo);
       }
-      // 8 independent chains; chain q covers elements q, q + 8, ..., q + 120.
-      float mx[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) mx[q] = fmaxf(__uint_as_float(sr[q]), __uint_as_float(sr[q + 8]));
-#pragma unroll
-      for (int j = 16; j < kBlockN; j += 16) {
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-          mx[q] = fmax3(mx[q], __uint_as_float(sr[j + q]), __uint_as_float(sr[j + 8 + q]));
-      }
-      const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
-
-      // Lazy rescale: keep the old running max unless this tile raises it by more than tau
-      // (P then stays <= 2^8).  The decision is warp-uniform because tcgen05.ld/st are.
-      float f = 1.0f;
-      bool rescale = false;
-      if (it == 0) {
-        m_use = mt;
-      } else if (__any_sync(0xffffffffu, mt > m_use + tau)) {
-        const float m_new = fmaxf(m_use, mt);
-        f = (m_new == m_use) ? 1.0f : ex2_approx((m_use - m_new) * c);
-        m_use = m_new;
-        rescale = true;
-      }
-      const float mb = (m_use == -INFINITY) ? 0.0f : m_use * c;
-      const float2 c2 = make_float2(c, c), nmb2 = make_float2(-mb, -mb);
-      ok = pwait(bar.turn(s, quarter), it & 1, abort_flag, a.err, kErrSoftmax, tmo);
-      ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
-      // Exponentials of the whole row into registers (packed pairs): P_s(it) is computed
-      // before the wait for P_s V(it - 1), which has the whole exponential phase to finish.
-      float2 sum0 = make_float2(0.0f, 0.0f), sum1 = make_float2(0.0f, 0.0f);
-      uint32_t pk[kBlockN / 2];
-#pragma unroll
-      for (int j = 0; j < kBlockN / 2; j += 2) {
-        const int e = 2 * j;
-        const float2 x0 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nmb2);
-        const float2 x1 = ffma2(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nmb2);
-        const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
-        const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
-        sum0 = fadd2(sum0, p0);
-        sum1 = fadd2(sum1, p1);
-        pk[j] = pack2<BF16>(p0.x, p0.y);
-        pk[j + 1] = pack2<BF16>(p1.x, p1.y);
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar.turn(1 - s, quarter));
-      const float2 sum = fadd2(sum0, sum1);
-      l_sum = fmaf(l_sum, f, sum.x + sum.y);
-      if (it > 0) {
-        // P_s and O_s are still read / written by P_s V of the previous tile until it is done.
-        ok = pwait(bar.pv_done(s), (it - 1) & 1, abort_flag, a.err, kErrSoftmax, tmo);
-        ok = __all_sync(0xffffffffu, ok);
-        if (!ok) break;
-        tc_fence_after();
-      }
-      if (DIFF) {
-        // row r of the K-major, 128-byte-swizzled P tile: atom h (keys 64h..64h+63),
-        // 16-byte chunk kq lands at chunk kq ^ (r & 7)
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t row_base = sP + s * 2 * kTile + h * kTile + r * 128;
-#pragma unroll
-          for (int kq = 0; kq < 8; ++kq)
-            st_shared_v4(row_base + ((kq ^ (r & 7)) << 4), pk[32 * h + 4 * kq], pk[32 * h + 4 * kq + 1],
-                         pk[32 * h + 4 * kq + 2], pk[32 * h + 4 * kq + 3]);
-        }
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      } else {
-        tmem_st32(tmem + C::p_col(s) + lane_off, pk);
-        tmem_st32(tmem + C::p_col(s) + lane_off + 32, pk + 32);
-      }
-      if (rescale) rescale_o<C::DV>(tmem + C::o_col(s) + lane_off, f);
-      tmem_wait_st();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar.p_full(s));
     }
+    if (peel_tail && ok)
+      ok = softmax_tile<DIFF, BF16, kMaskTail>(bar, n_loop, tmem, lane_off, s, quarter, lane, r, sP, c, tau, true,
+                                               0, L - (k_first + (t_lo + n_loop) * kBlockN), m_use, l_sum,
+                                               abort_flag, a.err, tmo);
 
     // ---------------------------------------------------------------- epilogue
     if (ok) ok = pwait(bar.o_full(s), 0, abort_flag, a.err, kErrSoftmax, tmo);
