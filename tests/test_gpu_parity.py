@@ -159,6 +159,47 @@ def test_q_rope_prologue_matches_prepass(attn, diff, dtype, window):
     compare(o2.float().cpu().numpy(), oracle.rope_attn_workload(x), "q prologue", dtype=dtype)
 
 
+@pytest.mark.parametrize("B,H,L,diff,dtype,window,explicit", [
+    (1, 3, 777, False, "fp16", -1, True),      # 12 CTAs
+    (1, 16, 1292, False, "fp16", -1, False),   # the L = 1292 DiT shape (96 CTAs)
+    (1, 3, 777, True, "bf16", 129, True),      # last-wave pieces
+    (1, 16, 2300, False, "fp16", -1, False),   # 144 CTAs
+    (2, 16, 1292, True, "bf16", -1, False),    # 352 units, last-wave pieces
+])
+def test_rope_attn_matches_two_pass_bits(attn, B, H, L, diff, dtype, window, explicit):
+    # the public call (K pass with the (cos, sin) table, q rotated in the attention kernel's
+    # prologue, workspace-backed last-wave pieces) has the bits of the two-pass path
+    # (sa_rope_qk, then sa_attn_fwd on q') across grid sizes, with and without positions.
+    w = small("twopass", B=B, H=H, L=L, window=window, nmaps=2 if diff else 1, dv=128 if diff else 64,
+              dtype=dtype, seed=77 + L, lam=("uniform", 0.2, 0.8) if diff else None)
+    x = synth.make_inputs(w)
+    nm = w.nmaps
+    q, k, v = dev(x["q"], dtype), dev(x["k"], dtype), dev(x["v"], dtype)
+    pos = torch.from_numpy(((np.arange(L) * 7) % 4099 + 3).astype(np.int32)).cuda() if explicit else None
+    pp = 0 if pos is None else pos.data_ptr()
+    lam = None if x["lam"] is None else [float(t) for t in x["lam"]]
+    dt = sa.SA_BF16 if dtype == "bf16" else sa.SA_FP16
+    s = torch.cuda.current_stream().cuda_stream
+    h = attn.handle
+    qr, kr = torch.empty_like(q), torch.empty_like(k)
+    split = torch.empty(sa.sa_attn_fwd_workspace_size(B, H, L, 64, diff), dtype=torch.uint8, device="cuda")
+    ws = torch.empty(sa.sa_rope_attn_workspace_size(B, H, L, 64, diff), dtype=torch.uint8, device="cuda")
+    o1 = torch.empty((B, H, L, w.dv), dtype=TDT[dtype], device="cuda")
+    o2 = torch.empty_like(o1)
+    sa.sa_rope_qk(h, q.data_ptr(), k.data_ptr(), pp or None, qr.data_ptr(), kr.data_ptr(), B, H, L, 64, nm, dt, s)
+    sa.sa_attn_fwd(h, qr.data_ptr(), kr.data_ptr(), v.data_ptr(), o1.data_ptr(), B, H, L, 64, window, lam, dt, s,
+                   split.data_ptr(), split.numel())
+    sa.sa_rope_attn(h, q.data_ptr(), k.data_ptr(), v.data_ptr(), pp or None, o2.data_ptr(), B, H, L, 64, window,
+                    lam, dt, ws.data_ptr(), ws.numel(), s)
+    torch.cuda.synchronize()
+    attn.check()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+    if L <= 1292 and B * H <= 3:
+        if explicit:
+            x["positions"] = pos.cpu().numpy()
+        compare(o2.float().cpu().numpy(), oracle.rope_attn_workload(x), "rope_attn", dtype=dtype)
+
+
 # ----------------------------------------------------------------------------- full outputs
 
 def test_tiny_workload(attn):
