@@ -576,7 +576,10 @@ namespace {
 
 // Chunks of sa_rope_attn_host: contiguous ranges of the B*H (batch, head) planes, at most
 // kHostChunks at a time in flight and at most kMaxDiffHeads planes each.  Every copy has a
-// fixed cost, so a chunk carries at least kHostChunkBytes of copies where the sizes allow.
+// fixed cost, so a chunk carries at least kHostChunkBytes of copies where the sizes allow;
+// copies of at least half that are still cut in two, so that one half's copies overlap the
+// other half's computation (measured: 94 -> 91 us per call at 10.6 MB of copies, while
+// 4 MiB chunks everywhere were slower at 50 MB).
 constexpr double kHostChunkBytes = 16.0 * 1024 * 1024;
 
 struct HostChunks {
@@ -592,7 +595,9 @@ HostChunks host_chunks(int B, int H, int L, bool diff) {
   hc.planes = static_cast<long long>(B) * H;
   // bytes copied per plane: q, k (both maps), v in and out out
   const double plane_bytes = 2.0 * L * sa::kHeadDim * (diff ? 2 : 1) * 4;
-  const long long by_size = std::max<long long>(1, static_cast<long long>(hc.planes * plane_bytes / kHostChunkBytes));
+  const double total = hc.planes * plane_bytes;
+  const long long by_size = total >= kHostChunkBytes ? static_cast<long long>(total / kHostChunkBytes)
+                            : (total >= kHostChunkBytes / 2 ? 2 : 1);
   long long n = std::min<long long>(std::min<long long>(sa::kHostChunks, by_size), hc.planes);
   n = std::max<long long>(n, (hc.planes + sa::kMaxDiffHeads - 1) / sa::kMaxDiffHeads);
   hc.n = static_cast<int>(n);

@@ -151,8 +151,8 @@ SA_API sa_status sa_rope_attn(sa_attn_t handle,
 /*
  * sa_rope_attn on HOST buffers: q, k, v are copied to the device, the path runs, and out is
  * copied back, all enqueued without blocking the host.  The (batch, head) planes are cut into
- * chunks of about 16 MiB of copies, at most 4 (more when a chunk would exceed
- * SA_MAX_DIFF_HEADS planes).  With one chunk everything runs on `stream` in order.  Otherwise
+ * chunks of about 16 MiB of copies (two from 8 MiB up), at most 4 (more when a chunk would
+ * exceed SA_MAX_DIFF_HEADS planes).  With one chunk everything runs on `stream` in order.  Otherwise
  * chunk c is copied in on the handle's copy-in stream, computed on compute stream c mod 4
  * (chunks on different streams run side by side on the GPU) and copied out on the copy-out
  * stream, so copies overlap computation.  Work enqueued on `stream` before the call is

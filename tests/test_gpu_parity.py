@@ -614,10 +614,12 @@ def test_qknorm_full_size(attn, name):
 
 def host_chunks(B, H, L, diff):
     """The host entry's chunks of the B*H planes (first plane, length): about one per 16 MiB of
-    copies, at most 4 (more when a chunk would exceed 128 planes)."""
+    copies (two from 8 MiB up), at most 4 (more when a chunk would exceed 128 planes)."""
     P = B * H
     plane_bytes = 2.0 * L * 64 * (2 if diff else 1) * 4
-    n = max(min(min(4, max(1, int(P * plane_bytes / (16 * 1024 * 1024)))), P), -(-P // 128))
+    total, mib16 = P * plane_bytes, 16 * 1024 * 1024
+    by_size = int(total / mib16) if total >= mib16 else (2 if total >= mib16 / 2 else 1)
+    n = max(min(min(4, by_size), P), -(-P // 128))
     return [(c * P // n, (c + 1) * P // n - c * P // n) for c in range(n)]
 
 
@@ -626,6 +628,7 @@ def host_chunks(B, H, L, diff):
     (1, 12, 8192, 129, False, "fp16", True),  # 12 planes of 4 MiB of copies: 3 chunks of 4
     (1, 6, 8192, 129, True, "bf16", True),    # differential: 3 chunks, each with its heads' lambdas
     (1, 1, 129, -1, False, "fp16", False),    # one plane, pageable host memory
+    (1, 16, 1292, -1, False, "fp16", True),   # 10.6 MB of copies: two chunks of 8 planes
     (5, 128, 64, -1, True, "bf16", True),     # 640 planes: 5 chunks of 128, streams reused
 ])
 def test_host_buffers_match_device_chunks(attn, B, H, L, window, diff, dtype, pinned):
