@@ -165,11 +165,21 @@ def test_q_rope_prologue_matches_prepass(attn, diff, dtype, window):
     (1, 3, 777, True, "bf16", 129, True),      # last-wave pieces
     (1, 16, 2300, False, "fp16", -1, False),   # 144 CTAs
     (2, 16, 1292, True, "bf16", -1, False),    # 352 units, last-wave pieces
+    # windows: 2 and 3 key tiles per differential block, 4 and 5 per standard block
+    (1, 3, 777, True, "bf16", 17, True),
+    (2, 4, 1000, True, "fp16", 64, False),
+    (1, 3, 777, True, "bf16", 65, True),
+    (1, 3, 777, False, "fp16", 100, True),
+    (1, 2, 900, False, "bf16", 128, False),
+    (1, 2, 900, False, "fp16", 129, False),
+    (1, 2, 300, False, "bf16", 0, True),
+    (1, 3, 129, True, "fp16", 1, False),       # ragged tail tile
 ])
 def test_rope_attn_matches_two_pass_bits(attn, B, H, L, diff, dtype, window, explicit):
     # the public call (K pass with the (cos, sin) table, q rotated in the attention kernel's
     # prologue, workspace-backed last-wave pieces) has the bits of the two-pass path
-    # (sa_rope_qk, then sa_attn_fwd on q') across grid sizes, with and without positions.
+    # (sa_rope_qk, then sa_attn_fwd on q') across grid sizes and windows, with and without
+    # positions.
     w = small("twopass", B=B, H=H, L=L, window=window, nmaps=2 if diff else 1, dv=128 if diff else 64,
               dtype=dtype, seed=77 + L, lam=("uniform", 0.2, 0.8) if diff else None)
     x = synth.make_inputs(w)
@@ -194,7 +204,7 @@ def test_rope_attn_matches_two_pass_bits(attn, B, H, L, diff, dtype, window, exp
     torch.cuda.synchronize()
     attn.check()
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
-    if L <= 1292 and B * H <= 3:
+    if L <= 1292 and B * H <= 8:
         if explicit:
             x["positions"] = pos.cpu().numpy()
         compare(o2.float().cpu().numpy(), oracle.rope_attn_workload(x), "rope_attn", dtype=dtype)
