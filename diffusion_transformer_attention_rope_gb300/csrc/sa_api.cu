@@ -22,6 +22,11 @@ struct sa_attn_s {
   float rope_base;
   float inv_freq[sa::kHeadDim / 2];
   int* d_err;  // 4-byte device error word
+  // (cos, sin) table of positions 0 .. cs_cap - 1 ([16][cs_cap] float4), written once at
+  // creation: calls with the default positions and L <= cs_cap read it instead of a per-call
+  // table (nullptr / 0 if it could not be allocated)
+  float2* d_cs;
+  int cs_cap;
   PFN_cuTensorMapEncodeTiled_v12000 encode;
   unsigned long long timeout_ns;
   // sa_rope_attn_host: copy-in, copy-out and per-chunk compute streams, and their events
@@ -105,7 +110,37 @@ bool create_host_streams(sa_attn_s* h) {
   return good;
 }
 
+// Positions the handle's (cos, sin) table covers (4 MiB of device memory).
+constexpr int kTableCap = 16384;
+
+// The handle's table of positions 0 .. kTableCap - 1, written once here with the RoPE pass's
+// arithmetic.  Without it (allocation failed) every call computes its own table.
+void create_table(sa_attn_s* h) {
+  h->d_cs = nullptr;
+  h->cs_cap = 0;
+  void* p = nullptr;
+  if (cudaMalloc(&p, static_cast<size_t>(kTableCap) * (sa::kHeadDim / 2) * sizeof(float2)) != cudaSuccess) {
+    cudaGetLastError();
+    return;
+  }
+  sa::RopeArgs ra;
+  std::memset(&ra, 0, sizeof(ra));
+  ra.cs = static_cast<float2*>(p);
+  ra.L = kTableCap;
+  std::memcpy(ra.inv_freq, h->inv_freq, sizeof(ra.inv_freq));
+  if (sa::rope_table_launch(ra, nullptr) != cudaSuccess || cudaStreamSynchronize(nullptr) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(p);
+    return;
+  }
+  h->d_cs = static_cast<float2*>(p);
+  h->cs_cap = kTableCap;
+}
+
+// Releases the handle's streams, events and table.
 void destroy_host_streams(sa_attn_s* h) {
+  if (h->d_cs) cudaFree(h->d_cs);
+  h->d_cs = nullptr;
   // (destroying a null stream or event handle is harmless)
   if (h->hs_in) cudaStreamDestroy(h->hs_in);
   if (h->hs_out) cudaStreamDestroy(h->hs_out);
@@ -172,9 +207,12 @@ sa_status make_qknorm(const char* fn, const float* gamma_q, const float* gamma_k
 
 // q == nullptr: rotate k only and write the (cos, sin) table cs (for the Q prologue).
 // nrm: QK-RMSNorm before the rotation, or nullptr.
+// side_blocks > 0 (q == nullptr, cs == nullptr): the k pass as at most that many blocks, on SMs
+// the attention grid leaves idle.
 sa_status launch_rope(const sa_attn_s* h, const void* q, const void* k, const int32_t* positions,
                       void* q_rot, void* k_rot, int B, int H, int L, int nmaps, sa_dtype dtype,
-                      sa_stream_t stream, void* cs = nullptr, const QkNorm* nrm = nullptr) {
+                      sa_stream_t stream, void* cs = nullptr, const QkNorm* nrm = nullptr,
+                      int side_blocks = 0) {
   DeviceGuard guard(h->device);
   if (!guard.ok) return fail(SA_ERR_CUDA, "cannot select device %d", h->device);
   sa::RopeArgs ra;
@@ -194,9 +232,10 @@ sa_status launch_rope(const sa_attn_s* h, const void* q, const void* k, const in
     ra.gamma_q[i] = nrm ? nrm->gamma_q[i] : 1.0f;
     ra.gamma_k[i] = nrm ? nrm->gamma_k[i] : 1.0f;
   }
-  cudaError_t e = sa::rope_launch(ra, dtype == SA_BF16, h->num_sms,
-                                  h->rope_blocks_per_sm[q != nullptr][nrm != nullptr],
-                                  reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e = side_blocks > 0
+      ? sa::rope_side_launch(ra, dtype == SA_BF16, side_blocks, reinterpret_cast<cudaStream_t>(stream))
+      : sa::rope_launch(ra, dtype == SA_BF16, h->num_sms, h->rope_blocks_per_sm[q != nullptr][nrm != nullptr],
+                        reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(SA_ERR_CUDA, "RoPE launch: %s", cudaGetErrorString(e));
   return ok();
 }
@@ -223,12 +262,57 @@ size_t split_bytes(int B, int H, int L, bool diff) {
          align256(static_cast<size_t>(sa::kMaxPieces) * sa::fmha_partial_floats(diff) * sizeof(float));
 }
 
+// The attention launch's grid: one CTA per unit, except that when the units leave the GPU's
+// last wave partly empty and a split region is given, the tail units (those of that last wave)
+// are cut into tail_k pieces of their key range, one CTA each, with tail_k as large as the wave
+// allows.
+struct AttnGrid {
+  long long units, ctas;
+  int n_qblocks, window, whole_ctas, tail_k;
+};
+
+AttnGrid attn_grid(const sa_attn_s* h, int B, int H, int L, int window, bool diff, bool split) {
+  AttnGrid g;
+  const int rows = sa::fmha_rows_per_cta(diff);
+  g.n_qblocks = (L + rows - 1) / rows;
+  g.window = (window < 0 || window >= L - 1) ? -1 : window;
+  g.units = static_cast<long long>(B) * H * g.n_qblocks;
+  g.whole_ctas = static_cast<int>(g.units);
+  g.tail_k = 1;
+  g.ctas = g.units;
+  const long long G = std::min<long long>(h->num_sms, sa::kMaxPieces);
+  const long long tail = g.units % G;
+  if (split && tail > 0) {
+    int min_nt = 1 << 30;
+    for (int qb = 0; qb < g.n_qblocks; ++qb) min_nt = std::min(min_nt, block_tiles_host(L, g.window, rows, qb));
+    const long long k = std::min<long long>(std::min<long long>(G / tail, min_nt), sa::kMaxTailK);
+    if (k >= 2) {
+      g.whole_ctas = static_cast<int>(g.units - tail);
+      g.tail_k = static_cast<int>(k);
+      g.ctas = (g.units - tail) + tail * k;
+    }
+  }
+  return g;
+}
+
+// SMs an attention grid of `ctas` CTAs (one per SM) leaves idle, if the k pass should run on
+// them (0: it runs on every SM, before the attention CTAs can start).  The attention CTAs then
+// start with the pass and do their setup and Q prologue meanwhile; only their K loads wait
+// for it.  Taken when the pass stays short there: at least 8 idle SMs and at most 256 KiB of
+// k for each.
+int side_sms(const sa_attn_s* h, long long ctas, long long k_bytes) {
+  const long long idle = h->num_sms - ctas;
+  if (idle < 8 || k_bytes > idle * 256 * 1024) return 0;
+  return static_cast<int>(idle);
+}
+
 // cs == nullptr: q_rot is rotated already; else q_rot is the raw q and the kernel rotates it
-// in its prologue with the (cos, sin) table cs.
+// in its prologue with the (cos, sin) table cs (row stride cs_stride, L if 0; cs_static: the
+// handle's table, which no kernel of this call writes).
 sa_status launch_attn(const sa_attn_s* h, const void* q_rot, const void* k_rot, const void* v,
                       void* out, int B, int H, int L, int window, const float* lambda,
                       sa_dtype dtype, void* split_ws, sa_stream_t stream, const void* cs = nullptr,
-                      const QkNorm* nrm = nullptr) {
+                      const QkNorm* nrm = nullptr, int cs_stride = 0, bool cs_static = false) {
   const bool diff = lambda != nullptr;
   const bool bf16 = dtype == SA_BF16;
   const int d = sa::kHeadDim;
@@ -248,41 +332,29 @@ sa_status launch_attn(const sa_attn_s* h, const void* q_rot, const void* k_rot, 
   fa.err = h->d_err;
   fa.L = L;
   fa.H = H;
-  const int rows = sa::fmha_rows_per_cta(diff);
-  fa.n_qblocks = (L + rows - 1) / rows;
-  fa.window = (window < 0 || window >= L - 1) ? -1 : window;
+  const AttnGrid g = attn_grid(h, B, H, L, window, diff, split_ws != nullptr);
+  fa.n_qblocks = g.n_qblocks;
+  fa.window = g.window;
   fa.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
   fa.timeout_ns = h->timeout_ns;
   fa.cs = static_cast<const float2*>(cs);
+  fa.cs_stride = cs_stride > 0 ? cs_stride : L;
+  fa.cs_static = cs_static;
   fa.qk_norm = nrm != nullptr;   // (with cs: the Q prologue normalises each raw q row)
   fa.eps = nrm ? nrm->eps : 0.0f;
   for (int i = 0; i < sa::kHeadDim; ++i) fa.gamma_q[i] = nrm ? nrm->gamma_q[i] : 1.0f;
   if (diff)
     for (int i = 0; i < H; ++i) fa.lambda[i] = lambda[i];
-  // One CTA per unit, except that when the units leave the GPU's last wave partly empty and a
-  // split region is given, the tail units (those of that last wave) are cut into tail_k pieces
-  // of their key range, one CTA each, with tail_k as large as the wave allows.
-  const long long units = static_cast<long long>(B) * H * fa.n_qblocks;
-  fa.whole_ctas = static_cast<int>(units);
-  fa.tail_k = 1;
-  long long ctas = units;
-  const long long G = std::min<long long>(h->num_sms, sa::kMaxPieces);
-  const long long tail = units % G;
-  if (split_ws != nullptr && tail > 0) {
-    int min_nt = 1 << 30;
-    for (int qb = 0; qb < fa.n_qblocks; ++qb) min_nt = std::min(min_nt, block_tiles_host(L, fa.window, rows, qb));
-    const long long k = std::min<long long>(std::min<long long>(G / tail, min_nt), sa::kMaxTailK);
-    if (k >= 2) {
-      fa.whole_ctas = static_cast<int>(units - tail);
-      fa.tail_k = static_cast<int>(k);
-      ctas = (units - tail) + tail * k;
-      uint8_t* ws = static_cast<uint8_t*>(split_ws);
-      fa.counters = reinterpret_cast<unsigned long long*>(ws);
-      fa.partials = reinterpret_cast<float*>(ws + align256(static_cast<size_t>(units) * 8));
-      unsigned ep = g_epoch.fetch_add(1u) + 1u;
-      if (ep == 0) ep = g_epoch.fetch_add(1u) + 1u;
-      fa.epoch = ep;
-    }
+  fa.whole_ctas = g.whole_ctas;
+  fa.tail_k = g.tail_k;
+  const long long ctas = g.ctas;
+  if (g.tail_k > 1) {
+    uint8_t* ws = static_cast<uint8_t*>(split_ws);
+    fa.counters = reinterpret_cast<unsigned long long*>(ws);
+    fa.partials = reinterpret_cast<float*>(ws + align256(static_cast<size_t>(g.units) * 8));
+    unsigned ep = g_epoch.fetch_add(1u) + 1u;
+    if (ep == 0) ep = g_epoch.fetch_add(1u) + 1u;
+    fa.epoch = ep;
   }
   fa.wave = h->num_sms;
   cudaError_t e = sa::fmha_launch(diff, bf16, tm_q, tm_k, tm_v, fa, ctas, reinterpret_cast<cudaStream_t>(stream));
@@ -387,6 +459,7 @@ sa_status sa_attn_create(sa_attn_t* handle, int device, float rope_base) {
   for (int wq = 0; wq < 2; ++wq)
     for (int nm = 0; nm < 2; ++nm) h->rope_blocks_per_sm[wq][nm] = sa::rope_blocks_per_sm(wq != 0, nm != 0);
   h->host_ready = create_host_streams(h);
+  create_table(h);
   if ((e = cudaMemset(h->d_err, 0, sizeof(int))) != cudaSuccess ||
       (e = sa::fmha_set_attributes()) != cudaSuccess) {
     cudaFree(h->d_err);
@@ -513,10 +586,12 @@ namespace {
 
 // sa_rope_attn and sa_rope_attn_qknorm: checks, then the K pass (with the table) and the
 // attention kernel (with the Q prologue), both on the caller's workspace.
+// side_ok: the call may run its k pass on the SMs its attention grid leaves idle (false when
+// other work of the same call runs beside it, as the chunks of the host-buffer call do).
 sa_status rope_attn_ws(const char* fn, sa_attn_t h, const void* q, const void* k, const void* v,
                        const int32_t* positions, void* out, int B, int H, int L, int d, int window,
                        const float* lambda, sa_dtype dtype, void* workspace, size_t workspace_bytes,
-                       sa_stream_t stream, const QkNorm* nrm) {
+                       sa_stream_t stream, const QkNorm* nrm, bool side_ok = true) {
   if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
   if (!q || !k || !v || !out)
     return fail(SA_ERR_INVALID_ARG, "%s: q, k, v and out must be non-NULL", fn);
@@ -538,6 +613,20 @@ sa_status rope_attn_ws(const char* fn, sa_attn_t h, const void* q, const void* k
   void* cs = ws;
   void* k_rot = ws + align256(sa_rope_table_bytes(L));
   void* split_ws = static_cast<uint8_t*>(k_rot) + align256(nqk * 2);
+  const int side = side_ok && positions == nullptr && h->d_cs != nullptr && L <= h->cs_cap
+                       ? side_sms(h, attn_grid(h, B, H, L, window, diff, true).ctas, static_cast<long long>(nqk) * 2)
+                       : 0;
+  if (side > 0) {
+    // A grid that leaves SMs idle, default positions: the pass runs on the idle SMs and writes
+    // no table, the prologue reads the handle's, and the attention CTAs start at once on the
+    // other SMs (only their K loads wait for the pass).  Larger grids keep the per-call table,
+    // which the pass leaves in L2 right before the prologue reads it.
+    st = launch_rope(h, nullptr, k, nullptr, nullptr, k_rot, B, H, L, diff ? 2 : 1, dtype, stream, nullptr, nrm,
+                     side);
+    if (st != SA_OK) return st;
+    return launch_attn(h, q, k_rot, v, out, B, H, L, window, lambda, dtype, split_ws, stream, h->d_cs, nrm,
+                       h->cs_cap, true);
+  }
   st = launch_rope(h, nullptr, k, positions, nullptr, k_rot, B, H, L, diff ? 2 : 1, dtype, stream, cs, nrm);
   if (st != SA_OK) return st;
   return launch_attn(h, q, k_rot, v, out, B, H, L, window, lambda, dtype, split_ws, stream, cs, nrm);
@@ -701,7 +790,8 @@ sa_status sa_rope_attn_host(sa_attn_t h, const void* q, const void* k, const voi
     if (diff)
       for (int i = 0; i < len; ++i) lam[i] = lambda[(p0 + i) % H];
     st = rope_attn_ws(fn, h, dq + oqk, dk + oqk, dv + ov, positions, dout + ov, 1, len, L, d, window,
-                      diff ? lam : nullptr, dtype, regions + slot * per_chunk, per_chunk, h->hs_comp[slot], nullptr);
+                      diff ? lam : nullptr, dtype, regions + slot * per_chunk, per_chunk, h->hs_comp[slot], nullptr,
+                      false);
     if (st != SA_OK) return st;
     e = cudaEventRecord(h->he_done[slot], h->hs_comp[slot]);
     e = e != cudaSuccess ? e : cudaStreamWaitEvent(h->hs_out, h->he_done[slot], 0);

@@ -160,17 +160,18 @@ __device__ __forceinline__ bool pwait_w(uint32_t bar, uint32_t parity, volatile 
 // the pre-pass's.  Kept out of line so that its registers do not weigh on the softmax loop's.
 // Returns the warp-uniform wait outcome.
 template <bool BF16, bool NORM>
-__device__ __noinline__ bool q_rope_prologue(const float2* cs, int L, int grow, uint32_t row, int r,
-                                             uint32_t q_full, volatile int* abort_flag, int* err,
-                                             uint64_t tmo, const float* gamma, float eps) {
-  // the table is the RoPE pass's output: wait for that grid (programmatic dependent launch)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  // the row's (cos, sin) pairs ([16][L] float4 table: a warp's loads are contiguous), loaded
-  // while the TMA brings Q
+__device__ __noinline__ bool q_rope_prologue(const float2* cs, int cs_stride, bool cs_static, int L, int grow,
+                                             uint32_t row, int r, uint32_t q_full, volatile int* abort_flag,
+                                             int* err, uint64_t tmo, const float* gamma, float eps) {
+  // a per-call table is the RoPE pass's output: wait for that grid (programmatic dependent
+  // launch); the handle's table was written long before
+  if (!cs_static) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the row's (cos, sin) pairs ([16][cs_stride] float4 table: a warp's loads are contiguous),
+  // loaded while the TMA brings Q
   float4 t[16];
   const float4* cs4 = reinterpret_cast<const float4*>(cs) + min(grow, L - 1);
 #pragma unroll
-  for (int m = 0; m < 16; ++m) t[m] = __ldg(cs4 + static_cast<size_t>(m) * L);
+  for (int m = 0; m < 16; ++m) t[m] = __ldg(cs4 + static_cast<size_t>(m) * cs_stride);
   bool ok = pwait(q_full, 0, abort_flag, err, kErrSoftmax, tmo);
   ok = __all_sync(0xffffffffu, ok);
   if (ok && grow < L) {
@@ -642,11 +643,11 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     if (a.cs != nullptr) {
       // RoPE prologue on this warpgroup's Q tile, then the tile goes to its MMA issuer.
       if (a.qk_norm)
-        ok = q_rope_prologue<BF16, true>(a.cs, L, grow, sQ + s * kTile + r * 128, r, bar.q_full, abort_flag,
-                                         a.err, tmo, a.gamma_q, a.eps);
+        ok = q_rope_prologue<BF16, true>(a.cs, a.cs_stride, a.cs_static, L, grow, sQ + s * kTile + r * 128, r,
+                                         bar.q_full, abort_flag, a.err, tmo, a.gamma_q, a.eps);
       else
-        ok = q_rope_prologue<BF16, false>(a.cs, L, grow, sQ + s * kTile + r * 128, r, bar.q_full, abort_flag,
-                                          a.err, tmo, nullptr, 0.0f);
+        ok = q_rope_prologue<BF16, false>(a.cs, a.cs_stride, a.cs_static, L, grow, sQ + s * kTile + r * 128, r,
+                                          bar.q_full, abort_flag, a.err, tmo, nullptr, 0.0f);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.q_ready(s));

@@ -81,6 +81,12 @@ struct FmhaArgs {
   int qk_norm;
   float eps;
   float gamma_q[kHeadDim];
+  // the table's row stride in float4 units per pair group (L for a per-call table, the
+  // capacity for the handle's table of positions 0 .. capacity - 1)
+  int cs_stride;
+  // cs is the handle's table, written when the handle was created: the prologue needs nothing
+  // from the RoPE pass
+  int cs_static;
 };
 
 // Rows of queries in one unit: two 128-row tiles (standard) or one tile with two maps.
@@ -97,6 +103,13 @@ constexpr int kMaxTailK = 4;
 // that rotates q as well as k (or k only), without or with the QK-RMSNorm.
 int rope_blocks_per_sm(bool with_q, bool qk_norm);
 cudaError_t rope_launch(const RopeArgs& a, bool bf16, int num_sms, int blocks_per_sm, cudaStream_t stream);
+// The k-only pass (no table) as at most `blocks` blocks of kRopeSideThreads that walk the
+// pass's items: for a call whose attention grid leaves SMs idle, the pass then occupies at
+// most `blocks` SMs and the attention CTAs start on the others at once.
+constexpr int kRopeSideThreads = 512;
+cudaError_t rope_side_launch(const RopeArgs& a, bool bf16, int blocks, cudaStream_t stream);
+// The (cos, sin) table alone (a.cs, [16][a.L] float4), with the pass's arithmetic.
+cudaError_t rope_table_launch(const RopeArgs& a, cudaStream_t stream);
 
 cudaError_t fmha_set_attributes();
 // Registers per thread ptxas assigned to each attention kernel (must equal kFmhaLaunchRegs).

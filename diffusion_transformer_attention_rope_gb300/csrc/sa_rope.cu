@@ -23,6 +23,11 @@
 // many bytes are in flight per thread.  The pass is HBM-bound: q, k read once, q', k' written
 // once.  Each block signals early that the dependent attention launch may start (its CTAs
 // then only prepare; they wait for this grid before reading q', k').
+//
+// Two more forms: the k pass as a few 512-thread blocks walking the same items (for a call
+// whose attention grid leaves SMs idle: the pass then stays on those SMs), and the (cos, sin)
+// table alone (the handle's table of positions 0 .. capacity - 1), both with the same
+// per-element arithmetic.
 #include "sa_kernels.h"
 #include "sa_ptx.cuh"
 
@@ -53,27 +58,30 @@ __device__ __forceinline__ float row_inv_rms(float t, unsigned gmask, float eps)
   return qknorm_inv_rms(u + __shfl_xor_sync(gmask, u, 2), eps);
 }
 
-// WITH_Q: rotate q as well as k (false when the attention kernel rotates q in its prologue).
-// NORM: QK-RMSNorm of every row before its rotation.
-template <bool BF16, bool WITH_Q, bool NORM>
-__device__ __forceinline__ void rope_body(const RopeArgs& a) {
-  // Let the dependent attention grid begin its prologue while this grid streams.
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  const int r = threadIdx.x >> 2;  // position within the block
-  const int g = threadIdx.x & 3;   // group of 8 pairs: pairs [8g, 8g + 8)
-  const int l = blockIdx.x * kRopeRows + r;
-  // gammas in shared memory (q then k; registers are what limits this pass's occupancy); a
-  // thread reads those of its 16 values, [8g, 8g + 8) and [32 + 8g, 32 + 8g + 8)
-  __shared__ float s_gamma[2][kHeadDim];
+// The gammas in shared memory (q then k; registers are what limits this pass's occupancy); a
+// thread reads those of its 16 values, [8g, 8g + 8) and [32 + 8g, 32 + 8g + 8).
+template <bool NORM, int THREADS>
+__device__ __forceinline__ void load_gamma(const RopeArgs& a, float (*s_gamma)[kHeadDim]) {
   if (NORM) {
-    static_assert(kRopeThreads == 2 * kHeadDim, "one gamma per thread");
-    s_gamma[threadIdx.x >> 6][threadIdx.x & 63] =
-        threadIdx.x < kHeadDim ? a.gamma_q[threadIdx.x] : a.gamma_k[threadIdx.x - kHeadDim];
+    for (int i = threadIdx.x; i < 2 * kHeadDim; i += THREADS)
+      s_gamma[i / kHeadDim][i % kHeadDim] = i < kHeadDim ? a.gamma_q[i] : a.gamma_k[i - kHeadDim];
     __syncthreads();
   }
+}
+
+// One item of the pass: positions [bx ROWS, (bx + 1) ROWS) of the planes of slice `by`
+// (planes_per_block planes), four threads per position.
+// WITH_Q: rotate q as well as k (false when the attention kernel rotates q in its prologue).
+// NORM: QK-RMSNorm of every row before its rotation.
+template <bool BF16, bool WITH_Q, bool NORM, int ROWS>
+__device__ __forceinline__ void rope_item(const RopeArgs& a, const float (*s_gamma)[kHeadDim], int bx,
+                                          long long by) {
+  const int r = threadIdx.x >> 2;  // position within the item
+  const int g = threadIdx.x & 3;   // group of 8 pairs: pairs [8g, 8g + 8)
+  const int l = bx * ROWS + r;
   if (l >= a.L) return;            // (all 4 lanes of a row leave together)
   const unsigned gmask = 0xFu << (threadIdx.x & 28);
-  const long long first = static_cast<long long>(blockIdx.y) * a.planes_per_block;
+  const long long first = by * a.planes_per_block;
   long long last = first + a.planes_per_block;
   if (last > a.planes) last = a.planes;
   const size_t row_stride = static_cast<size_t>(a.L) * kHeadDim;
@@ -105,7 +113,7 @@ __device__ __forceinline__ void rope_body(const RopeArgs& a) {
         sincosf(theta, &s[i], &c[i]);
       }
       have_cs = true;
-      if (a.cs != nullptr && blockIdx.y == 0) {
+      if (a.cs != nullptr && by == 0) {
         // this position's pairs [8g, 8g + 8) of the (cos, sin) table for the Q prologue; the
         // table is [16][L] float4 (pairs 2m and 2m + 1 of position l at [m][l]), so that the
         // prologue's loads of consecutive rows are contiguous
@@ -155,6 +163,15 @@ __device__ __forceinline__ void rope_body(const RopeArgs& a) {
   }
 }
 
+template <bool BF16, bool WITH_Q, bool NORM>
+__device__ __forceinline__ void rope_body(const RopeArgs& a) {
+  // Let the dependent attention grid begin its prologue while this grid streams.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ float s_gamma[2][kHeadDim];
+  load_gamma<NORM, kRopeThreads>(a, s_gamma);
+  rope_item<BF16, WITH_Q, NORM, kRopeRows>(a, s_gamma, blockIdx.x, blockIdx.y);
+}
+
 template <bool BF16, bool WITH_Q>
 __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constant__ RopeArgs a) {
   rope_body<BF16, WITH_Q, false>(a);
@@ -163,6 +180,37 @@ __global__ void __launch_bounds__(kRopeThreads) rope_kernel(const __grid_constan
 template <bool BF16, bool WITH_Q>
 __global__ void __launch_bounds__(kRopeThreads) rope_norm_kernel(const __grid_constant__ RopeArgs a) {
   rope_body<BF16, WITH_Q, true>(a);
+}
+
+// The k-only pass walking its items with a grid of at most the SMs the attention grid leaves
+// idle (items: kSideRows positions of planes_per_block planes).
+constexpr int kSideRows = kRopeSideThreads / 4;
+
+template <bool BF16, bool NORM>
+__global__ void __launch_bounds__(kRopeSideThreads) rope_side_kernel(const __grid_constant__ RopeArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  __shared__ float s_gamma[2][kHeadDim];
+  load_gamma<NORM, kRopeSideThreads>(a, s_gamma);
+  const int nx = (a.L + kSideRows - 1) / kSideRows;
+  const long long items = static_cast<long long>(nx) * ((a.planes + a.planes_per_block - 1) / a.planes_per_block);
+  for (long long item = blockIdx.x; item < items; item += gridDim.x)
+    rope_item<BF16, false, NORM, kSideRows>(a, s_gamma, static_cast<int>(item % nx), item / nx);
+}
+
+// The (cos, sin) table alone, for positions 0 .. L - 1 (or a.positions): four threads per
+// position, 8 pairs each, with the arithmetic of the pass above (so the table has its bits).
+__global__ void __launch_bounds__(kRopeThreads) rope_table_kernel(const __grid_constant__ RopeArgs a) {
+  const int r = threadIdx.x >> 2, g = threadIdx.x & 3;
+  const int l = blockIdx.x * kRopeRows + r;
+  if (l >= a.L) return;
+  const float pf = static_cast<float>(a.positions ? a.positions[l] : l);
+  float c[8], s[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) sincosf(__fmul_rn(pf, a.inv_freq[8 * g + i]), &s[i], &c[i]);
+  float4* t = reinterpret_cast<float4*>(a.cs);
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    t[static_cast<size_t>(4 * g + i) * a.L + l] = make_float4(c[2 * i], s[2 * i], c[2 * i + 1], s[2 * i + 1]);
 }
 
 // Resident blocks per SM of one variant (the fewer of its fp16 and bf16 forms).
@@ -221,6 +269,31 @@ cudaError_t rope_launch(const RopeArgs& a_in, bool bf16, int num_sms, int blocks
     if (with_q) launch_variant<false, true>(a, grid, stream);
     else launch_variant<false, false>(a, grid, stream);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t rope_side_launch(const RopeArgs& a_in, bool bf16, int blocks, cudaStream_t stream) {
+  RopeArgs a = a_in;
+  a.q = nullptr;
+  a.q_out = nullptr;
+  a.cs = nullptr;
+  a.planes_per_block = static_cast<int>(a.planes < kPlaneBatch ? a.planes : kPlaneBatch);
+  const int nx = (a.L + kSideRows - 1) / kSideRows;
+  const long long items = static_cast<long long>(nx) * ((a.planes + a.planes_per_block - 1) / a.planes_per_block);
+  const unsigned grid = static_cast<unsigned>(items < blocks ? items : blocks);
+  if (bf16) {
+    if (a.qk_norm) rope_side_kernel<true, true><<<grid, kRopeSideThreads, 0, stream>>>(a);
+    else rope_side_kernel<true, false><<<grid, kRopeSideThreads, 0, stream>>>(a);
+  } else {
+    if (a.qk_norm) rope_side_kernel<false, true><<<grid, kRopeSideThreads, 0, stream>>>(a);
+    else rope_side_kernel<false, false><<<grid, kRopeSideThreads, 0, stream>>>(a);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t rope_table_launch(const RopeArgs& a, cudaStream_t stream) {
+  const unsigned grid = static_cast<unsigned>((a.L + kRopeRows - 1) / kRopeRows);
+  rope_table_kernel<<<grid, kRopeThreads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 

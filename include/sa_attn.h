@@ -76,9 +76,13 @@ typedef enum {
 /*
  * Create a handle on CUDA device `device`.  rope_base is the RoPE base
  * (10000 for Stable Audio 3); the FP32 frequency table rope_base^(-2i/64) is
- * computed here in double and rounded once.  Fails with SA_ERR_NO_DEVICE when
- * there is no such device and SA_ERR_UNSUPPORTED when it is not an sm_103
- * (GB300) part.  Restores the caller's current device before returning.
+ * computed here in double and rounded once.  The handle also holds the FP32
+ * (cos, sin) table of positions 0..16383 (4 MiB of device memory, written here
+ * once with the RoPE pass's arithmetic; skipped if it cannot be allocated),
+ * which sa_rope_attn reads for small grids (below).  Fails with
+ * SA_ERR_NO_DEVICE when there is no such device and SA_ERR_UNSUPPORTED when it
+ * is not an sm_103 (GB300) part.  Restores the caller's current device before
+ * returning.
  */
 SA_API sa_status sa_attn_create(sa_attn_t* handle, int device, float rope_base);
 
@@ -112,7 +116,13 @@ SA_API size_t sa_rope_attn_workspace_size(int B, int H, int L, int d, int differ
 SA_API size_t sa_attn_fwd_workspace_size(int B, int H, int L, int d, int differential);
 
 /*
- * Enqueue RoPE + attention on `stream`.
+ * Enqueue RoPE + attention on `stream`: a pass rotates k into the workspace,
+ * and the attention kernel rotates q as each Q tile arrives.  Usually the pass
+ * also writes the (cos, sin) table the kernel reads.  When the attention grid
+ * leaves SMs idle (fewer query blocks than SMs) and positions is NULL, the pass
+ * runs on those SMs only and the kernel reads the handle's table, so its CTAs
+ * start at once.  Either form gives the bits of sa_rope_qk followed by
+ * sa_attn_fwd.
  *
  *   q, k      device, dtype.  Standard (lambda == NULL): [B, H, L, d].
  *             Differential (lambda != NULL): [B, H, 2, L, d]; map 0 is
