@@ -58,7 +58,9 @@ def test_single_process_env_defaults(monkeypatch):
     assert bench.reduce_max(None, 3.5) == 3.5
 
 
-def test_flop_accounting_matches_survey_figures():
+def test_flop_accounting_matches_closed_forms():
+    # 4 B H L^2 d for standard attention, 2 maps x 2 (d + d_v) per pair for the differential
+    # form, and the window's allowed pairs sum_i (min(L - 1, i + w) - max(0, i - w) + 1)
     import bench
     import synth
 
