@@ -143,3 +143,34 @@ def test_set_timeout_null_handle_is_rejected():
     with pytest.raises(sa.SaAttnError) as e:
         sa.sa_attn_set_timeout(0, 1000)
     assert e.value.status == 1
+
+
+def _host_chunks(B, H, L, diff):
+    # the host-buffer call's chunks: about one per 16 MiB of copies (two from 8 MiB up), at
+    # most 4, more when a chunk would exceed 128 planes; returns (chunks, planes of the largest)
+    P = B * H
+    total = P * 2.0 * L * 64 * (2 if diff else 1) * 4
+    mib16 = 16 * 1024 * 1024
+    by_size = int(total / mib16) if total >= mib16 else (2 if total >= mib16 / 2 else 1)
+    n = max(min(min(4, by_size), P), -(-P // 128))
+    return n, -(-P // n)
+
+
+@pytest.mark.parametrize("B,H,L,diff,chunks", [
+    (2, 3, 300, False, 1),      # 3.7 MB of copies: one chunk
+    (1, 16, 1292, False, 2),    # 10.6 MB: two chunks of 8 planes
+    (1, 24, 4096, False, 3),    # 50 MB: three chunks
+    (1, 16, 4096, True, 4),     # 67 MB: at most four
+    (5, 128, 64, True, 5),      # 640 planes: chunks of at most 128 planes
+])
+def test_host_workspace_follows_the_chunk_rule(B, H, L, diff, chunks):
+    # device copies of q, k (both maps), v and out, then one sa_rope_attn workspace (for the
+    # largest chunk) per compute stream in use
+    n, max_len = _host_chunks(B, H, L, diff)
+    assert n == chunks
+    nqk = B * H * (2 if diff else 1) * L * 64
+    nv = B * H * L * (128 if diff else 64)
+    per = sa.sa_rope_attn_workspace_size(1, max_len, L, 64, diff)
+    assert sa.sa_rope_attn_host_workspace_size(B, H, L, 64, diff) == \
+        2 * _a256(nqk * 2) + 2 * _a256(nv * 2) + min(n, 4) * per
+    assert sa.sa_rope_attn_host_workspace_size(0, H, L, 64, diff) == 0
