@@ -259,11 +259,12 @@ __device__ __forceinline__ bool softmax_tile(const Barriers& bar, int it, uint32
   ok = __all_sync(0xffffffffu, ok);
   if (!ok) return false;
   tc_fence_after();
+  // S row and its maximum in one load: the tensor memory's reducing load (sm_103a) returns the
+  // max of the 128 values with them, so an unmasked tile spends no instruction on its row max.
   uint32_t sr[kBlockN];
-#pragma unroll
-  for (int cc = 0; cc < kBlockN / 32; ++cc)
-    tmem_ld32_nowait(tmem + C::s_col(s) + lane_off + 32 * cc, sr + 32 * cc);
-  tmem_wait_ld_128(sr);
+  float mt;
+  tmem_ld128_max_nowait(tmem + C::s_col(s) + lane_off, sr, mt);
+  tmem_wait_ld_128_max(sr, mt);
   {
     // S_s is in registers: the issuer may write the next S_s into these columns now.
     // Every lane has waited for its own load; after the warp sync one lane arrives.
@@ -274,22 +275,23 @@ __device__ __forceinline__ bool softmax_tile(const Barriers& bar, int it, uint32
 
   if (TMASK == kMaskTail || (TMASK == kMaskWindow && need_mask)) {
     // this row's valid keys are columns [j_lo, j_hi) of the tile (one compare per column
-    // against bounds computed once keeps the masking code short)
+    // against bounds computed once keeps the masking code short); the loaded maximum also
+    // covers the masked columns, so the row max is taken again over the masked row.
 #pragma unroll
     for (int j = 0; j < kBlockN; ++j)
       if (j >= j_hi || (TMASK == kMaskWindow && j < j_lo)) sr[j] = __float_as_uint(-INFINITY);
+    // 8 independent chains; chain q covers elements q, q + 8, ..., q + 120.
+    float mx[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) mx[q] = fmaxf(__uint_as_float(sr[q]), __uint_as_float(sr[q + 8]));
+#pragma unroll
+    for (int j = 16; j < kBlockN; j += 16) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q)
+        mx[q] = fmax3(mx[q], __uint_as_float(sr[j + q]), __uint_as_float(sr[j + 8 + q]));
+    }
+    mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
   }
-  // 8 independent chains; chain q covers elements q, q + 8, ..., q + 120.
-  float mx[8];
-#pragma unroll
-  for (int q = 0; q < 8; ++q) mx[q] = fmaxf(__uint_as_float(sr[q]), __uint_as_float(sr[q + 8]));
-#pragma unroll
-  for (int j = 16; j < kBlockN; j += 16) {
-#pragma unroll
-    for (int q = 0; q < 8; ++q)
-      mx[q] = fmax3(mx[q], __uint_as_float(sr[j + q]), __uint_as_float(sr[j + 8 + q]));
-  }
-  const float mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
 
   // Lazy rescale: keep the old running max unless this tile raises it by more than tau
   // (P then stays <= 2^8).  The decision is warp-uniform because tcgen05.ld/st are.
