@@ -22,8 +22,9 @@
 //                      (only when the running max grows by more than 2^8), fp16/bf16 P
 //                      written to TMEM (standard) or to shared memory (differential)
 //   O_s += P_s V       tcgen05.mma, A = P from TMEM or smem, B = V (MN-major) from smem
-// The two warpgroups take turns on the exponential phase; each stream's S buffer is released
-// as soon as the softmax warps hold S in registers, so the next S MMA overlaps the softmax.
+// In the differential kernel the two warpgroups take turns on the exponential phase.  Each
+// stream's S buffer is released as soon as the softmax warps hold S in registers, so the next
+// S MMA overlaps the softmax.
 // TMEM (512 columns): standard S0|S1|P0|P1|O0|O1 = 128|128|64|64|64|64;
 // differential S0|S1|O0|O1 = 128|128|128|128.
 // The sliding window visits only the key tiles of [q0 - w, q_last + w], tiled from its first
@@ -307,9 +308,12 @@ __device__ __forceinline__ bool softmax_tile(const Barriers& bar, int it, uint32
   }
   const float mb = (m_use == -INFINITY) ? 0.0f : m_use * c;
   const float2 c2 = make_float2(c, c), nmb2 = make_float2(-mb, -mb);
-  ok = pwait(bar.turn(s, quarter), it & 1, abort_flag, err, kErrSoftmax, tmo);
-  ok = __all_sync(0xffffffffu, ok);
-  if (!ok) return false;
+  if (DIFF) {
+    // the differential kernel's warps take turns on the exp unit (see the kernel's softmax part)
+    ok = pwait(bar.turn(s, quarter), it & 1, abort_flag, err, kErrSoftmax, tmo);
+    ok = __all_sync(0xffffffffu, ok);
+    if (!ok) return false;
+  }
   // Exponentials of the whole row into registers (packed pairs): P_s(it) is computed
   // before the wait for P_s V(it - 1), which has the whole exponential phase to finish.
   float2 sum0 = make_float2(0.0f, 0.0f), sum1 = make_float2(0.0f, 0.0f);
@@ -326,8 +330,10 @@ __device__ __forceinline__ bool softmax_tile(const Barriers& bar, int it, uint32
     pk[j] = pack2<BF16>(p0.x, p0.y);
     pk[j + 1] = pack2<BF16>(p1.x, p1.y);
   }
-  __syncwarp();
-  if (lane == 0) mbar_arrive(bar.turn(1 - s, quarter));
+  if (DIFF) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar.turn(1 - s, quarter));
+  }
   const float2 sum = fadd2(sum0, sum1);
   l_sum = fmaf(l_sum, f, sum.x + sum.y);
   if (it > 0) {
@@ -635,12 +641,13 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     float m_use = -INFINITY;
     float l_sum = 0.0f;
     bool ok = true;
-    // The two warpgroups take turns on the exponential phase (the exp unit is the scarce
-    // resource), pairwise per SM sub-partition (warp q of group 0 with warp q of group 1,
-    // which share one): group 0 goes first, each warp hands the turn to its partner when its
-    // exponentials are issued, so one warp's max / TMEM / barrier work overlaps the other's
-    // exponentials without waiting for the slowest warp of the other group.
-    if (s == 1 && lane == 0) mbar_arrive(bar.turn(0, quarter));
+    // Differential kernel: the two warpgroups take turns on the exponential phase, pairwise
+    // per SM sub-partition (warp q of group 0 with warp q of group 1, which share one): group 0
+    // goes first, each warp hands the turn to its partner when its exponentials are issued, so
+    // one warp's TMEM / barrier / shared-memory work overlaps the other's exponentials.  The
+    // standard kernel (d_v = 64, P in tensor memory, row max from the reducing load) runs
+    // without turns: there the hand-over cost more than it saved (measured 8% at L = 4096).
+    if (DIFF && s == 1 && lane == 0) mbar_arrive(bar.turn(0, quarter));
 
     if (a.cs != nullptr) {
       // RoPE prologue on this warpgroup's Q tile, then the tile goes to its MMA issuer.
