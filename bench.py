@@ -7,6 +7,11 @@ the RoPE stage (q, k rotated in FP32, cast back) and the attention stage
 (QK^T/sqrt(d), FP32 softmax, P.V; differential / windowed per workload).
 Default workload: the DiT standard attention at L=1292 (B=1, H=16, d=64, fp16).
 
+The default run also measures the L=4096 DiT workload (the configuration the
+60%-of-peak target is quoted on), differential attention and the two sliding
+windows, each with the same fields, under the line's ``workloads`` map
+(``--headline-only`` skips them).
+
 Prints ONE JSON line (rank 0).  ``value`` is attention TFLOP/s of the whole job
 (algorithmic FLOPs, inputs resident in HBM, L2 flushed between steps, CUDA
 events on the launching stream, max over ranks).  ``e2e`` is the same metric
@@ -41,6 +46,7 @@ import synth  # noqa: E402
 
 METRIC = "attention TFLOP/s and % of GB300 FP16/BF16 tensor peak at L=1292/4096"
 DEFAULT_WORKLOAD = "dit_l1292"
+DEFAULT_WORKLOADS_HEADLINE = DEFAULT_WORKLOAD
 L2_FLUSH_BYTES = 256 << 20
 
 
@@ -296,16 +302,41 @@ def workload_of(args):
     return w
 
 
+# Workloads measured beside the headline one in the default run (each in the line's `workloads`
+# map): the long-sequence DiT configuration that the 60% target is quoted on, differential
+# attention, and the two sliding windows.
+EXTRA_WORKLOADS = ["dit_l4096_outliers", "diff_l4096", "swa_diff_l8192", "swa17_diff_l8192"]
+
+
 def run_ours(args):
     import torch
-
-    import diffusion_transformer_attention_rope_gb300 as sa
 
     world, rank, local = dist_env()
     dist = dist_init(world, "nccl")
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
     w = workload_of(args)
+    res = measure(args, w, dist, world, rank, local, device, cpu_budget=args.cpu_budget)
+    if args.all_workloads and args.workload == DEFAULT_WORKLOADS_HEADLINE and args.batch is None:
+        extra = {}
+        for name in EXTRA_WORKLOADS:
+            r = measure(args, synth.WORKLOADS[name], dist, world, rank, local, device,
+                        cpu_budget=args.extra_cpu_budget)
+            if r is not None:
+                extra[name] = {k: r[k] for k in ("value", "unit", "ms_per_step", "step_ms", "frac_of_peak", "dtype",
+                                                 "config", "roofline", "stages_ms", "graph", "cpu_baseline", "e2e",
+                                                 "gpu_launches", "clocks")}
+        if res is not None:
+            res["workloads"] = extra
+    return res
+
+
+def measure(args, w, dist, world, rank, local, device, cpu_budget):
+    """One workload: the timed regions below; the JSON fields of rank 0 (None elsewhere)."""
+    import torch
+
+    import diffusion_transformer_attention_rope_gb300 as sa
+
     x = synth.make_inputs(w, seed=w.seed + rank)
     tdt = torch.float16 if w.dtype == "fp16" else torch.bfloat16
     dtype = sa.SA_FP16 if w.dtype == "fp16" else sa.SA_BF16
@@ -480,7 +511,7 @@ def run_ours(args):
     achieved = fl / attn_avg_s / 1e12
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        tfl, dt, n, th = oracle_sample(w, x, args.cpu_budget, np.random.default_rng(0), qk_norm=nrm)
+        tfl, dt, n, th = oracle_sample(w, x, cpu_budget, np.random.default_rng(0), qk_norm=nrm)
         cpu = {"value": tfl, "unit": "TFLOP/s", "cores": th, "kind": "oracle",
                "sample": f"{n} of {w.B * w.H * w.L} query rows (random, all heads), {dt:.1f} s, FP64 C oracle"}
     return {
@@ -508,7 +539,11 @@ def run_ours(args):
                      "kernel": "attention (sa_attn_fwd_rope_q)" if nrm is None else
                                "attention (sa_attn_fwd on sa_qknorm_rope_qk output)", "kernel_sha": kernel_sha(),
                      "peak_source": peaks["source"] + " bf16 burst",
-                     "avg_ms": attn_avg_s * 1e3},
+                     "avg_ms": attn_avg_s * 1e3,
+                     # the same launch against the HBM roof: algorithmic bytes (q', k', v read once,
+                     # out written once) over its duration, of the measured copy bandwidth
+                     "hbm": {"achieved": io_bytes(w) / attn_avg_s / 1e9, "peak": peaks["hbm_gbs"],
+                             "unit": "GB/s", "frac": io_bytes(w) / attn_avg_s / 1e9 / peaks["hbm_gbs"]}},
         "stages_ms": {"rope": statistics.mean(rope_ms), "attention": statistics.mean(attn_ms)},
         "graph": None if graph_ms is None else {"ms_per_step": graph_ms,
                                                 "value": job_throughput(world, fl, 1, graph_ms)},
@@ -575,6 +610,10 @@ def main():
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch size B")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--extra-cpu-budget", type=float, default=3.0,
+                    help="seconds of oracle work for each extra workload's cpu_baseline")
+    ap.add_argument("--headline-only", dest="all_workloads", action="store_false",
+                    help="measure the selected workload only (no `workloads` map)")
     ap.add_argument("--qk-norm", action="store_true",
                     help="QK-RMSNorm (FP32, seeded gammas, eps 1e-6) before RoPE: sa_rope_attn_qknorm")
     args = ap.parse_args()

@@ -33,6 +33,9 @@ struct sa_attn_s {
   cudaStream_t hs_in, hs_out, hs_comp[sa::kHostChunks];
   cudaEvent_t he_entry, he_in[sa::kHostChunks], he_done[sa::kHostChunks], he_exit;
   bool host_ready;
+  // sa_rope_attn_noalloc: device address of the library's static scratch array in this
+  // handle's context, looked up on the handle's first call of that function (nullptr before)
+  void* noalloc_scratch;
 };
 
 namespace {
@@ -371,6 +374,15 @@ sa_status set_error(sa_status st, const char* msg) { return fail(st, "%s", msg);
 
 int handle_device(sa_attn_t h) { return h->device; }
 
+void** handle_noalloc_slot(sa_attn_t h) { return &h->noalloc_scratch; }
+
+sa_status check_call(const char* fn, int B, int H, int L, int d, const float* lambda, sa_dtype dtype) {
+  const bool diff = lambda != nullptr;
+  sa_status st = check_shape(fn, B, H, L, d, dtype, diff);
+  if (st != SA_OK) return st;
+  return check_lambda(fn, lambda, H);
+}
+
 // The checks and the two launches of sa_rope_attn, with q', k' placed at caller-given
 // device addresses instead of a workspace argument.
 sa_status rope_attn_into(const char* fn, sa_attn_t h, const void* q, const void* k, const void* v,
@@ -380,9 +392,10 @@ sa_status rope_attn_into(const char* fn, sa_attn_t h, const void* q, const void*
   if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
   if (!q || !k || !v || !out)
     return fail(SA_ERR_INVALID_ARG, "%s: q, k, v and out must be non-NULL", fn);
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(q_rot) ||
-      !aligned16(k_rot))
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return fail(SA_ERR_INVALID_ARG, "%s: q, k, v and out must be 16-byte aligned", fn);
+  if (!aligned16(q_rot) || !aligned16(k_rot))
+    return fail(SA_ERR_INVALID_ARG, "%s: the q' / k' scratch must be 16-byte aligned", fn);
   const bool diff = lambda != nullptr;
   sa_status st = check_shape(fn, B, H, L, d, dtype, diff);
   if (st != SA_OK) return st;
@@ -475,7 +488,7 @@ sa_status sa_attn_create(sa_attn_t* handle, int device, float rope_base) {
     destroy_host_streams(h);
     delete h;
     return fail(SA_ERR_UNSUPPORTED, "sa_attn_create: attention kernel built with %d registers per "
-                "thread, expected %d", regs, sa::kFmhaLaunchRegs);
+                "thread (expected %d) or for an architecture other than sm_103a", regs, sa::kFmhaLaunchRegs);
   }
   *handle = h;
   return ok();

@@ -914,6 +914,8 @@ bool fmha_check_registers(int* got) {
     if (cudaFuncGetAttributes(&attr, f) != cudaSuccess) return false;
     *got = attr.numRegs;
     if (attr.numRegs != kFmhaLaunchRegs) return false;
+    // the library holds sm_103a code only
+    if (attr.binaryVersion != 103) return false;
   }
   return true;
 }

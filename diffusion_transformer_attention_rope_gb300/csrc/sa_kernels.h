@@ -112,7 +112,8 @@ cudaError_t rope_side_launch(const RopeArgs& a, bool bf16, int blocks, cudaStrea
 cudaError_t rope_table_launch(const RopeArgs& a, cudaStream_t stream);
 
 cudaError_t fmha_set_attributes();
-// Registers per thread ptxas assigned to each attention kernel (must equal kFmhaLaunchRegs).
+// Registers per thread ptxas assigned to each attention kernel (must equal kFmhaLaunchRegs);
+// false also when a kernel's binary is not sm_103a code.
 bool fmha_check_registers(int* got);
 cudaError_t fmha_launch(bool diff, bool bf16, const CUtensorMap& tm_q, const CUtensorMap& tm_k,
                         const CUtensorMap& tm_v, const FmhaArgs& a, long long num_ctas,
@@ -121,6 +122,10 @@ cudaError_t fmha_launch(bool diff, bool bf16, const CUtensorMap& tm_q, const CUt
 // Library-internal hooks defined in sa_api.cu (not part of the exported C ABI).
 sa_status set_error(sa_status st, const char* msg);
 int handle_device(sa_attn_t h);
+// The handle's slot for the noalloc scratch address (nullptr until its first noalloc call).
+void** handle_noalloc_slot(sa_attn_t h);
+// The shape, dtype and lambda checks of sa_rope_attn, in its order.
+sa_status check_call(const char* fn, int B, int H, int L, int d, const float* lambda, sa_dtype dtype);
 sa_status rope_attn_into(const char* fn, sa_attn_t h, const void* q, const void* k, const void* v,
                          const int32_t* positions, void* out, int B, int H, int L, int d,
                          int window, const float* lambda, sa_dtype dtype, void* q_rot, void* k_rot,

@@ -9,10 +9,12 @@
 // that array until the process exits.
 //
 // The array's name is only a host-side stand-in in host code, so its device address is looked up
-// with cudaGetSymbolAddress, with the device current, once per device, on the first call made on
-// that device (that first call should therefore come before any stream capture).  All calls share
-// the one array: calls that can overlap on the GPU (different streams, no ordering) race on it.
-// Nothing in it has to start at zero: the RoPE stage overwrites every byte a call then reads.
+// with cudaGetSymbolAddress, with the handle's device current, on the handle's first call of this
+// entry point, and kept in the handle (that first call should therefore come before any stream
+// capture).  A handle created after the context was torn down and made again looks the address up
+// afresh.  All calls share the one array: calls that can overlap on the GPU (different streams, no
+// ordering) race on it.  Nothing in it has to start at zero: the RoPE stage overwrites every byte
+// a call then reads.
 #include <cuda_runtime.h>
 
 #include <cstdio>
@@ -24,24 +26,25 @@
 namespace {
 
 constexpr size_t kScratchBytes = SA_NOALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// Device address of g_scratch on `device`, looked up once with that device current.
-sa_status scratch_address(int device, void** addr) {
-  if (device < 0 || device >= kMaxDevices)
-    return sa::set_error(SA_ERR_UNSUPPORTED, "sa_rope_attn_noalloc: device index out of range");
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Device address of g_scratch in the context of the handle's device, looked up on the handle's
+// first call (with that device current) and kept in the handle.
+sa_status scratch_address(sa_attn_t h, void** addr) {
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[device]) {
-    *addr = g_scratch_addr[device];
+  void** slot = sa::handle_noalloc_slot(h);
+  if (*slot) {
+    *addr = *slot;
     return SA_OK;
   }
+  const int device = sa::handle_device(h);
   int prev = -1;
   if (cudaGetDevice(&prev) != cudaSuccess)
     return sa::set_error(SA_ERR_CUDA, "sa_rope_attn_noalloc: cudaGetDevice failed");
@@ -56,7 +59,7 @@ sa_status scratch_address(int device, void** addr) {
              cudaGetErrorString(e));
     return sa::set_error(SA_ERR_CUDA, msg);
   }
-  g_scratch_addr[device] = p;
+  *slot = p;
   *addr = p;
   return SA_OK;
 }
@@ -67,12 +70,19 @@ extern "C" sa_status sa_rope_attn_noalloc(sa_attn_t h, const void* q, const void
                                           const int32_t* positions, void* out, int B, int H, int L,
                                           int d, int window, const float* lambda, sa_dtype dtype,
                                           sa_stream_t stream) {
+  const char* fn = "sa_rope_attn_noalloc";
   if (!h) return sa::set_error(SA_ERR_INVALID_ARG, "sa_rope_attn_noalloc: handle is NULL");
-  const bool diff = lambda != nullptr;
-  if (sa_rope_attn_workspace_size(B, H, L, d, diff ? 1 : 0) == 0)
-    return sa::set_error(SA_ERR_INVALID_ARG, "sa_rope_attn_noalloc: invalid sizes (B, H, L >= 1, d = 64)");
+  // sa_rope_attn's checks in its order (pointers, alignment, shape and dtype, lambda), then the
+  // scratch size
+  if (!q || !k || !v || !out)
+    return sa::set_error(SA_ERR_INVALID_ARG, "sa_rope_attn_noalloc: q, k, v and out must be non-NULL");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return sa::set_error(SA_ERR_INVALID_ARG, "sa_rope_attn_noalloc: q, k, v and out must be 16-byte aligned");
+  sa_status st = sa::check_call(fn, B, H, L, d, lambda, dtype);
+  if (st != SA_OK) return st;
   // The scratch holds q' and k' only: this entry point runs the attention stage without the
   // split region (one CTA per query block).
+  const bool diff = lambda != nullptr;
   const size_t nqk = static_cast<size_t>(B) * H * (diff ? 2 : 1) * L * d;
   const size_t need = 2 * round256(nqk * 2);
   if (need > kScratchBytes) {
@@ -84,9 +94,9 @@ extern "C" sa_status sa_rope_attn_noalloc(sa_attn_t h, const void* q, const void
     return sa::set_error(SA_ERR_WORKSPACE, msg);
   }
   void* base = nullptr;
-  const sa_status st = scratch_address(sa::handle_device(h), &base);
+  st = scratch_address(h, &base);
   if (st != SA_OK) return st;
   unsigned char* ws = static_cast<unsigned char*>(base);
-  return sa::rope_attn_into("sa_rope_attn_noalloc", h, q, k, v, positions, out, B, H, L, d, window,
-                            lambda, dtype, ws, ws + round256(nqk * 2), stream);
+  return sa::rope_attn_into(fn, h, q, k, v, positions, out, B, H, L, d, window, lambda, dtype, ws,
+                            ws + round256(nqk * 2), stream);
 }

@@ -328,15 +328,20 @@ SA_API sa_status sa_attn_fwd(sa_attn_t handle,
  *
  * It takes no workspace and allocates nothing: the rotated q', k' go to one
  * static device array of SA_NOALLOC_SCRATCH_BYTES inside the library, which
- * every GPU that loads the library keeps until the process exits.  The first
- * call on a device looks up that array's device address (with the device
- * current), so make that first call before any stream capture.  All calls
- * share the array: calls that may overlap on the GPU race on it, so order them
- * (one stream).  Nothing in it needs clearing between calls.
+ * every GPU that loads the library keeps until the process exits.  A handle's
+ * first call of this function looks up that array's device address (with the
+ * handle's device current) and keeps it in the handle, so make that first call
+ * before any stream capture.  All calls share the array: calls that may
+ * overlap on the GPU race on it, so order them (one stream).  Nothing in it
+ * needs clearing between calls.  The attention stage runs without the split
+ * region of sa_rope_attn (one CTA per query block).
  *
- * Arguments, layouts and errors are those of sa_rope_attn, except that a shape
- * whose scratch (sa_rope_attn_workspace_size) exceeds SA_NOALLOC_SCRATCH_BYTES
- * is rejected with SA_ERR_WORKSPACE before anything is enqueued.
+ * Arguments, layouts and errors are those of sa_rope_attn, checked in the same
+ * order.  Then a shape is accepted only if q' and k' fit the array:
+ *   2 * round_up_256(B * H * maps * L * 64 * 2) <= SA_NOALLOC_SCRATCH_BYTES
+ * (maps = 2 for differential attention, else 1), that is at most 262,144
+ * rows of 64 values (B * H * maps * L); a larger shape is rejected with
+ * SA_ERR_WORKSPACE before anything is enqueued.
  */
 SA_API sa_status sa_rope_attn_noalloc(sa_attn_t handle,
                                       const void* q, const void* k, const void* v,
