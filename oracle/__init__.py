@@ -42,7 +42,7 @@ _LIB = os.path.join(_HERE, "libsa_oracle.so")
 _lock = threading.Lock()
 _lib = None
 
-DTYPES = {"fp16": 0, "bf16": 1}
+DTYPES = {"fp16": 0, "bf16": 1, "fp32": 2}
 CASTS = {"method": 0, "exact": 1}
 
 
@@ -74,14 +74,16 @@ def _load():
             lib.sa_oracle_fp16_to_double.restype = ctypes.c_double
             lib.sa_oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
             lib.sa_oracle_bf16_to_double.restype = ctypes.c_double
+            lib.sa_oracle_fp32_to_double.argtypes = [ctypes.c_uint32]
+            lib.sa_oracle_fp32_to_double.restype = ctypes.c_double
             lib.sa_oracle_rope_attn.argtypes = [
-                P(ctypes.c_uint16), P(ctypes.c_uint16), P(ctypes.c_uint16), P(ctypes.c_int32),
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, P(ctypes.c_int32),
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, P(ctypes.c_double), ctypes.c_int, ctypes.c_int, ctypes.c_double,
                 P(ctypes.c_int64), ctypes.c_int64, P(ctypes.c_double), ctypes.c_int]
             lib.sa_oracle_rope_attn.restype = ctypes.c_int
             lib.sa_oracle_rope_attn_qknorm.argtypes = [
-                P(ctypes.c_uint16), P(ctypes.c_uint16), P(ctypes.c_uint16), P(ctypes.c_int32),
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, P(ctypes.c_int32),
                 ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                 ctypes.c_int, P(ctypes.c_double), ctypes.c_int, ctypes.c_int, ctypes.c_double,
                 ctypes.c_int, P(ctypes.c_double), P(ctypes.c_double), ctypes.c_double,
@@ -139,7 +141,7 @@ def rmsnorm(x: np.ndarray, gamma: Optional[np.ndarray] = None, eps: float = 1e-6
 
 
 def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
-    """Round doubles to the nearest fp16/bf16 value (ties to even), returned as double."""
+    """Round doubles to the nearest fp16/bf16/FP32 value (ties to even), returned as double."""
     lib = _load()
     x = np.ascontiguousarray(x, dtype=np.float64)
     y = np.empty_like(x)
@@ -149,6 +151,9 @@ def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
 
 def bits_to_double(bits: np.ndarray, dtype: str) -> np.ndarray:
     lib = _load()
+    if dtype == "fp32":
+        b = np.ascontiguousarray(bits, dtype=np.uint32).reshape(-1)
+        return np.array([lib.sa_oracle_fp32_to_double(int(x)) for x in b], dtype=np.float64).reshape(np.shape(bits))
     f = lib.sa_oracle_bf16_to_double if dtype == "bf16" else lib.sa_oracle_fp16_to_double
     b = np.ascontiguousarray(bits, dtype=np.uint16).reshape(-1)
     return np.array([f(int(x)) for x in b], dtype=np.float64).reshape(np.shape(bits))
@@ -162,15 +167,16 @@ def rope_attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, B: int, H: int, L:
     """RoPE + attention core in FP64.
 
     q, k: uint16 bits, [B, H, L, d] (nmaps=1) or [B, H, 2, L, d] (nmaps=2);
-    v: uint16 bits [B, H, L, dv].  rows: flattened ids (b*H + h)*L + i, or None
+    v: uint16 bits [B, H, L, dv] (dtype "fp32": uint32 bits of FP32 values).  rows: flattened ids (b*H + h)*L + i, or None
     for every row.  qk_norm: None, or (gamma_q, gamma_k, eps) to RMSNorm every q
     and k row before RoPE (a gamma of None means ones).  Returns double
     [len(rows), dv] (or [B, H, L, dv] for None).
     """
     lib = _load()
-    q = np.ascontiguousarray(q, dtype=np.uint16)
-    k = np.ascontiguousarray(k, dtype=np.uint16)
-    v = np.ascontiguousarray(v, dtype=np.uint16)
+    bt, ct = (np.uint32, ctypes.c_uint32) if dtype == "fp32" else (np.uint16, ctypes.c_uint16)
+    q = np.ascontiguousarray(q, dtype=bt)
+    k = np.ascontiguousarray(k, dtype=bt)
+    v = np.ascontiguousarray(v, dtype=bt)
     if q.size != B * H * nmaps * L * d or k.size != q.size or v.size != B * H * L * dv:
         raise ValueError("shape mismatch")
     lam64 = None
@@ -193,7 +199,8 @@ def rope_attn(q: np.ndarray, k: np.ndarray, v: np.ndarray, *, B: int, H: int, L:
         if (gq is not None and gq.shape[0] != d) or (gk is not None and gk.shape[0] != d):
             raise ValueError("gamma must have d entries")
     rc = lib.sa_oracle_rope_attn_qknorm(
-        _ptr(q, ctypes.c_uint16), _ptr(k, ctypes.c_uint16), _ptr(v, ctypes.c_uint16),
+        ctypes.cast(_ptr(q, ct), ctypes.c_void_p), ctypes.cast(_ptr(k, ct), ctypes.c_void_p),
+        ctypes.cast(_ptr(v, ct), ctypes.c_void_p),
         _ptr(pos, ctypes.c_int32), B, H, L, d, nmaps, dv, int(window), _ptr(lam64, ctypes.c_double),
         DTYPES[dtype], CASTS[cast], float(base), int(qk_norm is not None), _ptr(gq, ctypes.c_double),
         _ptr(gk, ctypes.c_double), float(eps), _ptr(r, ctypes.c_int64), nrows,

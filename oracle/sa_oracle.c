@@ -8,7 +8,9 @@
  *
  * What it computes (slow, obviously correct, in the order the pages describe):
  *
- *   1. Decode the fp16/bf16 input bits exactly to double.
+ *   1. Decode the fp16/bf16 input bits exactly to double (or the FP32 bits of
+ *      the FP32-input form, SAME-L's FP32 attention projections, HF
+ *      discussion #6 "sm_120 SAME-L", "How the kernels differ").
  *   2. RoPE on every q and k row (rotate-half over the full head dim, base
  *      10000): theta_{p,i} = p * base^(-2i/d) for i < d/2, and
  *      x'_i = x_i cos - x_{i+d/2} sin,  x'_{i+d/2} = x_{i+d/2} cos + x_i sin.
@@ -18,7 +20,10 @@
  *      #3 "fp16mixed attention-core fix", sections "The bug" and "The fix").  Here the rotation is FP64 and,
  *      in the default "method" cast mode, the rotated q/k are rounded to the
  *      storage dtype (round to nearest even) and decoded back to double.
- *      Cast mode "exact" skips that rounding.
+ *      Cast mode "exact" skips that rounding.  For FP32 inputs the storage
+ *      dtype is FP32, so the method's cast rounds to FP32.  The TF32 rounding
+ *      of the tensor-core products is part of the method's kernel, not of
+ *      what it computes, and is not modelled.
  *   3. Scaled dot-product attention per row with the exact two-pass softmax:
  *      s_j = q.k_j / sqrt(d) over the allowed keys, m = max s_j,
  *      e_j = exp(s_j - m), l = sum e_j, o = sum (e_j / l) v_j
@@ -39,7 +44,8 @@
  *      for q and one for k, then RoPE, then the single cast-back of step 2.
  *
  * Layouts (C order): q, k [B][H][nmaps][L][d]; v [B][H][L][dv];
- * output rows [nrows][dv] in double.
+ * output rows [nrows][dv] in double.  Input elements are 2-byte fp16/bf16 bits,
+ * or 4-byte FP32 bits for dtype 2.
  */
 #include <math.h>
 #include <pthread.h>
@@ -49,6 +55,7 @@
 
 #define OR_FP16 0
 #define OR_BF16 1
+#define OR_FP32 2
 #define OR_CAST_METHOD 0
 #define OR_CAST_EXACT 1
 
@@ -84,8 +91,27 @@ double sa_oracle_bf16_to_double(uint16_t b)
     return sign ? -v : v;
 }
 
-static double bits_to_double(uint16_t x, int dtype)
+double sa_oracle_fp32_to_double(uint32_t f)
 {
+    int sign = (f >> 31) & 1;
+    int e = (f >> 23) & 0xff;
+    uint32_t m = f & 0x7fffff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -149);                /* subnormal: m * 2^(-126-23) */
+    else if (e == 255)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(m | 0x800000), e - 150); /* (2^23+m) * 2^(e-127-23) */
+    return sign ? -v : v;
+}
+
+/* Element i of an input array of the given dtype (2-byte bits, or 4-byte FP32 bits). */
+static double elem_to_double(const void* p, size_t i, int dtype)
+{
+    if (dtype == OR_FP32)
+        return sa_oracle_fp32_to_double(((const uint32_t*)p)[i]);
+    uint16_t x = ((const uint16_t*)p)[i];
     return dtype == OR_BF16 ? sa_oracle_bf16_to_double(x) : sa_oracle_fp16_to_double(x);
 }
 
@@ -113,6 +139,8 @@ static double round_generic(double x, int sig_bits, int emin, double max_finite)
 
 double sa_oracle_round(double x, int dtype)
 {
+    if (dtype == OR_FP32)   /* 24 significant bits, emin -126, max (2-2^-23)*2^127 */
+        return round_generic(x, 24, -126, ldexp(16777215.0, 104));
     if (dtype == OR_BF16)   /* 8 significant bits, emin -126, max (2-2^-7)*2^127 */
         return round_generic(x, 8, -126, ldexp(255.0, 120));
     /* fp16: 11 significant bits, emin -14, max 65504 */
@@ -179,7 +207,7 @@ int sa_oracle_rope(const double* x, const int32_t* pos, int64_t n, int d, double
 
 typedef struct {
     /* inputs */
-    const uint16_t *q, *k, *v;
+    const void *q, *k, *v;           /* uint16 bits (fp16, bf16) or uint32 bits (FP32) */
     const int32_t* positions;
     int B, H, L, d, nmaps, dv, window, dtype, cast_mode;
     const double* lambda;
@@ -228,10 +256,10 @@ static int prepare_head(job_t* J, int64_t bh)
         return -1;
     }
     for (int m = 0; m < nm; ++m) {
-        const uint16_t* ksrc = J->k + (((size_t)bh * nm + m) * L) * d;
+        size_t kbase = (((size_t)bh * nm + m) * L) * d;
         for (int l = 0; l < L; ++l) {
             for (int c = 0; c < d; ++c)
-                row[c] = bits_to_double(ksrc[(size_t)l * d + c], J->dtype);
+                row[c] = elem_to_double(J->k, kbase + (size_t)l * d + c, J->dtype);
             if (J->qk_norm)
                 rmsnorm_row(row, row, d, J->gamma_k, J->eps);
             double* dst = kr + ((size_t)m * L + l) * d;
@@ -240,9 +268,9 @@ static int prepare_head(job_t* J, int64_t bh)
                 dst[c] = cast_back(dst[c], J);
         }
     }
-    const uint16_t* vsrc = J->v + (size_t)bh * L * dv;
+    size_t vbase = (size_t)bh * L * dv;
     for (size_t i = 0; i < (size_t)L * dv; ++i)
-        vd[i] = bits_to_double(vsrc[i], J->dtype);
+        vd[i] = elem_to_double(J->v, vbase + i, J->dtype);
     free(row);
     J->vd[bh] = vd;
     J->kr[bh] = kr;   /* published last */
@@ -315,9 +343,9 @@ static void* worker(void* arg)
         for (int c = 0; c < dv; ++c)
             dst[c] = 0.0;
         for (int m = 0; m < nm; ++m) {
-            const uint16_t* qsrc = J->q + ((((size_t)bh * nm + m) * L) + i) * d;
+            size_t qbase = ((((size_t)bh * nm + m) * L) + i) * d;
             for (int c = 0; c < d; ++c)
-                qraw[c] = bits_to_double(qsrc[c], J->dtype);
+                qraw[c] = elem_to_double(J->q, qbase + c, J->dtype);
             if (J->qk_norm)
                 rmsnorm_row(qraw, qraw, d, J->gamma_q, J->eps);
             rope_row(qraw, qr, d, pos_of(J, i), J->base);
@@ -343,7 +371,7 @@ static void* worker(void* arg)
  * eps >= 0 normalise every q and k row before RoPE.
  * Returns 0 on success, a negative code on bad arguments or allocation failure.
  */
-int sa_oracle_rope_attn_qknorm(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+int sa_oracle_rope_attn_qknorm(const void* q, const void* k, const void* v,
                                const int32_t* positions, int B, int H, int L, int d, int nmaps,
                                int dv, int window, const double* lambda, int dtype, int cast_mode,
                                double base, int qk_norm, const double* gamma_q,
@@ -358,7 +386,7 @@ int sa_oracle_rope_attn_qknorm(const uint16_t* q, const uint16_t* k, const uint1
         return -2;
     if (nmaps == 2 && !lambda)
         return -3;
-    if (dtype != OR_FP16 && dtype != OR_BF16)
+    if (dtype != OR_FP16 && dtype != OR_BF16 && dtype != OR_FP32)
         return -4;
     int64_t total = (int64_t)B * H * L;
     if (!rows)
@@ -410,7 +438,7 @@ int sa_oracle_rope_attn_qknorm(const uint16_t* q, const uint16_t* k, const uint1
 }
 
 /* Public entry without the QK-RMSNorm (the attention core as the pages describe it). */
-int sa_oracle_rope_attn(const uint16_t* q, const uint16_t* k, const uint16_t* v,
+int sa_oracle_rope_attn(const void* q, const void* k, const void* v,
                         const int32_t* positions, int B, int H, int L, int d, int nmaps,
                         int dv, int window, const double* lambda, int dtype, int cast_mode,
                         double base, const int64_t* rows, int64_t nrows, double* out,

@@ -14,11 +14,15 @@ The five named workloads are the Stable Audio 3 attention shapes:
 * ``swa_diff_l8192``     B=1 H=16 L=8192 differential + |i-j|<=256 window, bf16,
                          per-head lambda ~ U(0.2, 0.8)
 
+Two more on the same shape: SAME-L's own window of +-17 (bf16), and the FP32-input
+form of the +-256 window workload (FP32 q, k, v: SAME-L's FP32 attention
+projections, whose products the method runs in TF32).
+
 Recipe (fixed order of draws from ``numpy.random.PCG64(seed)``):
 q, k, v as float32 N(0, 1); then, if requested, a Bernoulli(p) outlier mask
 over k that multiplies the hit entries by ``k_outlier_scale``; then lambda.
 Each tensor is rounded once, round-to-nearest-even, from float32 to the
-storage dtype.  Layouts: standard q/k/v ``[B, H, L, d]``; differential q/k
+storage dtype (FP32 inputs keep the drawn float32 values).  Layouts: standard q/k/v ``[B, H, L, d]``; differential q/k
 ``[B, H, 2, L, d]`` (map 0 = Q1/K1, map 1 = Q2/K2) and v ``[B, H, L, d_v]``.
 """
 
@@ -41,7 +45,7 @@ class Workload:
     d: int = 64
     nmaps: int = 1           # 1 = standard attention, 2 = differential attention
     dv: int = 64
-    dtype: str = "fp16"      # "fp16" | "bf16"
+    dtype: str = "fp16"      # "fp16" | "bf16" | "fp32"
     window: int = -1         # < 0: full attention; else |i - j| <= window
     seed: int = 0
     k_outlier_frac: float = 0.0
@@ -71,6 +75,10 @@ WORKLOADS = {
         # shape of the window workload above: a measurement case beyond the five configurations
         Workload("swa17_diff_l8192", B=1, H=16, L=8192, nmaps=2, dv=128, dtype="bf16",
                  window=17, seed=5, lam=("uniform", 0.2, 0.8)),
+        # the FP32-input form of the window workload (SAME-L's FP32 attention projections,
+        # TF32 products; same page, "How the kernels differ")
+        Workload("swa_diff_l8192_fp32", B=1, H=16, L=8192, nmaps=2, dv=128, dtype="fp32",
+                 window=256, seed=6, lam=("uniform", 0.2, 0.8)),
     ]
 }
 
@@ -80,8 +88,11 @@ def get_workload(name: str) -> Workload:
 
 
 def encode(x32: np.ndarray, dtype: str) -> np.ndarray:
-    """float32 -> uint16 bit patterns of fp16 / bf16, round to nearest even."""
+    """float32 -> uint16 bit patterns of fp16 / bf16, round to nearest even (uint32 bit
+    patterns of the float32 values themselves for "fp32")."""
     x32 = np.ascontiguousarray(x32, dtype=np.float32)
+    if dtype == "fp32":
+        return x32.view(np.uint32).copy()
     if dtype == "fp16":
         return x32.astype(np.float16).view(np.uint16)
     if dtype == "bf16":
@@ -95,7 +106,9 @@ def encode(x32: np.ndarray, dtype: str) -> np.ndarray:
 
 
 def decode(bits: np.ndarray, dtype: str) -> np.ndarray:
-    """uint16 bit patterns -> float32 (exact)."""
+    """uint16 (uint32 for "fp32") bit patterns -> float32 (exact)."""
+    if dtype == "fp32":
+        return np.ascontiguousarray(bits, dtype=np.uint32).view(np.float32).copy()
     bits = np.ascontiguousarray(bits, dtype=np.uint16)
     if dtype == "fp16":
         return bits.view(np.float16).astype(np.float32)

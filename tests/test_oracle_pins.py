@@ -528,3 +528,67 @@ def test_golden_tiny_rows(oracle_mod):
     x = synth.make_inputs(synth.WORKLOADS["tiny"])
     got = oracle_mod.rope_attn_workload(x, rows=rows)
     np.testing.assert_allclose(got, data[:, 1:], rtol=0, atol=1e-15)
+
+
+# ----------------------------------------------------------------------------- FP32-input form
+
+def test_fp32_decode_matches_numpy(oracle_mod):
+    # catches: wrong FP32 exponent bias or mantissa width, subnormal scale, sign, specials
+    rng = np.random.default_rng(41)
+    bits = np.concatenate([rng.integers(0, 2 ** 32, 20000, dtype=np.uint64).astype(np.uint32),
+                           np.array([0, 1, 0x7FFFFF, 0x800000, 0x3F800000, 0x7F7FFFFF, 0x7F800000,
+                                     0x80000000, 0x80000001, 0xFF800000], dtype=np.uint32)])
+    bits = bits[((bits & 0x7F800000) != 0x7F800000) | ((bits & 0x7FFFFF) == 0)]   # no NaNs
+    got = oracle_mod.bits_to_double(bits, "fp32")
+    ref = bits.view(np.float32).astype(np.float64)
+    np.testing.assert_array_equal(got, ref)
+
+
+def test_round_fp32_matches_numpy(oracle_mod):
+    # the method's cast for FP32 storage: numpy's float64 -> float32 cast (RNE) is the library
+    # routine; includes exact ties (midpoints between adjacent floats) and subnormals
+    rng = np.random.default_rng(42)
+    x = rng.standard_normal(20000) * np.exp(rng.uniform(-90, 90, 20000))
+    f = rng.standard_normal(2000).astype(np.float32)
+    ties = (f.astype(np.float64) + np.nextafter(f, np.float32(np.inf)).astype(np.float64)) / 2
+    sub = rng.uniform(-1, 1, 500) * 2.0 ** -130
+    x = np.concatenate([x, ties, sub, [0.0, -0.0, 3.4028234663852886e38]])
+    got = oracle_mod.round_to(x, "fp32")
+    np.testing.assert_array_equal(got, x.astype(np.float32).astype(np.float64))
+
+
+def _f32_bits(rng, shape):
+    return synth.encode(rng.standard_normal(shape).astype(np.float32), "fp32")
+
+
+def test_fp32_differential_window_is_rope_cast_two_masked_sdpa(oracle_mod):
+    # composition in the FP32-input form: oracle RoPE (pinned above) -> numpy float32 cast ->
+    # torch float64 SDPA with the window mask, map 1 weighted by -lambda_h.  catches: FP32 bits
+    # read as 16-bit elements, a 16-bit cast applied to FP32 storage, lambda on the wrong map
+    rng = np.random.default_rng(43)
+    B, H, L, w = 1, 2, 45, 6
+    q, k, v = _f32_bits(rng, (B, H, 2, L, 64)), _f32_bits(rng, (B, H, 2, L, 64)), _f32_bits(rng, (B, H, L, 128))
+    lam = np.array([0.35, 0.65])
+    pos = np.arange(L, dtype=np.int32) * 11 + 3
+    got = oracle_mod.rope_attn(q, k, v, B=B, H=H, L=L, nmaps=2, dv=128, dtype="fp32", lam=lam, window=w,
+                               positions=pos)
+    cast = lambda a: a.astype(np.float32).astype(np.float64)
+    rot = lambda bits: cast(oracle_mod.rope(_decode64(bits, "fp32").reshape(-1, 64),
+                                            np.tile(pos, bits.size // (64 * L))).reshape(bits.shape))
+    qr, kr, vd = rot(q), rot(k), _decode64(v, "fp32")
+    m = _window_mask(L, w)
+    ref = _sdpa64(qr[:, :, 0], kr[:, :, 0], vd, m) - lam[None, :, None, None] * _sdpa64(qr[:, :, 1], kr[:, :, 1], vd, m)
+    np.testing.assert_allclose(got, ref, rtol=1e-11, atol=1e-13)
+
+
+def test_fp32_form_on_fp16_values_equals_fp16_form_exact(oracle_mod):
+    # inputs that fp16 represents exactly: with the cast skipped ("exact" mode) only the decoding
+    # differs, so the FP32 and fp16 forms must agree bit for bit
+    rng = np.random.default_rng(44)
+    B, H, L = 1, 2, 33
+    h = [_rand_bits(rng, s, "fp16") for s in [(B, H, 2, L, 64), (B, H, 2, L, 64), (B, H, L, 128)]]
+    f = [synth.encode(synth.decode(b, "fp16"), "fp32") for b in h]
+    lam = np.array([0.4, 0.6])
+    a = oracle_mod.rope_attn(*h, B=B, H=H, L=L, nmaps=2, dv=128, dtype="fp16", lam=lam, window=9, cast="exact")
+    b = oracle_mod.rope_attn(*f, B=B, H=H, L=L, nmaps=2, dv=128, dtype="fp32", lam=lam, window=9, cast="exact")
+    np.testing.assert_array_equal(a, b)
