@@ -67,8 +67,15 @@ def flops(w) -> int:
 
 
 def io_bytes(w) -> int:
+    """q', k' (both maps), v read once and out written once, in the storage dtype."""
     n = w.B * w.H * w.L
-    return 2 * (n * w.nmaps * w.d * 2 + n * w.dv + n * w.dv)
+    elem = 4 if w.dtype == "fp32" else 2
+    return elem * (n * w.nmaps * w.d * 2 + n * w.dv + n * w.dv)
+
+
+# Dense TF32 / dense BF16 tensor rate, nominal (GB300: 1.1 and 2.25 PFLOP/s): the FP32-input
+# workloads' products run as TF32 MMAs, so their peak is the measured bf16 rate times this.
+TF32_OVER_BF16 = 1.1 / 2.25
 
 
 def load_peaks():
@@ -304,8 +311,8 @@ def workload_of(args):
 
 # Workloads measured beside the headline one in the default run (each in the line's `workloads`
 # map): the long-sequence DiT configuration that the 60% target is quoted on, differential
-# attention, and the two sliding windows.
-EXTRA_WORKLOADS = ["dit_l4096_outliers", "diff_l4096", "swa_diff_l8192", "swa17_diff_l8192"]
+# attention, the two sliding windows, and the FP32-input form (TF32 products) of the first.
+EXTRA_WORKLOADS = ["dit_l4096_outliers", "diff_l4096", "swa_diff_l8192", "swa17_diff_l8192", "swa_diff_l8192_fp32"]
 
 
 def run_ours(args):
@@ -338,16 +345,19 @@ def measure(args, w, dist, world, rank, local, device, cpu_budget):
     import diffusion_transformer_attention_rope_gb300 as sa
 
     x = synth.make_inputs(w, seed=w.seed + rank)
-    tdt = torch.float16 if w.dtype == "fp16" else torch.bfloat16
-    dtype = sa.SA_FP16 if w.dtype == "fp16" else sa.SA_BF16
+    tdt = {"fp16": torch.float16, "bf16": torch.bfloat16, "fp32": torch.float32}[w.dtype]
+    dtype = {"fp16": sa.SA_FP16, "bf16": sa.SA_BF16, "fp32": sa.SA_FP32}[w.dtype]
+    fp32 = w.dtype == "fp32"
 
     def to_dev(bits):
+        if fp32:
+            return torch.from_numpy(bits.view(np.int32)).to(device).view(tdt)
         return torch.from_numpy(bits.view(np.int16)).to(device).view(tdt)
 
     q, k, v = to_dev(x["q"]), to_dev(x["k"]), to_dev(x["v"])
     out = torch.empty((w.B, w.H, w.L, w.dv), dtype=tdt, device=device)
     lam = None if x["lam"] is None else [float(t) for t in x["lam"]]
-    ws_bytes = sa.sa_rope_attn_workspace_size(w.B, w.H, w.L, w.d, w.differential)
+    ws_bytes = sa.sa_rope_attn_workspace_bytes(w.B, w.H, w.L, w.d, w.differential, dtype)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
     nqk = q.numel()
     # the workspace of sa_rope_attn: the (cos, sin) table, k', the split region; region 2 runs
@@ -364,7 +374,26 @@ def measure(args, w, dist, world, rank, local, device, cpu_budget):
     s = stream.cuda_stream
 
     nrm = qk_norm_params(args.qk_norm)
-    if nrm is None:
+    if fp32:
+        # the FP32-input form: its two stages are the FP32 RoPE pass (q' and k' into the
+        # workspace) and the TF32 attention kernel on them
+        if nrm is not None:
+            raise SystemExit("--qk-norm has no FP32 form")
+        off_k32 = a256(nqk * 4)
+        off_v32 = 2 * a256(nqk * 4)
+
+        def rope():
+            sa.sa_rope_qkv_f32(h, q.data_ptr(), k.data_ptr(), v.data_ptr(), None, ws.data_ptr(),
+                               ws.data_ptr() + off_k32, ws.data_ptr() + off_v32, w.B, w.H, w.L, w.d, s)
+
+        def attn():
+            sa.sa_attn_fwd_f32(h, ws.data_ptr(), ws.data_ptr() + off_k32, ws.data_ptr() + off_v32, out.data_ptr(),
+                               w.B, w.H, w.L, w.d, w.window, lam, s)
+
+        def full():
+            sa.sa_rope_attn(h, q.data_ptr(), k.data_ptr(), v.data_ptr(), None, out.data_ptr(), w.B, w.H,
+                            w.L, w.d, w.window, lam, dtype, ws.data_ptr(), ws_bytes, s)
+    elif nrm is None:
         def rope():
             sa.sa_rope_k(h, k.data_ptr(), None, k_rot.data_ptr(), cs_table.data_ptr(),
                          w.B, w.H, w.L, w.d, w.nmaps, dtype, s)
@@ -464,17 +493,18 @@ def measure(args, w, dist, world, rank, local, device, cpu_budget):
 
     # e2e: the C-ABI call on pinned HOST buffers (sa_rope_attn_host: copies in, the path, copy out,
     # pipelined over chunks of planes), the copies inside the timed region.  The QK-norm variant
-    # has no host entry: its copies are plain stream copies around the device call.
+    # and the FP32 form have no host entry: their copies are plain stream copies around the
+    # device call.
     qh, kh, vh = (t.cpu().pin_memory() for t in (q, k, v))
     oh = torch.empty(out.shape, dtype=tdt).pin_memory()
     ev2 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     hws_bytes = sa.sa_rope_attn_host_workspace_size(w.B, w.H, w.L, w.d, w.differential)
-    hws = torch.empty(hws_bytes, dtype=torch.uint8, device=device) if nrm is None else None
+    hws = torch.empty(hws_bytes, dtype=torch.uint8, device=device) if nrm is None and not fp32 else None
 
     def e2e_step(e=None):
         if e is not None:
             e[0].record(stream)
-        if nrm is None:
+        if nrm is None and not fp32:
             sa.sa_rope_attn_host(h, qh.data_ptr(), kh.data_ptr(), vh.data_ptr(), None, oh.data_ptr(), w.B, w.H,
                                  w.L, w.d, w.window, lam, dtype, hws.data_ptr(), hws_bytes, s)
         else:
@@ -506,6 +536,9 @@ def measure(args, w, dist, world, rank, local, device, cpu_budget):
         return None
     fl = flops(w)
     peaks = load_peaks()
+    if fp32:
+        peaks = dict(peaks, tflops=peaks["tflops"] * TF32_OVER_BF16,
+                     source=peaks["source"] + " bf16 burst x nominal tf32/bf16 (1.1/2.25); tf32")
     value = job_throughput(world, fl, args.steps, total_ms)
     attn_avg_s = statistics.mean(attn_ms) * 1e-3
     achieved = fl / attn_avg_s / 1e12
@@ -536,9 +569,11 @@ def measure(args, w, dist, world, rank, local, device, cpu_budget):
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["tflops"],
                      "traffic": load_traffic(w.name) if nrm is None else None,
-                     "kernel": "attention (sa_attn_fwd_rope_q)" if nrm is None else
-                               "attention (sa_attn_fwd on sa_qknorm_rope_qk output)", "kernel_sha": kernel_sha(),
-                     "peak_source": peaks["source"] + " bf16 burst",
+                     "kernel": ("attention, TF32 (sa_attn_fwd_f32 on sa_rope_qkv_f32 output)" if fp32 else
+                                "attention (sa_attn_fwd_rope_q)" if nrm is None else
+                                "attention (sa_attn_fwd on sa_qknorm_rope_qk output)"),
+                     "kernel_sha": kernel_sha(),
+                     "peak_source": peaks["source"] if fp32 else peaks["source"] + " bf16 burst",
                      "avg_ms": attn_avg_s * 1e3,
                      # the same launch against the HBM roof: algorithmic bytes (q', k', v read once,
                      # out written once) over its duration, of the measured copy bandwidth

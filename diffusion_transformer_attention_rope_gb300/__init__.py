@@ -17,7 +17,7 @@ import threading
 from typing import Optional, Sequence
 
 __all__ = [
-    "SA_FP16", "SA_BF16", "SaAttnError", "library_path", "load_library",
+    "SA_FP16", "SA_BF16", "SA_FP32", "SaAttnError", "sa_rope_attn_workspace_bytes", "sa_attn_fwd_workspace_bytes", "sa_rope_qkv_f32", "sa_attn_fwd_f32", "library_path", "load_library",
     "sa_attn_create", "sa_attn_destroy", "sa_rope_attn_workspace_size", "sa_attn_fwd_workspace_size", "sa_rope_table_bytes", "sa_rope_k", "sa_attn_fwd_rope_q", "sa_rope_attn",
     "sa_rope_qk", "sa_rope_attn_qknorm", "sa_qknorm_rope_qk", "sa_rope_attn_host",
     "sa_rope_attn_host_workspace_size", "sa_attn_fwd", "sa_rope_attn_noalloc", "sa_attn_check", "sa_attn_set_timeout", "sa_last_error", "sa_status_string", "RopeAttention",
@@ -25,6 +25,7 @@ __all__ = [
 
 SA_FP16 = 0
 SA_BF16 = 1
+SA_FP32 = 2   # differential attention with FP32 q, k, v, out (TF32 products)
 STATUS_NAMES = {0: "SA_OK", 1: "SA_ERR_INVALID_ARG", 2: "SA_ERR_UNSUPPORTED", 3: "SA_ERR_CUDA",
                 4: "SA_ERR_DEVICE_TIMEOUT", 5: "SA_ERR_NO_DEVICE", 6: "SA_ERR_WORKSPACE"}
 
@@ -62,6 +63,14 @@ def load_library():
         lib.sa_attn_destroy.restype = i
         lib.sa_rope_attn_workspace_size.argtypes = [i, i, i, i, i]
         lib.sa_rope_attn_workspace_size.restype = sz
+        lib.sa_rope_attn_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        lib.sa_rope_attn_workspace_bytes.restype = sz
+        lib.sa_attn_fwd_workspace_bytes.argtypes = [i, i, i, i, i, i]
+        lib.sa_attn_fwd_workspace_bytes.restype = sz
+        lib.sa_rope_qkv_f32.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i, i, i, i, vp]
+        lib.sa_rope_qkv_f32.restype = i
+        lib.sa_attn_fwd_f32.argtypes = [vp, vp, vp, vp, vp, i, i, i, i, i, ctypes.POINTER(f), vp]
+        lib.sa_attn_fwd_f32.restype = i
         lib.sa_rope_attn.argtypes = [vp, vp, vp, vp, vp, vp, i, i, i, i, i,
                                      ctypes.POINTER(f), i, vp, sz, vp]
         lib.sa_rope_attn.restype = i
@@ -128,6 +137,31 @@ def sa_attn_destroy(handle: int) -> None:
 
 def sa_rope_attn_workspace_size(B: int, H: int, L: int, d: int, differential: bool) -> int:
     return int(load_library().sa_rope_attn_workspace_size(B, H, L, d, 1 if differential else 0))
+
+
+def sa_rope_attn_workspace_bytes(B: int, H: int, L: int, d: int, differential: bool, dtype: int) -> int:
+    return int(load_library().sa_rope_attn_workspace_bytes(B, H, L, d, 1 if differential else 0, int(dtype)))
+
+
+def sa_attn_fwd_workspace_bytes(B: int, H: int, L: int, d: int, differential: bool, dtype: int) -> int:
+    return int(load_library().sa_attn_fwd_workspace_bytes(B, H, L, d, 1 if differential else 0, int(dtype)))
+
+
+def sa_rope_qkv_f32(handle: int, q: int, k: int, v: int, positions: Optional[int], q_rot: int, k_rot: int,
+                    v_t: int, B: int, H: int, L: int, d: int, stream: Optional[int]) -> None:
+    """The FP32 form's pre-pass: q', k' rotated and rounded to TF32, v transposed to v^T (TF32)."""
+    _check(load_library().sa_rope_qkv_f32(
+        ctypes.c_void_p(handle), ctypes.c_void_p(q), ctypes.c_void_p(k), ctypes.c_void_p(v),
+        ctypes.c_void_p(positions), ctypes.c_void_p(q_rot), ctypes.c_void_p(k_rot), ctypes.c_void_p(v_t),
+        int(B), int(H), int(L), int(d), ctypes.c_void_p(stream)))
+
+
+def sa_attn_fwd_f32(handle: int, q_rot: int, k_rot: int, v_t: int, out: int, B: int, H: int, L: int, d: int,
+                    window: int, lam: Sequence[float], stream: Optional[int]) -> None:
+    """The FP32 form's TF32 attention kernel on the pre-pass's q', k', v^T."""
+    _check(load_library().sa_attn_fwd_f32(
+        ctypes.c_void_p(handle), ctypes.c_void_p(q_rot), ctypes.c_void_p(k_rot), ctypes.c_void_p(v_t),
+        ctypes.c_void_p(out), int(B), int(H), int(L), int(d), int(window), _lam(lam), ctypes.c_void_p(stream)))
 
 
 def sa_attn_fwd_workspace_size(B: int, H: int, L: int, d: int, differential: bool) -> int:
@@ -280,6 +314,7 @@ class RopeAttention:
     ``attn(q, k, v, positions=None, window=-1, lam=None)`` returns ``out``.
     Standard attention: q, k, v ``[B, H, L, 64]``.  Differential (``lam`` given,
     one float per head or a scalar): q, k ``[B, H, 2, L, 64]``, v ``[B, H, L, 128]``.
+    fp16 / bf16 tensors, or float32 for differential attention (TF32 products).
     Output and workspace are allocated with torch on the current stream.
     """
 
@@ -299,10 +334,10 @@ class RopeAttention:
         except Exception:
             pass
 
-    def workspace(self, B: int, H: int, L: int, differential: bool):
+    def workspace(self, B: int, H: int, L: int, differential: bool, dtype: int = SA_FP16):
         import torch
 
-        need = sa_rope_attn_workspace_size(B, H, L, 64, differential)
+        need = sa_rope_attn_workspace_bytes(B, H, L, 64, differential, dtype)
         if self._ws is None or self._ws.numel() < need:
             self._ws = torch.empty(need, dtype=torch.uint8, device=f"cuda:{self.device}")
         return self._ws
@@ -310,7 +345,7 @@ class RopeAttention:
     def __call__(self, q, k, v, positions=None, window: int = -1, lam=None, out=None, stream=None):
         import torch
 
-        dtype = {torch.float16: SA_FP16, torch.bfloat16: SA_BF16}.get(q.dtype)
+        dtype = {torch.float16: SA_FP16, torch.bfloat16: SA_BF16, torch.float32: SA_FP32}.get(q.dtype)
         if dtype is None:
             raise SaAttnError(1, f"unsupported dtype {q.dtype}")
         for name, t in (("q", q), ("k", k), ("v", v), ("positions", positions), ("out", out)):
@@ -326,7 +361,7 @@ class RopeAttention:
             lam = [float(lam)] * H
         if out is None:
             out = torch.empty((B, H, L, dv), dtype=q.dtype, device=q.device)
-        ws = self.workspace(B, H, L, diff)
+        ws = self.workspace(B, H, L, diff, dtype)
         s = torch.cuda.current_stream(q.device).cuda_stream if stream is None else stream
         sa_rope_attn(self.handle, q.data_ptr(), k.data_ptr(), v.data_ptr(),
                      None if positions is None else positions.data_ptr(), out.data_ptr(),

@@ -89,6 +89,30 @@ bool encode_map(const sa_attn_s* h, CUtensorMap* m, const void* base, bool bf16,
   return r == CUDA_SUCCESS;
 }
 
+// The FP32 form: [planes][rows][cols] FP32 (rows row_pitch elements apart, cols if 0), box = 32
+// cols (128 bytes) x box_rows x 1 plane, 128-byte swizzle, elements past the end read as zeros.
+bool encode_map_f32(const sa_attn_s* h, CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows,
+                    uint64_t planes, uint32_t box_rows, uint64_t row_pitch = 0) {
+  const uint64_t pitch = row_pitch ? row_pitch : cols;   // elements per row in memory
+  const cuuint64_t dims[3] = {cols, rows, planes};
+  const cuuint64_t strides[2] = {pitch * 4, pitch * 4 * rows};
+  const cuuint32_t box[3] = {32, box_rows, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = h->encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box,
+                         estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Entry points whose 16-bit-only forms (the Q prologue, the QK-RMSNorm, host buffers) have no
+// FP32 counterpart.
+sa_status reject_fp32(const char* fn, sa_dtype dtype) {
+  if (dtype == SA_FP32)
+    return fail(SA_ERR_UNSUPPORTED, "%s: SA_FP32 is supported by sa_rope_attn, sa_rope_attn_noalloc, "
+                "sa_rope_qk and sa_attn_fwd only", fn);
+  return SA_OK;
+}
+
 bool qk_elems(int B, int H, int L, int nmaps, size_t* out) {
   if (B <= 0 || H <= 0 || L <= 0) return false;
   const unsigned long long n = static_cast<unsigned long long>(B) * H * nmaps * L * sa::kHeadDim;
@@ -164,8 +188,11 @@ sa_status check_shape(const char* fn, int B, int H, int L, int d, sa_dtype dtype
     return fail(SA_ERR_UNSUPPORTED, "%s: L = %d exceeds the supported maximum %d", fn, L, sa::kMaxL - 1);
   if (d != sa::kHeadDim)
     return fail(SA_ERR_UNSUPPORTED, "%s: head dim d = %d; only d = 64 is supported", fn, d);
-  if (dtype != SA_FP16 && dtype != SA_BF16)
+  if (dtype != SA_FP16 && dtype != SA_BF16 && dtype != SA_FP32)
     return fail(SA_ERR_INVALID_ARG, "%s: unknown dtype %d", fn, static_cast<int>(dtype));
+  if (dtype == SA_FP32 && !diff)
+    return fail(SA_ERR_UNSUPPORTED, "%s: SA_FP32 inputs are supported for differential attention "
+                "(lambda != NULL, two maps) only", fn);
   if (diff && H > sa::kMaxDiffHeads)
     return fail(SA_ERR_UNSUPPORTED, "%s: differential attention supports H <= %d (got %d)", fn,
                 sa::kMaxDiffHeads, H);
@@ -365,6 +392,77 @@ sa_status launch_attn(const sa_attn_s* h, const void* q_rot, const void* k_rot, 
   return ok();
 }
 
+// Keys per row of the FP32 form's v^T (rows of 16 bytes for its tensor map).
+int f32_lpad(int L) { return (L + 3) & ~3; }
+
+size_t f32_vt_bytes(int B, int H, int L) {
+  return align256(static_cast<size_t>(B) * H * 2 * sa::kHeadDim * f32_lpad(L) * 4);
+}
+
+// The FP32 form's pre-pass: q' and k' (both maps) rotated in FP32 and rounded to TF32 (q == nullptr:
+// none), and v^T [B*H][128][L_pad] rounded to TF32 (v == nullptr: none).
+sa_status launch_rope_f32(const sa_attn_s* h, const void* q, const void* k, const int32_t* positions,
+                          void* q_rot, void* k_rot, int B, int H, int L, sa_stream_t stream,
+                          const void* v = nullptr, void* v_t = nullptr) {
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return fail(SA_ERR_CUDA, "cannot select device %d", h->device);
+  sa::RopeF32Args ra;
+  std::memset(&ra, 0, sizeof(ra));
+  ra.q = static_cast<const float*>(q);
+  ra.k = static_cast<const float*>(k);
+  ra.q_out = static_cast<float*>(q_rot);
+  ra.k_out = static_cast<float*>(k_rot);
+  ra.positions = positions;
+  ra.planes = static_cast<long long>(B) * H * 2;
+  ra.L = L;
+  std::memcpy(ra.inv_freq, h->inv_freq, sizeof(ra.inv_freq));
+  ra.v = static_cast<const float*>(v);
+  ra.v_t = static_cast<float*>(v_t);
+  ra.planes_v = static_cast<long long>(B) * H;
+  ra.L_pad = f32_lpad(L);
+  const cudaError_t e = sa::rope_f32_launch(ra, h->num_sms, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(SA_ERR_CUDA, "RoPE (FP32) launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+// The FP32 form's attention stage on q', k' and v^T (TF32 products), one CTA per 128-row query
+// block.
+sa_status launch_attn_f32(const sa_attn_s* h, const void* q_rot, const void* k_rot, const void* v_t, void* out,
+                          int B, int H, int L, int window, const float* lambda, sa_stream_t stream) {
+  const int d = sa::kHeadDim;
+  const unsigned long long planes_qk = static_cast<unsigned long long>(B) * H * 2;
+  const unsigned long long planes_v = static_cast<unsigned long long>(B) * H;
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (!encode_map_f32(h, &tm_q, q_rot, d, L, planes_qk, sa::kBlockM) ||
+      !encode_map_f32(h, &tm_k, k_rot, d, L, planes_qk, 64) ||
+      !encode_map_f32(h, &tm_v, v_t, L, 2 * d, planes_v, sa::kBlockM, f32_lpad(L)))
+    return fail(SA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor map");
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return fail(SA_ERR_CUDA, "cannot select device %d", h->device);
+  sa::FmhaF32Args fa;
+  std::memset(&fa, 0, sizeof(fa));
+  fa.out = static_cast<float*>(out);
+  fa.err = h->d_err;
+  fa.L = L;
+  fa.H = H;
+  fa.n_qblocks = (L + sa::kBlockM - 1) / sa::kBlockM;
+  fa.window = (window < 0 || window >= L - 1) ? -1 : window;
+  fa.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(d)));
+  fa.timeout_ns = h->timeout_ns;
+  for (int i = 0; i < H; ++i) fa.lambda[i] = lambda[i];
+  const long long ctas = static_cast<long long>(B) * H * fa.n_qblocks;
+  const cudaError_t e = sa::fmha_tf32_launch(tm_q, tm_k, tm_v, fa, ctas, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(SA_ERR_CUDA, "attention (TF32) launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
+// sa_rope_attn's FP32 workspace: q', k', v^T.
+size_t f32_ws_bytes(int B, int H, int L) {
+  size_t n = 0;
+  if (!qk_elems(B, H, L, 2, &n)) return 0;
+  return 2 * align256(n * 4) + f32_vt_bytes(B, H, L);
+}
+
 }  // namespace
 
 namespace sa {
@@ -400,6 +498,15 @@ sa_status rope_attn_into(const char* fn, sa_attn_t h, const void* q, const void*
   sa_status st = check_shape(fn, B, H, L, d, dtype, diff);
   if (st != SA_OK) return st;
   if ((st = check_lambda(fn, lambda, H)) != SA_OK) return st;
+  if (dtype == SA_FP32) {
+    // v^T follows k' (the caller's scratch holds all three)
+    size_t n32 = 0;
+    qk_elems(B, H, L, 2, &n32);
+    void* v_t = static_cast<uint8_t*>(k_rot) + align256(n32 * 4);
+    st = launch_rope_f32(h, q, k, positions, q_rot, k_rot, B, H, L, stream, v, v_t);
+    if (st != SA_OK) return st;
+    return launch_attn_f32(h, q_rot, k_rot, v_t, out, B, H, L, window, lambda, stream);
+  }
   st = launch_rope(h, q, k, positions, q_rot, k_rot, B, H, L, diff ? 2 : 1, dtype, stream);
   if (st != SA_OK) return st;
   return launch_attn(h, q_rot, k_rot, v, out, B, H, L, window, lambda, dtype, nullptr, stream);
@@ -474,14 +581,14 @@ sa_status sa_attn_create(sa_attn_t* handle, int device, float rope_base) {
   h->host_ready = create_host_streams(h);
   create_table(h);
   if ((e = cudaMemset(h->d_err, 0, sizeof(int))) != cudaSuccess ||
-      (e = sa::fmha_set_attributes()) != cudaSuccess) {
+      (e = sa::fmha_set_attributes()) != cudaSuccess || (e = sa::fmha_tf32_set_attributes()) != cudaSuccess) {
     cudaFree(h->d_err);
     destroy_host_streams(h);
     delete h;
     return fail(SA_ERR_CUDA, "sa_attn_create: %s", cudaGetErrorString(e));
   }
-  int regs = -1;
-  if (!sa::fmha_check_registers(&regs)) {
+  int regs = -1, regs_tf32 = -1;
+  if (!sa::fmha_check_registers(&regs) || !sa::fmha_tf32_check(&regs_tf32)) {
     // The warpgroup register split (setmaxnreg) is sized for this launch allocation; any
     // other value could make the register grow wait forever, so refuse to run.
     cudaFree(h->d_err);
@@ -517,6 +624,20 @@ size_t sa_rope_attn_workspace_size(int B, int H, int L, int d, int differential)
   return align256(sa_rope_table_bytes(L)) + align256(n * 2) + split_bytes(B, H, L, differential != 0);
 }
 
+size_t sa_rope_attn_workspace_bytes(int B, int H, int L, int d, int differential, sa_dtype dtype) {
+  if (dtype == SA_FP16 || dtype == SA_BF16) return sa_rope_attn_workspace_size(B, H, L, d, differential);
+  if (dtype != SA_FP32 || !differential || d != sa::kHeadDim || L >= sa::kMaxL) return 0;
+  return f32_ws_bytes(B, H, L);
+}
+
+size_t sa_attn_fwd_workspace_bytes(int B, int H, int L, int d, int differential, sa_dtype dtype) {
+  if (dtype == SA_FP16 || dtype == SA_BF16) return sa_attn_fwd_workspace_size(B, H, L, d, differential);
+  size_t n = 0;
+  if (dtype != SA_FP32 || !differential || d != sa::kHeadDim || L >= sa::kMaxL || !qk_elems(B, H, L, 2, &n))
+    return 0;
+  return f32_vt_bytes(B, H, L);
+}
+
 size_t sa_attn_fwd_workspace_size(int B, int H, int L, int d, int differential) {
   size_t n = 0;
   if (d != sa::kHeadDim || !qk_elems(B, H, L, differential ? 2 : 1, &n)) return 0;
@@ -535,6 +656,7 @@ sa_status sa_rope_qk(sa_attn_t h, const void* q, const void* k, const int32_t* p
   if (nmaps != 1 && nmaps != 2) return fail(SA_ERR_INVALID_ARG, "%s: nmaps must be 1 or 2", fn);
   sa_status st = check_shape(fn, B, H, L, d, dtype, nmaps == 2);
   if (st != SA_OK) return st;
+  if (dtype == SA_FP32) return launch_rope_f32(h, q, k, positions, q_rot, k_rot, B, H, L, stream);
   return launch_rope(h, q, k, positions, q_rot, k_rot, B, H, L, nmaps, dtype, stream);
 }
 
@@ -552,6 +674,15 @@ sa_status sa_attn_fwd(sa_attn_t h, const void* q_rot, const void* k_rot, const v
   sa_status st = check_shape(fn, B, H, L, d, dtype, diff);
   if (st != SA_OK) return st;
   if ((st = check_lambda(fn, lambda, H)) != SA_OK) return st;
+  if (dtype == SA_FP32) {
+    // v^T (TF32) into the workspace, then attention on it
+    if (!workspace || workspace_bytes < f32_vt_bytes(B, H, L))
+      return fail(SA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed for the FP32 form, %zu given%s", fn,
+                  f32_vt_bytes(B, H, L), workspace_bytes, workspace ? "" : " (NULL)");
+    st = launch_rope_f32(h, nullptr, nullptr, nullptr, nullptr, nullptr, B, H, L, stream, v, workspace);
+    if (st != SA_OK) return st;
+    return launch_attn_f32(h, q_rot, k_rot, workspace, out, B, H, L, window, lambda, stream);
+  }
   if (workspace && workspace_bytes < split_bytes(B, H, L, diff))
     return fail(SA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given", fn,
                 split_bytes(B, H, L, diff), workspace_bytes);
@@ -562,6 +693,7 @@ sa_status sa_rope_k(sa_attn_t h, const void* k, const int32_t* positions, void* 
                     int B, int H, int L, int d, int nmaps, sa_dtype dtype, sa_stream_t stream) {
   const char* fn = "sa_rope_k";
   if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
+  if (reject_fp32(fn, dtype) != SA_OK) return SA_ERR_UNSUPPORTED;
   if (!k || !k_rot || !cs_table)
     return fail(SA_ERR_INVALID_ARG, "%s: k, k_rot and cs_table must be non-NULL", fn);
   if (!aligned16(k) || !aligned16(k_rot) || !aligned16(cs_table))
@@ -578,6 +710,7 @@ sa_status sa_attn_fwd_rope_q(sa_attn_t h, const void* q, const void* k_rot, cons
                              size_t workspace_bytes, sa_stream_t stream) {
   const char* fn = "sa_attn_fwd_rope_q";
   if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
+  if (reject_fp32(fn, dtype) != SA_OK) return SA_ERR_UNSUPPORTED;
   if (!q || !k_rot || !cs_table || !v || !out)
     return fail(SA_ERR_INVALID_ARG, "%s: q, k_rot, cs_table, v and out must be non-NULL", fn);
   if (!aligned16(q) || !aligned16(k_rot) || !aligned16(cs_table) || !aligned16(v) || !aligned16(out) ||
@@ -615,6 +748,21 @@ sa_status rope_attn_ws(const char* fn, sa_attn_t h, const void* q, const void* k
   sa_status st = check_shape(fn, B, H, L, d, dtype, diff);
   if (st != SA_OK) return st;
   if ((st = check_lambda(fn, lambda, H)) != SA_OK) return st;
+  if (dtype == SA_FP32) {
+    if (nrm) return fail(SA_ERR_UNSUPPORTED, "%s: the QK-RMSNorm form takes SA_FP16 or SA_BF16", fn);
+    const size_t need32 = f32_ws_bytes(B, H, L);
+    if (!workspace || workspace_bytes < need32)
+      return fail(SA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given%s", fn, need32,
+                  workspace_bytes, workspace ? "" : " (NULL)");
+    size_t n32 = 0;
+    qk_elems(B, H, L, 2, &n32);
+    uint8_t* ws32 = static_cast<uint8_t*>(workspace);
+    uint8_t* k32 = ws32 + align256(n32 * 4);
+    uint8_t* vt32 = k32 + align256(n32 * 4);
+    st = launch_rope_f32(h, q, k, positions, ws32, k32, B, H, L, stream, v, vt32);
+    if (st != SA_OK) return st;
+    return launch_attn_f32(h, ws32, k32, vt32, out, B, H, L, window, lambda, stream);
+  }
   const size_t need = sa_rope_attn_workspace_size(B, H, L, d, diff);
   if (!workspace || workspace_bytes < need)
     return fail(SA_ERR_WORKSPACE, "%s: workspace of %zu bytes needed, %zu given%s", fn, need,
@@ -736,6 +884,7 @@ sa_status sa_rope_attn_host(sa_attn_t h, const void* q, const void* k, const voi
                             size_t workspace_bytes, sa_stream_t stream) {
   const char* fn = "sa_rope_attn_host";
   if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
+  if (reject_fp32(fn, dtype) != SA_OK) return SA_ERR_UNSUPPORTED;
   if (!q || !k || !v || !out)
     return fail(SA_ERR_INVALID_ARG, "%s: q, k, v and out must be non-NULL", fn);
   if (!workspace || !aligned16(workspace))
@@ -828,6 +977,7 @@ sa_status sa_qknorm_rope_qk(sa_attn_t h, const void* q, const void* k, const int
                             sa_stream_t stream) {
   const char* fn = "sa_qknorm_rope_qk";
   if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
+  if (reject_fp32(fn, dtype) != SA_OK) return SA_ERR_UNSUPPORTED;
   if (!q || !k || !q_rot || !k_rot)
     return fail(SA_ERR_INVALID_ARG, "%s: q, k, q_rot and k_rot must be non-NULL", fn);
   if (!aligned16(q) || !aligned16(k) || !aligned16(q_rot) || !aligned16(k_rot))
@@ -838,6 +988,34 @@ sa_status sa_qknorm_rope_qk(sa_attn_t h, const void* q, const void* k, const int
   QkNorm nrm;
   if ((st = make_qknorm(fn, gamma_q, gamma_k, eps, &nrm)) != SA_OK) return st;
   return launch_rope(h, q, k, positions, q_rot, k_rot, B, H, L, nmaps, dtype, stream, nullptr, &nrm);
+}
+
+sa_status sa_rope_qkv_f32(sa_attn_t h, const void* q, const void* k, const void* v, const int32_t* positions,
+                         void* q_rot, void* k_rot, void* v_t, int B, int H, int L, int d, sa_stream_t stream) {
+  const char* fn = "sa_rope_qkv_f32";
+  if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
+  if (!q || !k || !v || !q_rot || !k_rot || !v_t)
+    return fail(SA_ERR_INVALID_ARG, "%s: q, k, v, q_rot, k_rot and v_t must be non-NULL", fn);
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(q_rot) || !aligned16(k_rot) || !aligned16(v_t))
+    return fail(SA_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);
+  sa_status st = check_shape(fn, B, H, L, d, SA_FP32, true);
+  if (st != SA_OK) return st;
+  return launch_rope_f32(h, q, k, positions, q_rot, k_rot, B, H, L, stream, v, v_t);
+}
+
+sa_status sa_attn_fwd_f32(sa_attn_t h, const void* q_rot, const void* k_rot, const void* v_t, void* out, int B,
+                          int H, int L, int d, int window, const float* lambda, sa_stream_t stream) {
+  const char* fn = "sa_attn_fwd_f32";
+  if (!h) return fail(SA_ERR_INVALID_ARG, "%s: handle is NULL", fn);
+  if (!q_rot || !k_rot || !v_t || !out)
+    return fail(SA_ERR_INVALID_ARG, "%s: q_rot, k_rot, v_t and out must be non-NULL", fn);
+  if (!aligned16(q_rot) || !aligned16(k_rot) || !aligned16(v_t) || !aligned16(out))
+    return fail(SA_ERR_INVALID_ARG, "%s: pointers must be 16-byte aligned", fn);
+  if (!lambda) return fail(SA_ERR_UNSUPPORTED, "%s: the FP32 form is differential attention (lambda != NULL)", fn);
+  sa_status st = check_shape(fn, B, H, L, d, SA_FP32, true);
+  if (st != SA_OK) return st;
+  if ((st = check_lambda(fn, lambda, H)) != SA_OK) return st;
+  return launch_attn_f32(h, q_rot, k_rot, v_t, out, B, H, L, window, lambda, stream);
 }
 
 sa_status sa_attn_set_timeout(sa_attn_t h, unsigned long long timeout_ns) {

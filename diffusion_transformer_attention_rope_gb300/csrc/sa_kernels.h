@@ -111,6 +111,43 @@ cudaError_t rope_side_launch(const RopeArgs& a, bool bf16, int blocks, cudaStrea
 // The (cos, sin) table alone (a.cs, [16][a.L] float4), with the pass's arithmetic.
 cudaError_t rope_table_launch(const RopeArgs& a, cudaStream_t stream);
 
+// FP32-input path (sa_tf32.cu): RoPE of q and k in FP32, results rounded to TF32.
+struct RopeF32Args {
+  const float* q;
+  const float* k;
+  float* q_out;
+  float* k_out;
+  const int32_t* positions;   // [L] or nullptr for 0..L-1
+  long long planes;           // B * H * 2 planes of L rows in q (and in k)
+  int L;
+  float inv_freq[kHeadDim / 2];
+  // v [planes_v][L][128] -> v_t [planes_v][128][L_pad] (TF32), or v == nullptr: no transpose
+  const float* v;
+  float* v_t;
+  long long planes_v;
+  int L_pad;                  // L rounded up to a multiple of 4 (16-byte rows)
+};
+
+// FP32-input differential attention (TF32 products): one CTA per (batch, head, 128-row block).
+struct FmhaF32Args {
+  float* out;                 // [B, H, L, 128]
+  int* err;
+  int L;
+  int H;
+  int n_qblocks;
+  int window;                 // < 0: full attention
+  float scale_log2;
+  unsigned long long timeout_ns;
+  float lambda[kMaxDiffHeads];
+};
+
+cudaError_t rope_f32_launch(const RopeF32Args& a, int num_sms, cudaStream_t stream);
+cudaError_t fmha_tf32_set_attributes();
+// false when the kernel's binary is not sm_103a code
+bool fmha_tf32_check(int* regs);
+cudaError_t fmha_tf32_launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const FmhaF32Args& a, long long num_ctas, cudaStream_t stream);
+
 cudaError_t fmha_set_attributes();
 // Registers per thread ptxas assigned to each attention kernel (must equal kFmhaLaunchRegs);
 // false also when a kernel's binary is not sm_103a code.

@@ -84,7 +84,10 @@ extern "C" sa_status sa_rope_attn_noalloc(sa_attn_t h, const void* q, const void
   // split region (one CTA per query block).
   const bool diff = lambda != nullptr;
   const size_t nqk = static_cast<size_t>(B) * H * (diff ? 2 : 1) * L * d;
-  const size_t need = 2 * round256(nqk * 2);
+  const size_t elem = dtype == SA_FP32 ? 4 : 2;
+  // the FP32 form also keeps a transposed copy of v (128 rows of L rounded up to 4 keys)
+  const size_t vt = dtype == SA_FP32 ? round256(static_cast<size_t>(B) * H * 2 * d * ((L + 3) & ~3) * 4) : 0;
+  const size_t need = 2 * round256(nqk * elem) + vt;
   if (need > kScratchBytes) {
     char msg[256];
     snprintf(msg, sizeof(msg),
@@ -98,5 +101,5 @@ extern "C" sa_status sa_rope_attn_noalloc(sa_attn_t h, const void* q, const void
   if (st != SA_OK) return st;
   unsigned char* ws = static_cast<unsigned char*>(base);
   return sa::rope_attn_into(fn, h, q, k, v, positions, out, B, H, L, d, window, lambda, dtype, ws,
-                            ws + round256(nqk * 2), stream);
+                            ws + round256(nqk * elem), stream);
 }

@@ -58,7 +58,13 @@ typedef struct sa_attn_s* sa_attn_t;
 /* The same type as cudaStream_t; NULL is the legacy default stream. */
 typedef struct CUstream_st* sa_stream_t;
 
-typedef enum { SA_FP16 = 0, SA_BF16 = 1 } sa_dtype;
+/* Element type of q, k, v and out.  SA_FP32 is the FP32-input form of SAME-L's
+ * differential sliding-window attention (HF discussion #6 "sm_120 SAME-L",
+ * "How the kernels differ": FP32 attention projections, both attention products
+ * as TF32 MMAs with FP32 accumulation); it is accepted by sa_rope_attn,
+ * sa_rope_attn_noalloc, sa_rope_qk and sa_attn_fwd for differential attention
+ * (lambda != NULL, two maps) and refused with SA_ERR_UNSUPPORTED elsewhere. */
+typedef enum { SA_FP16 = 0, SA_BF16 = 1, SA_FP32 = 2 } sa_dtype;
 
 typedef enum {
     SA_OK = 0,
@@ -99,6 +105,23 @@ SA_API sa_status sa_attn_destroy(sa_attn_t handle);
 SA_API size_t sa_rope_attn_workspace_size(int B, int H, int L, int d, int differential);
 
 /*
+ * Bytes of device workspace sa_rope_attn needs for this shape and element type.
+ * SA_FP16 / SA_BF16: sa_rope_attn_workspace_size.  SA_FP32 (differential only):
+ * the rotated q' and k' (B*H*2*L*d values of 4 bytes each), then v^T, the
+ * transposed v ([B*H][2d][L4] FP32 values, L4 = L rounded up to a multiple of
+ * 4), each rounded up to 256 bytes.  Returns 0 for invalid sizes or an
+ * unsupported combination.
+ */
+SA_API size_t sa_rope_attn_workspace_bytes(int B, int H, int L, int d, int differential, sa_dtype dtype);
+
+/*
+ * Bytes of device workspace sa_attn_fwd needs for this element type:
+ * sa_attn_fwd_workspace_size (optional) for SA_FP16 / SA_BF16; for SA_FP32 the
+ * v^T region of sa_rope_attn_workspace_bytes (required).  0 for invalid sizes.
+ */
+SA_API size_t sa_attn_fwd_workspace_bytes(int B, int H, int L, int d, int differential, sa_dtype dtype);
+
+/*
  * Bytes of the split region that sa_attn_fwd may be given: one 8-byte counter
  * per query block (256 rows standard, 128 differential) of every (batch,
  * head), rounded up to 256 bytes, then 160 FP32 partial-result slots of
@@ -137,10 +160,17 @@ SA_API size_t sa_attn_fwd_workspace_size(int B, int H, int L, int d, int differe
  *   window    < 0: full attention; >= 0: |i - j| <= window.
  *   lambda    host float[H] (H <= SA_MAX_DIFF_HEADS) or NULL.  Read during the
  *             call only (copied into the kernel arguments).
- *   dtype     SA_FP16 or SA_BF16 for q, k, v and out alike.
- *   workspace device scratch of at least sa_rope_attn_workspace_size bytes,
- *             16-byte aligned; contents on entry are ignored.  Calls that use
- *             the same workspace must be ordered on the GPU (same stream).
+ *   dtype     SA_FP16 or SA_BF16 for q, k, v and out alike; or SA_FP32 for
+ *             differential attention with FP32 q, k, v and out.  The FP32 form
+ *             rotates q and k in FP32 in one pass that also transposes v (q', k',
+ *             v^T in the workspace, each value rounded to TF32 to nearest, ties
+ *             away from zero), then runs both attention products as kind::tf32
+ *             MMAs (FP32 accumulate), the softmax and the lambda subtraction in
+ *             FP32, and writes FP32 out.
+ *   workspace device scratch of at least sa_rope_attn_workspace_bytes (for
+ *             dtype) bytes, 16-byte aligned; contents on entry are ignored.
+ *             Calls that use the same workspace must be ordered on the GPU
+ *             (same stream).
  *   stream    CUDA stream; the call is asynchronous with respect to the host.
  *
  * Errors: SA_ERR_INVALID_ARG, SA_ERR_UNSUPPORTED, SA_ERR_WORKSPACE from host
@@ -234,7 +264,9 @@ SA_API sa_status sa_rope_attn_qknorm(sa_attn_t handle,
  *
  * sa_rope_qk: q_rot = cast(RoPE_fp32(q)), k_rot = cast(RoPE_fp32(k)) for all
  *   B*H*nmaps planes of L rows (nmaps = 1 standard, 2 differential); q_rot and
- *   k_rot have the layout of q and k and must not overlap them.
+ *   k_rot have the layout of q and k and must not overlap them.  With SA_FP32
+ *   (nmaps = 2 only) the cast is the rounding to TF32 of sa_rope_attn's FP32
+ *   form and q_rot, k_rot hold FP32 values.
  */
 SA_API sa_status sa_rope_qk(sa_attn_t handle,
                             const void* q, const void* k,
@@ -300,6 +332,10 @@ SA_API sa_status sa_attn_fwd_rope_q(sa_attn_t handle,
  *   query block; otherwise it is a device split region (16-byte aligned) of at
  *   least sa_attn_fwd_workspace_size bytes (SA_ERR_WORKSPACE if smaller), and
  *   calls that use the same region must be ordered on the GPU (same stream).
+ *   With SA_FP32 (lambda != NULL only) the attention stage of sa_rope_attn's
+ *   FP32 form runs (TF32 products, one CTA per 128-row query block) after v
+ *   is transposed into the workspace, which is then required: at least
+ *   sa_attn_fwd_workspace_bytes bytes.
  */
 SA_API sa_status sa_attn_fwd(sa_attn_t handle,
                              const void* q_rot, const void* k_rot, const void* v,
@@ -312,9 +348,36 @@ SA_API sa_status sa_attn_fwd(sa_attn_t handle,
                              sa_stream_t stream);
 
 /*
+ * The two stages of sa_rope_attn's FP32 form (SA_FP32, differential only), for
+ * callers that want them apart.  Their composition has the bits of
+ * sa_rope_attn.
+ *
+ * sa_rope_qkv_f32: q_rot, k_rot = RoPE of q, k ([B, H, 2, L, d] FP32) in FP32,
+ *   rounded to TF32 (the layout of q and k); v_t = v ([B, H, L, 2d] FP32)
+ *   transposed to [B*H][2d][L4] (L4 = L rounded up to a multiple of 4; keys
+ *   L..L4-1 are zero), rounded to TF32.  All device, 16-byte aligned.
+ * sa_attn_fwd_f32: the TF32 attention kernel on q_rot, k_rot and v_t as
+ *   sa_rope_qkv_f32 leaves them; window and lambda as in sa_rope_attn.
+ */
+SA_API sa_status sa_rope_qkv_f32(sa_attn_t handle,
+                                 const void* q, const void* k, const void* v,
+                                 const int32_t* positions,
+                                 void* q_rot, void* k_rot, void* v_t,
+                                 int B, int H, int L, int d, sa_stream_t stream);
+
+SA_API sa_status sa_attn_fwd_f32(sa_attn_t handle,
+                                 const void* q_rot, const void* k_rot, const void* v_t,
+                                 void* out,
+                                 int B, int H, int L, int d,
+                                 int window,
+                                 const float* lambda,
+                                 sa_stream_t stream);
+
+/*
  * Size of the scratch array built into the library for sa_rope_attn_noalloc:
  * 64 MiB, enough for 2 * B*H*nmaps*L*64 two-byte elements up to that total
- * (every Stable Audio 3 shape here, up to B*H*nmaps*L = 262144 rows).
+ * (every Stable Audio 3 shape here, up to B*H*nmaps*L = 262144 rows; a third
+ * of that with SA_FP32, which also holds v^T).
  */
 #define SA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20)
 
@@ -339,9 +402,11 @@ SA_API sa_status sa_attn_fwd(sa_attn_t handle,
  * Arguments, layouts and errors are those of sa_rope_attn, checked in the same
  * order.  Then a shape is accepted only if q' and k' fit the array:
  *   2 * round_up_256(B * H * maps * L * 64 * 2) <= SA_NOALLOC_SCRATCH_BYTES
- * (maps = 2 for differential attention, else 1), that is at most 262,144
- * rows of 64 values (B * H * maps * L); a larger shape is rejected with
- * SA_ERR_WORKSPACE before anything is enqueued.
+ * (maps = 2 for differential attention, else 1), that is at most 262,144 rows
+ * of 64 values (B * H * maps * L).  SA_FP32 also keeps v^T there:
+ *   2 * round_up_256(B * H * 2 * L * 64 * 4)
+ *     + round_up_256(B * H * 128 * round_up_4(L) * 4) <= SA_NOALLOC_SCRATCH_BYTES.
+ * A larger shape is rejected with SA_ERR_WORKSPACE before anything is enqueued.
  */
 SA_API sa_status sa_rope_attn_noalloc(sa_attn_t handle,
                                       const void* q, const void* k, const void* v,
