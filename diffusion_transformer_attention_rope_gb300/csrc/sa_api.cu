@@ -73,14 +73,14 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-// 3-D tiled map over a [planes][rows][cols] array of 2-byte elements: box = 64 cols x 128 rows x
-// 1 plane, 128-byte swizzle (the layout the tcgen05 descriptors expect).  Rows past the end
-// of a plane read as zeros.
+// 3-D tiled map over a [planes][rows][cols] array of 2-byte elements: box = 64 cols x box_rows
+// rows x 1 plane, 128-byte swizzle (the layout the tcgen05 descriptors expect).  Rows past the
+// end of a plane read as zeros.
 bool encode_map(const sa_attn_s* h, CUtensorMap* m, const void* base, bool bf16, uint64_t cols,
-                uint64_t rows, uint64_t planes) {
+                uint64_t rows, uint64_t planes, uint32_t box_rows = sa::kBlockN) {
   const cuuint64_t dims[3] = {cols, rows, planes};
   const cuuint64_t strides[2] = {cols * 2, cols * 2 * rows};
-  const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(sa::kBlockN), 1};
+  const cuuint32_t box[3] = {64, box_rows, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = h->encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
                          3, const_cast<void*>(base), dims, strides, box, estr,
@@ -336,6 +336,42 @@ int side_sms(const sa_attn_s* h, long long ctas, long long k_bytes) {
   return static_cast<int>(idle);
 }
 
+// Differential attention with a window of at most kSwaMaxWindow: the narrow-window kernel, one
+// CTA per SM walking runs of query blocks (q rotated in its prologue with the table cs, or q'
+// rotated already when cs is nullptr).
+sa_status launch_attn_swa(const sa_attn_s* h, const void* q, const void* k_rot, const void* v, void* out, int B,
+                          int H, int L, int window, const float* lambda, bool bf16, sa_stream_t stream,
+                          const void* cs, int cs_stride, bool cs_static) {
+  const unsigned long long planes_qk = static_cast<unsigned long long>(B) * H * 2;
+  const unsigned long long planes_v = static_cast<unsigned long long>(B) * H;
+  CUtensorMap tm_q, tm_k, tm_v;
+  if (!encode_map(h, &tm_q, q, bf16, sa::kHeadDim, L, planes_qk, sa::kBlockM) ||
+      !encode_map(h, &tm_k, k_rot, bf16, sa::kHeadDim, L, planes_qk, 64) ||
+      !encode_map(h, &tm_v, v, bf16, 2 * sa::kHeadDim, L, planes_v, 64))
+    return fail(SA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor map");
+  DeviceGuard guard(h->device);
+  if (!guard.ok) return fail(SA_ERR_CUDA, "cannot select device %d", h->device);
+  sa::FmhaSwaArgs fa;
+  std::memset(&fa, 0, sizeof(fa));
+  fa.out = out;
+  fa.err = h->d_err;
+  fa.L = L;
+  fa.H = H;
+  fa.n_qblocks = (L + sa::kBlockM - 1) / sa::kBlockM;
+  fa.window = window;
+  fa.scale_log2 = static_cast<float>(1.4426950408889634 / std::sqrt(static_cast<double>(sa::kHeadDim)));
+  fa.timeout_ns = h->timeout_ns;
+  fa.units = static_cast<long long>(B) * H * fa.n_qblocks;
+  fa.cs = static_cast<const float2*>(cs);
+  fa.cs_stride = cs_stride > 0 ? cs_stride : L;
+  fa.cs_static = cs_static;
+  for (int i = 0; i < H; ++i) fa.lambda[i] = lambda[i];
+  const int ctas = static_cast<int>(std::min<long long>(fa.units, h->num_sms));
+  const cudaError_t e = sa::fmha_swa_launch(bf16, tm_q, tm_k, tm_v, fa, ctas, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return fail(SA_ERR_CUDA, "attention (narrow window) launch: %s", cudaGetErrorString(e));
+  return ok();
+}
+
 // cs == nullptr: q_rot is rotated already; else q_rot is the raw q and the kernel rotates it
 // in its prologue with the (cos, sin) table cs (row stride cs_stride, L if 0; cs_static: the
 // handle's table, which no kernel of this call writes).
@@ -349,6 +385,9 @@ sa_status launch_attn(const sa_attn_s* h, const void* q_rot, const void* k_rot, 
   const int dv = diff ? 2 * d : d;
   const unsigned long long planes_qk = static_cast<unsigned long long>(B) * H * (diff ? 2 : 1);
   const unsigned long long planes_v = static_cast<unsigned long long>(B) * H;
+  const int wnd = (window < 0 || window >= L - 1) ? -1 : window;
+  if (diff && wnd >= 0 && wnd <= sa::kSwaMaxWindow && nrm == nullptr)
+    return launch_attn_swa(h, q_rot, k_rot, v, out, B, H, L, wnd, lambda, bf16, stream, cs, cs_stride, cs_static);
   CUtensorMap tm_q, tm_k, tm_v;
   if (!encode_map(h, &tm_q, q_rot, bf16, d, L, planes_qk) ||
       !encode_map(h, &tm_k, k_rot, bf16, d, L, planes_qk) ||
@@ -581,14 +620,15 @@ sa_status sa_attn_create(sa_attn_t* handle, int device, float rope_base) {
   h->host_ready = create_host_streams(h);
   create_table(h);
   if ((e = cudaMemset(h->d_err, 0, sizeof(int))) != cudaSuccess ||
-      (e = sa::fmha_set_attributes()) != cudaSuccess || (e = sa::fmha_tf32_set_attributes()) != cudaSuccess) {
+      (e = sa::fmha_set_attributes()) != cudaSuccess || (e = sa::fmha_tf32_set_attributes()) != cudaSuccess ||
+      (e = sa::fmha_swa_set_attributes()) != cudaSuccess) {
     cudaFree(h->d_err);
     destroy_host_streams(h);
     delete h;
     return fail(SA_ERR_CUDA, "sa_attn_create: %s", cudaGetErrorString(e));
   }
   int regs = -1, regs_tf32 = -1;
-  if (!sa::fmha_check_registers(&regs) || !sa::fmha_tf32_check(&regs_tf32)) {
+  if (!sa::fmha_check_registers(&regs) || !sa::fmha_tf32_check(&regs_tf32) || !sa::fmha_swa_check()) {
     // The warpgroup register split (setmaxnreg) is sized for this launch allocation; any
     // other value could make the register grow wait forever, so refuse to run.
     cudaFree(h->d_err);

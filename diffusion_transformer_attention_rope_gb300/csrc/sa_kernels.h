@@ -148,6 +148,31 @@ bool fmha_tf32_check(int* regs);
 cudaError_t fmha_tf32_launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                              const FmhaF32Args& a, long long num_ctas, cudaStream_t stream);
 
+// Differential attention with a narrow window (sa_swa.cu): one CTA per SM walks a contiguous
+// run of 128-row query blocks (units); raw q is rotated in its prologue with the (cos, sin) table
+// (or taken as rotated already).
+constexpr int kSwaMaxWindow = 64;     // windows up to this width take this kernel
+struct FmhaSwaArgs {
+  void* out;                  // [B, H, L, 128]
+  int* err;
+  int L;
+  int H;
+  int n_qblocks;              // 128-row blocks per (batch, head)
+  int window;                 // 0 <= window <= kSwaMaxWindow
+  float scale_log2;
+  unsigned long long timeout_ns;
+  long long units;            // B * H * n_qblocks
+  const float2* cs;           // [16][cs_stride] float4 (cos, sin) table, or nullptr: q rotated already
+  int cs_stride;
+  int cs_static;              // the handle's table (no wait for the RoPE pass)
+  float lambda[kMaxDiffHeads];
+};
+
+cudaError_t fmha_swa_set_attributes();
+bool fmha_swa_check();
+cudaError_t fmha_swa_launch(bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FmhaSwaArgs& a, int num_ctas, cudaStream_t stream);
+
 cudaError_t fmha_set_attributes();
 // Registers per thread ptxas assigned to each attention kernel (must equal kFmhaLaunchRegs);
 // false also when a kernel's binary is not sm_103a code.

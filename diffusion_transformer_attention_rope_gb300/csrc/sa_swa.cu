@@ -1,0 +1,538 @@
+// sa_swa.cu -- differential attention with a narrow symmetric sliding window for sm_103a
+// (GB300): SAME-L's diff_attn_swa at its own window of +-17 (HF discussion #6 "sm_120 SAME-L",
+// "Three gotchas": a key tile much wider than the window is mostly masked-out waste, and the
+// kernel there is faster with small tiles).  Same result as the general attention kernel:
+//   out = softmax(q1' k1'^T / sqrt(d)) v - lambda_h * softmax(q2' k2'^T / sqrt(d)) v
+// over the keys |i - j| <= w, RoPE of q in the prologue (FP32, cast back), softmax in FP32, the
+// subtraction in FP32 on the FP32 accumulators.
+//
+// With a narrow window a query block touches only a few key tiles, so the general kernel's
+// fixed costs per CTA (setup, Q load and rotation, pipeline fill, drain, epilogue, relaunch)
+// outweigh its key loop.  Here one CTA per SM walks a contiguous run of query blocks (units):
+//   - 64-key tiles (the span of a 128-row block at +-17 is 162 keys: 3 tiles of 64 instead of 2
+//     of 128), S double-buffered per map in tensor memory and P (fp16/bf16) written over its S
+//     buffer, the A operand of a TS P.V MMA, so P never goes through shared memory;
+//   - Q double-buffered in shared memory: the next unit's raw Q arrives while this one runs;
+//   - the rings, S buffers and their barriers run on across units with a CTA-wide tile count;
+//     the first P.V of a unit (which overwrites O) waits until the previous epilogue has read O.
+// Warp roles as in the general kernel: warps 0-3 / 4-7 softmax of map 0 / 1 (thread = query row
+// = TMEM lane), warp 8 TMA of Q and the K ring, warp 9 TMEM allocation and MMA issuer of map 0,
+// warp 10 MMA issuer of map 1, warp 11 TMA of the V ring.
+// Tensor memory (512 columns): map m at 256 m: S buffer 0 | S buffer 1 | O = 64 | 64 | 128.
+// Shared memory: Q 2 x 32 KB, K ring 4 x 16 KB, V ring 4 x 16 KB.  Every wait is bounded.
+#include <cuda.h>
+
+#include "sa_kernels.h"
+#include "sa_pipe.cuh"
+#include "sa_ptx.cuh"
+
+namespace sa {
+namespace {
+
+constexpr int kBN = 64;                        // keys per tile
+constexpr int kQTile = kBlockM * kHeadDim * 2; // one map's 128 x 64 Q tile (16 KB, one atom)
+constexpr int kKMap = kBN * kHeadDim * 2;      // one map's 64 x 64 K tile (8 KB)
+constexpr int kNS = 4;                         // K and V ring stages
+constexpr int kQBuf = 2 * kQTile;              // both maps
+constexpr int kKStage = 2 * kKMap;             // both maps
+constexpr int kVStage = kBN * 2 * kHeadDim * 2;// 64 keys x 128 values (two 8 KB atoms)
+constexpr int kVAtom = kVStage / 2;
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + 2 * kQBuf;
+constexpr int kOffV = kOffK + kNS * kKStage;
+// barriers: q_full[2], q_ready[2][2], q_free[2], k_full[4], k_empty[4], v_full[4], v_empty[4],
+//           s_full[2][2], p_full[2][2], pv_done[2], o_full[2], o_free, drain[2], l_ready
+constexpr int kNBar = 2 + 4 + 2 + 4 * kNS + 4 + 4 + 2 + 2 + 1 + 2 + 1;
+constexpr int kOffBar = kOffV + kNS * kVStage;
+constexpr int kOffMisc = kOffBar + 8 * kNBar;  // tmem base, abort flag
+constexpr int kOffLsum = kOffMisc + 16;        // float [2 units][2 maps][128]
+constexpr int kSmemUsed = kOffLsum + 2 * 2 * kBlockM * 4;
+constexpr int kSmemAlloc = kSmemUsed + 1024;
+static_assert(kSmemAlloc <= 227 * 1024, "smem budget");
+constexpr int kTmaWarp = 8, kMmaWarp = 9, kTmaWarpV = 11;
+
+struct Bars {
+  uint32_t base;
+  __device__ uint32_t q_full(int b) const { return base + 8 * b; }
+  __device__ uint32_t q_ready(int b, int m) const { return base + 16 + 8 * (2 * b + m); }
+  __device__ uint32_t q_free(int b) const { return base + 48 + 8 * b; }
+  __device__ uint32_t k_full(int i) const { return base + 64 + 8 * i; }
+  __device__ uint32_t k_empty(int i) const { return base + 64 + 8 * kNS + 8 * i; }
+  __device__ uint32_t v_full(int i) const { return base + 64 + 16 * kNS + 8 * i; }
+  __device__ uint32_t v_empty(int i) const { return base + 64 + 24 * kNS + 8 * i; }
+  __device__ uint32_t s_full(int m, int b) const { return base + 64 + 32 * kNS + 8 * (2 * m + b); }
+  __device__ uint32_t p_full(int m, int b) const { return base + 96 + 32 * kNS + 8 * (2 * m + b); }
+  __device__ uint32_t pv_done(int m) const { return base + 128 + 32 * kNS + 8 * m; }
+  __device__ uint32_t o_full(int m) const { return base + 144 + 32 * kNS + 8 * m; }
+  __device__ uint32_t o_free() const { return base + 160 + 32 * kNS; }
+  __device__ uint32_t drain(int m) const { return base + 168 + 32 * kNS + 8 * m; }
+  // the epilogue's exchange of row sums between the two maps' warpgroups (an mbarrier, so that
+  // its wait is bounded like every other)
+  __device__ uint32_t l_ready() const { return base + 184 + 32 * kNS; }
+};
+static_assert(192 + 32 * kNS == 8 * kNBar, "barrier layout");
+
+__device__ __forceinline__ uint32_t s_col(int m, int b) { return 256 * m + 64 * b; }
+__device__ __forceinline__ uint32_t o_col(int m) { return 256 * m + 128; }
+
+// A unit (128 query rows of one (batch, head), both maps) and the key tiles it visits: the
+// window span [q0 - w, q_last + w] clipped to [0, L - 1], tiled from its first key.
+struct Unit {
+  int bh, q0, k_first, n_tiles;
+};
+
+__device__ __forceinline__ Unit unit_of(const FmhaSwaArgs& a, long long u) {
+  Unit x;
+  x.bh = static_cast<int>(u / a.n_qblocks);
+  x.q0 = static_cast<int>(u % a.n_qblocks) * kBlockM;
+  const int q_last = min(a.L, x.q0 + kBlockM) - 1;
+  x.k_first = max(0, x.q0 - a.window);
+  x.n_tiles = (min(a.L - 1, q_last + a.window) - x.k_first) / kBN + 1;
+  return x;
+}
+
+// O_m *= f in tensor memory (the lazy rescale; rare, out of line).
+__device__ __noinline__ void rescale_o128(uint32_t taddr, float f) {
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    uint32_t o[32];
+    tmem_ld32_nowait(taddr + 32 * cc, o);
+    tmem_wait_ld_32(o);
+#pragma unroll
+    for (int j = 0; j < 32; j += 2) {
+      const float2 v2 = fmul2(make_float2(__uint_as_float(o[j]), __uint_as_float(o[j + 1])), make_float2(f, f));
+      o[j] = __float_as_uint(v2.x);
+      o[j + 1] = __float_as_uint(v2.y);
+    }
+    tmem_st32(taddr + 32 * cc, o);
+  }
+}
+
+// RoPE of this thread's raw Q row in shared memory (128-byte-swizzled), with the (cos, sin)
+// table of the RoPE pass and its arithmetic (rope_rotate8), so that q' has the pass's bits.
+template <bool BF16>
+__device__ __noinline__ void rotate_q_row(const float2* cs, int cs_stride, int L, int grow, uint32_t row, int r) {
+  if (grow >= L) return;
+  float4 t[16];
+  const float4* cs4 = reinterpret_cast<const float4*>(cs) + grow;
+#pragma unroll
+  for (int m = 0; m < 16; ++m) t[m] = __ldg(cs4 + static_cast<size_t>(m) * cs_stride);
+  uint4 lo[4], hi[4];
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    lo[g] = ld_shared_v4(row + ((g ^ (r & 7)) << 4));
+    hi[g] = ld_shared_v4(row + (((g + 4) ^ (r & 7)) << 4));
+  }
+#pragma unroll
+  for (int g = 0; g < 4; ++g) {
+    float cg[8], sg[8];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      cg[2 * i] = t[4 * g + i].x;
+      sg[2 * i] = t[4 * g + i].y;
+      cg[2 * i + 1] = t[4 * g + i].z;
+      sg[2 * i + 1] = t[4 * g + i].w;
+    }
+    uint4 olo, ohi;
+    rope_rotate8<BF16>(lo[g], hi[g], cg, sg, olo, ohi);
+    st_shared_v4(row + ((g ^ (r & 7)) << 4), olo.x, olo.y, olo.z, olo.w);
+    st_shared_v4(row + (((g + 4) ^ (r & 7)) << 4), ohi.x, ohi.y, ohi.z, ohi.w);
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(kFmhaThreads, 1)
+    fmha_swa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FmhaSwaArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t sQ = sb + kOffQ, sK = sb + kOffK, sV = sb + kOffV;
+  Bars bar;
+  bar.base = sb + kOffBar;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kOffMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kOffMisc + 4);
+  float* lsum = reinterpret_cast<float*>(smem + kOffLsum);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int L = a.L;
+  // this CTA's run of units
+  const long long u_begin = static_cast<long long>(blockIdx.x) * a.units / gridDim.x;
+  const long long u_end = static_cast<long long>(blockIdx.x + 1) * a.units / gridDim.x;
+  const int n_units = static_cast<int>(u_end - u_begin);
+  const uint64_t tmo = a.timeout_ns;
+  const uint64_t drain_tmo = tmo > 1000000000ull ? tmo : 1000000000ull;
+
+  if (threadIdx.x == 0) {
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar.q_full(b), 1);
+      mbar_init(bar.q_ready(b, 0), 4);   // one elected arrival per softmax warp of the map
+      mbar_init(bar.q_ready(b, 1), 4);
+      mbar_init(bar.q_free(b), 2);       // one commit from each MMA issuer
+    }
+    for (int i = 0; i < kNS; ++i) {
+      mbar_init(bar.k_full(i), 1);
+      mbar_init(bar.k_empty(i), 2);
+      mbar_init(bar.v_full(i), 1);
+      mbar_init(bar.v_empty(i), 2);
+    }
+    for (int m = 0; m < 2; ++m) {
+      for (int b = 0; b < 2; ++b) {
+        mbar_init(bar.s_full(m, b), 1);
+        mbar_init(bar.p_full(m, b), 4);
+      }
+      mbar_init(bar.pv_done(m), 1);
+      mbar_init(bar.o_full(m), 1);
+      mbar_init(bar.drain(m), 1);
+    }
+    mbar_init(bar.o_free(), 8);          // every softmax warp, after the epilogue read O
+    mbar_init(bar.l_ready(), 8);         // every softmax warp, after writing its row sums
+    *abort_flag = 0;
+    mbar_fence_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == kTmaWarp && lane == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+  }
+  if (warp == kTmaWarpV && lane == 0) tma_prefetch_desc(&tm_v);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == kTmaWarp) {
+    // ---------------------------------------------------------------- Q and K producer
+    // raw q is the caller's; k' is the RoPE pass's output (programmatic dependent launch)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    int g = 0, issued = 0, q_issued = 0;
+    bool ok = true;
+    for (int ui = 0; ok && ui < n_units; ++ui) {
+      const Unit x = unit_of(a, u_begin + ui);
+      const int qb = ui & 1;
+      // the buffer's previous unit (ui - 2) must be done with it (its S MMAs have completed)
+      if (ui >= 2 && !pwait_w(bar.q_free(qb), ((ui >> 1) - 1) & 1, abort_flag, a.err, kErrProducer, tmo)) break;
+      q_issued = ui + 1;
+      mbar_arrive_expect_tx_w(bar.q_full(qb), kQBuf);
+      tma_load_3d_w(sQ + qb * kQBuf, &tm_q, bar.q_full(qb), 0, x.q0, 2 * x.bh);
+      tma_load_3d_w(sQ + qb * kQBuf + kQTile, &tm_q, bar.q_full(qb), 0, x.q0, 2 * x.bh + 1);
+      for (int t = 0; t < x.n_tiles; ++t, ++g) {
+        const int st = g % kNS;
+        if (!pwait_w(bar.k_empty(st), ((g / kNS) & 1) ^ 1, abort_flag, a.err, kErrProducer, tmo)) {
+          ok = false;
+          break;
+        }
+        const int key0 = x.k_first + t * kBN;
+        const uint32_t dst = sK + st * kKStage;
+        mbar_arrive_expect_tx_w(bar.k_full(st), kKStage);
+        tma_load_3d_w(dst, &tm_k, bar.k_full(st), 0, key0, 2 * x.bh);
+        tma_load_3d_w(dst + kKMap, &tm_k, bar.k_full(st), 0, key0, 2 * x.bh + 1);
+        issued = g + 1;
+      }
+    }
+    // copies still in flight land before the CTA's shared memory goes away
+    for (int i = issued > kNS ? issued - kNS : 0; i < issued; ++i)
+      mbar_wait_limit(bar.k_full(i % kNS), (i / kNS) & 1, drain_tmo);
+    for (int ui = q_issued > 2 ? q_issued - 2 : 0; ui < q_issued; ++ui)
+      mbar_wait_limit(bar.q_full(ui & 1), (ui >> 1) & 1, drain_tmo);
+    __syncwarp();
+  } else if (warp == kTmaWarpV) {
+    // ---------------------------------------------------------------- V producer
+    int g = 0, issued = 0;
+    bool ok = true;
+    for (int ui = 0; ok && ui < n_units; ++ui) {
+      const Unit x = unit_of(a, u_begin + ui);
+      for (int t = 0; t < x.n_tiles; ++t, ++g) {
+        const int st = g % kNS;
+        if (!pwait_w(bar.v_empty(st), ((g / kNS) & 1) ^ 1, abort_flag, a.err, kErrProducer, tmo)) {
+          ok = false;
+          break;
+        }
+        const int key0 = x.k_first + t * kBN;
+        const uint32_t dst = sV + st * kVStage;
+        mbar_arrive_expect_tx_w(bar.v_full(st), kVStage);
+        tma_load_3d_w(dst, &tm_v, bar.v_full(st), 0, key0, x.bh);
+        tma_load_3d_w(dst + kVAtom, &tm_v, bar.v_full(st), 64, key0, x.bh);
+        issued = g + 1;
+      }
+    }
+    for (int i = issued > kNS ? issued - kNS : 0; i < issued; ++i)
+      mbar_wait_limit(bar.v_full(i % kNS), (i / kNS) & 1, drain_tmo);
+    __syncwarp();
+  } else if (warp == kMmaWarp || warp == kMmaWarp + 1) {
+    // ---------------------------------------------------------------- MMA issuer of map m
+    const int m = warp - kMmaWarp;
+    constexpr uint32_t idesc_s = make_idesc_f16(kBlockM, kBN, BF16, false);
+    constexpr uint32_t idesc_o = make_idesc_f16(kBlockM, 2 * kHeadDim, BF16, true);
+    // K-major Q and K (one 128-byte atom per row: an MMA of K = 16 reads 32 bytes of it); V
+    // MN-major, its 128 values two atoms 8 KB apart, 8-key groups 1 KB apart.
+    const uint64_t dq0 = smem_desc_sw128(sQ + m * kQTile, 16, 1024);
+    const uint64_t dk0 = smem_desc_sw128(sK + m * kKMap, 16, 1024);
+    const uint64_t dv0 = smem_desc_sw128(sV, kVAtom, 1024);
+    const int eb = kErrMma;
+    auto issue_s = [&](int gg, uint64_t dq) {
+      const int st = gg % kNS;
+      const uint64_t dk = dk0 + static_cast<uint64_t>(st * (kKStage >> 4));
+      const uint32_t d = tmem + s_col(m, gg & 1);
+#pragma unroll
+      for (int kk = 0; kk < kHeadDim / 16; ++kk) umma_ss_w(d, dq + 2 * kk, dk + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
+      umma_commit_w(bar.s_full(m, gg & 1));
+      umma_commit_w(bar.k_empty(st));
+    };
+    int g = 0;
+    bool ok = true;
+    for (int ui = 0; ok && ui < n_units; ++ui) {
+      const Unit x = unit_of(a, u_begin + ui);
+      const int qb = ui & 1;
+      const uint64_t dq = dq0 + static_cast<uint64_t>(qb * (kQBuf >> 4));
+      const int n = x.n_tiles;
+      ok = pwait_w(bar.q_ready(qb, m), (ui >> 1) & 1, abort_flag, a.err, eb, tmo);
+      // both S buffers free: the previous unit's last P.V has read its P
+      if (ok && ui > 0) ok = pwait_w(bar.pv_done(m), (g - 1) & 1, abort_flag, a.err, eb, tmo);
+      if (ok) ok = pwait_w(bar.k_full(g % kNS), (g / kNS) & 1, abort_flag, a.err, eb, tmo);
+      if (!ok) break;
+      tc_fence_after();
+      issue_s(g, dq);
+      if (n > 1) {
+        ok = pwait_w(bar.k_full((g + 1) % kNS), ((g + 1) / kNS) & 1, abort_flag, a.err, eb, tmo);
+        if (!ok) break;
+        tc_fence_after();
+        issue_s(g + 1, dq);
+      }
+      for (int t = 0; t < n; ++t) {
+        const int gg = g + t;
+        const int sv = gg % kNS;
+        ok = pwait_w(bar.v_full(sv), (gg / kNS) & 1, abort_flag, a.err, eb, tmo) &&
+             pwait_w(bar.p_full(m, gg & 1), (gg >> 1) & 1, abort_flag, a.err, eb, tmo);
+        // the first P.V of a unit overwrites O: the previous unit's epilogue must have read it
+        if (ok && t == 0 && ui > 0) ok = pwait_w(bar.o_free(), (ui - 1) & 1, abort_flag, a.err, eb, tmo);
+        if (!ok) break;
+        tc_fence_after();
+        const uint64_t dv = dv0 + static_cast<uint64_t>(sv * (kVStage >> 4));
+        const uint32_t a_p = tmem + s_col(m, gg & 1);
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          umma_ts_w(tmem + o_col(m), a_p + 8 * kk, dv + 128 * kk, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
+        umma_commit_w(bar.pv_done(m));
+        umma_commit_w(bar.v_empty(sv));
+        if (t + 1 == n) {
+          umma_commit_w(bar.o_full(m));
+          umma_commit_w(bar.q_free(qb));
+        }
+        if (t + 2 < n) {
+          // S(gg + 2) goes into the buffer P(gg) occupies: after P.V(gg) has read it
+          ok = pwait_w(bar.pv_done(m), gg & 1, abort_flag, a.err, eb, tmo) &&
+               pwait_w(bar.k_full((gg + 2) % kNS), ((gg + 2) / kNS) & 1, abort_flag, a.err, eb, tmo);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(gg + 2, dq);
+        }
+      }
+      g += n;
+    }
+    umma_commit_w(bar.drain(m));
+    mbar_wait_limit(bar.drain(m), 0, drain_tmo);
+    __syncwarp();
+  } else if (warp < 8) {
+    // ---------------------------------------------------------------- softmax of map m
+    const int m = warp >> 2;
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const float c = a.scale_log2;
+    const float tau = 8.0f / c;
+    const int w = a.window;
+    // a per-call (cos, sin) table is the RoPE pass's output
+    if (!a.cs_static) asm volatile("griddepcontrol.wait;" ::: "memory");
+    int g = 0;
+    bool ok = true;
+    for (int ui = 0; ok && ui < n_units; ++ui) {
+      const Unit x = unit_of(a, u_begin + ui);
+      const int qb = ui & 1;
+      const int grow = x.q0 + r;
+      const int rows_lo = x.q0, rows_hi = x.q0 + kBlockM - 1;
+      // RoPE prologue of this row in the unit's Q buffer
+      ok = pwait(bar.q_full(qb), (ui >> 1) & 1, abort_flag, a.err, kErrSoftmax, tmo);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      if (a.cs != nullptr)
+        rotate_q_row<BF16>(a.cs, a.cs_stride, L, grow, sQ + qb * kQBuf + m * kQTile + r * 128, r);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.q_ready(qb, m));
+
+      float m_use = -INFINITY, l_sum = 0.0f;
+      for (int t = 0; t < x.n_tiles; ++t) {
+        const int gg = g + t;
+        const int b = gg & 1;
+        ok = pwait(bar.s_full(m, b), (gg >> 1) & 1, abort_flag, a.err, kErrSoftmax, tmo);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t sa = tmem + s_col(m, b) + lane_off;
+        uint32_t sr[kBN];
+        float mt;
+        tmem_ld64_max_nowait(sa, sr, mt);
+        tmem_wait_ld_64_max(sr, mt);
+        const int key0 = x.k_first + t * kBN;
+        const bool need_mask = (key0 + kBN > L) || !(key0 >= rows_hi - w && key0 + kBN - 1 <= rows_lo + w);
+        if (need_mask) {
+          // this row's keys are columns [j_lo, j_hi) of the tile; the loaded maximum also
+          // covers the masked columns, so the row max is taken again over the masked row
+          const int j_lo = grow - w - key0;
+          const int j_hi = min(L - key0, grow + w + 1 - key0);
+          mt = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < kBN; ++j) {
+            if (j < j_lo || j >= j_hi) sr[j] = __float_as_uint(-INFINITY);
+            mt = fmaxf(mt, __uint_as_float(sr[j]));
+          }
+        }
+        float f = 1.0f;
+        bool rescale = false;
+        if (t == 0) {
+          m_use = mt;
+        } else if (__any_sync(0xffffffffu, mt > m_use + tau)) {
+          const float m_new = fmaxf(m_use, mt);
+          f = (m_new == m_use) ? 1.0f : ex2_approx((m_use - m_new) * c);
+          m_use = m_new;
+          rescale = true;
+        }
+        const float mb = (m_use == -INFINITY) ? 0.0f : m_use * c;
+        const float2 c2 = make_float2(c, c), nmb2 = make_float2(-mb, -mb);
+        float2 sum0 = make_float2(0.0f, 0.0f), sum1 = make_float2(0.0f, 0.0f);
+        uint32_t pk[kBN / 2];
+#pragma unroll
+        for (int j = 0; j < kBN / 2; j += 2) {
+          const int e = 2 * j;
+          const float2 x0 = ffma2(make_float2(__uint_as_float(sr[e]), __uint_as_float(sr[e + 1])), c2, nmb2);
+          const float2 x1 = ffma2(make_float2(__uint_as_float(sr[e + 2]), __uint_as_float(sr[e + 3])), c2, nmb2);
+          const float2 p0 = make_float2(ex2_approx(x0.x), ex2_approx(x0.y));
+          const float2 p1 = make_float2(ex2_approx(x1.x), ex2_approx(x1.y));
+          sum0 = fadd2(sum0, p0);
+          sum1 = fadd2(sum1, p1);
+          pk[j] = pack2<BF16>(p0.x, p0.y);
+          pk[j + 1] = pack2<BF16>(p1.x, p1.y);
+        }
+        const float2 sum = fadd2(sum0, sum1);
+        l_sum = fmaf(l_sum, f, sum.x + sum.y);
+        if (rescale) {
+          // O_m is still written by P.V of the previous tile until it is done
+          ok = pwait(bar.pv_done(m), (gg - 1) & 1, abort_flag, a.err, kErrSoftmax, tmo);
+          ok = __all_sync(0xffffffffu, ok);
+          if (!ok) break;
+          tc_fence_after();
+          rescale_o128(tmem + o_col(m) + lane_off, f);
+        }
+        // P over S in this buffer (the A operand of P.V)
+        tmem_st32(sa, pk);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.p_full(m, b));
+      }
+      if (!ok) break;
+
+      // ---------------------------------------------------------------- epilogue of the unit
+      ok = pwait(bar.o_full(0), ui & 1, abort_flag, a.err, kErrSoftmax, tmo);
+      if (ok) ok = pwait(bar.o_full(1), ui & 1, abort_flag, a.err, kErrSoftmax, tmo);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      float* ls = lsum + (ui & 1) * 2 * kBlockM;
+      ls[m * kBlockM + r] = l_sum;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.l_ready());
+      ok = pwait(bar.l_ready(), ui & 1, abort_flag, a.err, kErrSoftmax, tmo);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      const float l0 = ls[r], l1 = ls[kBlockM + r];
+      const float inv0 = l0 > 0.0f ? 1.0f / l0 : 0.0f;
+      const float inv1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;
+      const float lam = a.lambda[x.bh % a.H];
+      uint16_t* dst = static_cast<uint16_t*>(a.out) +
+                      (static_cast<size_t>(x.bh) * L + grow) * static_cast<size_t>(2 * kHeadDim) + 64 * m;
+      // warpgroup m writes output columns [64 m, 64 m + 64)
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const uint32_t col = 64 * m + 32 * cc;
+        uint32_t o0[32], o1[32];
+        tmem_ld32_nowait(tmem + o_col(0) + lane_off + col, o0);
+        tmem_ld32_nowait(tmem + o_col(1) + lane_off + col, o1);
+        tmem_wait_ld_32(o0);
+        tmem_wait_ld_32(o1);
+        uint32_t pkd[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const float y0 = fmaf(-lam, __uint_as_float(o1[2 * j]) * inv1, __uint_as_float(o0[2 * j]) * inv0);
+          const float y1 = fmaf(-lam, __uint_as_float(o1[2 * j + 1]) * inv1, __uint_as_float(o0[2 * j + 1]) * inv0);
+          pkd[j] = pack2<BF16>(y0, y1);
+        }
+        if (grow < L) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * cc);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pkd[4 * j], pkd[4 * j + 1], pkd[4 * j + 2], pkd[4 * j + 3]);
+        }
+      }
+      // O has been read: the next unit's first P.V may overwrite it
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.o_free());
+      g += x.n_tiles;
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <bool BF16>
+cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FmhaSwaArgs& a,
+                   int num_ctas, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(num_ctas));
+  cfg.blockDim = dim3(kFmhaThreads);
+  cfg.dynamicSmemBytes = kSmemAlloc;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fmha_swa_kernel<BF16>, tq, tk, tv, a);
+}
+
+}  // namespace
+
+cudaError_t fmha_swa_set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(fmha_swa_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fmha_swa_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+  return e;
+}
+
+bool fmha_swa_check() {
+  for (const void* f : {reinterpret_cast<const void*>(fmha_swa_kernel<false>),
+                        reinterpret_cast<const void*>(fmha_swa_kernel<true>)}) {
+    cudaFuncAttributes attr;
+    if (cudaFuncGetAttributes(&attr, f) != cudaSuccess || attr.binaryVersion != 103) return false;
+  }
+  return true;
+}
+
+cudaError_t fmha_swa_launch(bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FmhaSwaArgs& a, int num_ctas, cudaStream_t stream) {
+  return bf16 ? launch<true>(tq, tk, tv, a, num_ctas, stream) : launch<false>(tq, tk, tv, a, num_ctas, stream);
+}
+
+}  // namespace sa
