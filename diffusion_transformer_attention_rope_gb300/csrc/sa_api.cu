@@ -344,10 +344,13 @@ sa_status launch_attn_swa(const sa_attn_s* h, const void* q, const void* k_rot, 
                           const void* cs, int cs_stride, bool cs_static) {
   const unsigned long long planes_qk = static_cast<unsigned long long>(B) * H * 2;
   const unsigned long long planes_v = static_cast<unsigned long long>(B) * H;
-  CUtensorMap tm_q, tm_k, tm_v;
+  CUtensorMap tm_q, tm_k, tm_v, tm_o;
+  if (!aligned16(out))
+    return fail(SA_ERR_INVALID_ARG, "out must be 16-byte aligned");
   if (!encode_map(h, &tm_q, q, bf16, sa::kHeadDim, L, planes_qk, sa::kBlockM) ||
       !encode_map(h, &tm_k, k_rot, bf16, sa::kHeadDim, L, planes_qk, 64) ||
-      !encode_map(h, &tm_v, v, bf16, 2 * sa::kHeadDim, L, planes_v, 64))
+      !encode_map(h, &tm_v, v, bf16, 2 * sa::kHeadDim, L, planes_v, 64) ||
+      !encode_map(h, &tm_o, out, bf16, 2 * sa::kHeadDim, L, planes_v, 32))
     return fail(SA_ERR_CUDA, "cuTensorMapEncodeTiled rejected a tensor map");
   DeviceGuard guard(h->device);
   if (!guard.ok) return fail(SA_ERR_CUDA, "cannot select device %d", h->device);
@@ -367,7 +370,8 @@ sa_status launch_attn_swa(const sa_attn_s* h, const void* q, const void* k_rot, 
   fa.cs_static = cs_static;
   for (int i = 0; i < H; ++i) fa.lambda[i] = lambda[i];
   const int ctas = static_cast<int>(std::min<long long>(fa.units, h->num_sms));
-  const cudaError_t e = sa::fmha_swa_launch(bf16, tm_q, tm_k, tm_v, fa, ctas, reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t e =
+      sa::fmha_swa_launch(bf16, tm_q, tm_k, tm_v, tm_o, fa, ctas, reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return fail(SA_ERR_CUDA, "attention (narrow window) launch: %s", cudaGetErrorString(e));
   return ok();
 }

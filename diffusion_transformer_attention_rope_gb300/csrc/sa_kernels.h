@@ -170,8 +170,9 @@ struct FmhaSwaArgs {
 
 cudaError_t fmha_swa_set_attributes();
 bool fmha_swa_check();
+// to: the output [B*H][L][128] (box 64 x 32 rows), written by the epilogue's TMA stores
 cudaError_t fmha_swa_launch(bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const FmhaSwaArgs& a, int num_ctas, cudaStream_t stream);
+                            const CUtensorMap& to, const FmhaSwaArgs& a, int num_ctas, cudaStream_t stream);
 
 cudaError_t fmha_set_attributes();
 // Registers per thread ptxas assigned to each attention kernel (must equal kFmhaLaunchRegs);

@@ -12,14 +12,20 @@
 //   - 64-key tiles (the span of a 128-row block at +-17 is 162 keys: 3 tiles of 64 instead of 2
 //     of 128), S double-buffered per map in tensor memory and P (fp16/bf16) written over its S
 //     buffer, the A operand of a TS P.V MMA, so P never goes through shared memory;
-//   - Q double-buffered in shared memory: the next unit's raw Q arrives while this one runs;
-//   - the rings, S buffers and their barriers run on across units with a CTA-wide tile count;
-//     the first P.V of a unit (which overwrites O) waits until the previous epilogue has read O.
+//   - Q double-buffered in shared memory: the next unit's raw Q arrives while this one runs,
+//     and the softmax warps rotate it right after this unit's last key tile, before this unit's
+//     epilogue, so the next unit's first S MMAs run while this unit's last P.V and epilogue do;
+//   - the rings, S buffers and their barriers run on across units with a CTA-wide tile count
+//     (the P.V completion is tracked per S buffer, so an S MMA waits only for the P.V that read
+//     its buffer); the first P.V of a unit (which overwrites O) waits until the previous
+//     epilogue has read O.
 // Warp roles as in the general kernel: warps 0-3 / 4-7 softmax of map 0 / 1 (thread = query row
 // = TMEM lane), warp 8 TMA of Q and the K ring, warp 9 TMEM allocation and MMA issuer of map 0,
 // warp 10 MMA issuer of map 1, warp 11 TMA of the V ring.
 // Tensor memory (512 columns): map m at 256 m: S buffer 0 | S buffer 1 | O = 64 | 64 | 128.
-// Shared memory: Q 2 x 32 KB, K ring 4 x 16 KB, V ring 4 x 16 KB.  Every wait is bounded.
+// Shared memory: Q 2 x 32 KB, K ring 3 x 16 KB, V ring 3 x 16 KB, output staging 32 KB (the
+// epilogue writes each warp's 32 x 64 block of the output with one TMA store, not as scattered
+// 16-byte stores of rows 256 bytes apart).  Every wait is bounded.
 #include <cuda.h>
 
 #include "sa_kernels.h"
@@ -32,7 +38,7 @@ namespace {
 constexpr int kBN = 64;                        // keys per tile
 constexpr int kQTile = kBlockM * kHeadDim * 2; // one map's 128 x 64 Q tile (16 KB, one atom)
 constexpr int kKMap = kBN * kHeadDim * 2;      // one map's 64 x 64 K tile (8 KB)
-constexpr int kNS = 4;                         // K and V ring stages
+constexpr int kNS = 3;                         // K and V ring stages
 constexpr int kQBuf = 2 * kQTile;              // both maps
 constexpr int kKStage = 2 * kKMap;             // both maps
 constexpr int kVStage = kBN * 2 * kHeadDim * 2;// 64 keys x 128 values (two 8 KB atoms)
@@ -40,10 +46,13 @@ constexpr int kVAtom = kVStage / 2;
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + 2 * kQBuf;
 constexpr int kOffV = kOffK + kNS * kKStage;
+// output staging for the epilogue's TMA stores: per softmax warp 32 rows x 64 values (4 KB)
+constexpr int kStageWarp = 32 * 128;
+constexpr int kOffStage = kOffV + kNS * kVStage;
 // barriers: q_full[2], q_ready[2][2], q_free[2], k_full[4], k_empty[4], v_full[4], v_empty[4],
-//           s_full[2][2], p_full[2][2], pv_done[2], o_full[2], o_free, drain[2], l_ready
-constexpr int kNBar = 2 + 4 + 2 + 4 * kNS + 4 + 4 + 2 + 2 + 1 + 2 + 1;
-constexpr int kOffBar = kOffV + kNS * kVStage;
+//           s_full[2][2], p_full[2][2], pv_done[2][2], o_full[2], o_free, drain[2], l_ready
+constexpr int kNBar = 2 + 4 + 2 + 4 * kNS + 4 + 4 + 4 + 2 + 1 + 2 + 1;
+constexpr int kOffBar = kOffStage + 8 * kStageWarp;
 constexpr int kOffMisc = kOffBar + 8 * kNBar;  // tmem base, abort flag
 constexpr int kOffLsum = kOffMisc + 16;        // float [2 units][2 maps][128]
 constexpr int kSmemUsed = kOffLsum + 2 * 2 * kBlockM * 4;
@@ -62,15 +71,16 @@ struct Bars {
   __device__ uint32_t v_empty(int i) const { return base + 64 + 24 * kNS + 8 * i; }
   __device__ uint32_t s_full(int m, int b) const { return base + 64 + 32 * kNS + 8 * (2 * m + b); }
   __device__ uint32_t p_full(int m, int b) const { return base + 96 + 32 * kNS + 8 * (2 * m + b); }
-  __device__ uint32_t pv_done(int m) const { return base + 128 + 32 * kNS + 8 * m; }
-  __device__ uint32_t o_full(int m) const { return base + 144 + 32 * kNS + 8 * m; }
-  __device__ uint32_t o_free() const { return base + 160 + 32 * kNS; }
-  __device__ uint32_t drain(int m) const { return base + 168 + 32 * kNS + 8 * m; }
+  // P.V completion of map m, per S buffer b (the P.V of tile g commits pv_done(m, g & 1))
+  __device__ uint32_t pv_done(int m, int b) const { return base + 128 + 32 * kNS + 8 * (2 * m + b); }
+  __device__ uint32_t o_full(int m) const { return base + 160 + 32 * kNS + 8 * m; }
+  __device__ uint32_t o_free() const { return base + 176 + 32 * kNS; }
+  __device__ uint32_t drain(int m) const { return base + 184 + 32 * kNS + 8 * m; }
   // the epilogue's exchange of row sums between the two maps' warpgroups (an mbarrier, so that
   // its wait is bounded like every other)
-  __device__ uint32_t l_ready() const { return base + 184 + 32 * kNS; }
+  __device__ uint32_t l_ready() const { return base + 200 + 32 * kNS; }
 };
-static_assert(192 + 32 * kNS == 8 * kNBar, "barrier layout");
+static_assert(208 + 32 * kNS == 8 * kNBar, "barrier layout");
 
 __device__ __forceinline__ uint32_t s_col(int m, int b) { return 256 * m + 64 * b; }
 __device__ __forceinline__ uint32_t o_col(int m) { return 256 * m + 128; }
@@ -81,14 +91,24 @@ struct Unit {
   int bh, q0, k_first, n_tiles;
 };
 
-__device__ __forceinline__ Unit unit_of(const FmhaSwaArgs& a, long long u) {
+__device__ __forceinline__ Unit unit_at(const FmhaSwaArgs& a, int bh, int q0) {
   Unit x;
-  x.bh = static_cast<int>(u / a.n_qblocks);
-  x.q0 = static_cast<int>(u % a.n_qblocks) * kBlockM;
-  const int q_last = min(a.L, x.q0 + kBlockM) - 1;
-  x.k_first = max(0, x.q0 - a.window);
+  x.bh = bh;
+  x.q0 = q0;
+  const int q_last = min(a.L, q0 + kBlockM) - 1;
+  x.k_first = max(0, q0 - a.window);
   x.n_tiles = (min(a.L - 1, q_last + a.window) - x.k_first) / kBN + 1;
   return x;
+}
+
+// Unit u (one 64-bit division, at the start of a run only).
+__device__ __forceinline__ Unit unit_of(const FmhaSwaArgs& a, long long u) {
+  return unit_at(a, static_cast<int>(u / a.n_qblocks), static_cast<int>(u % a.n_qblocks) * kBlockM);
+}
+
+// The unit after x in the run (the next query block, or the next (batch, head)'s first).
+__device__ __forceinline__ Unit next_unit(const FmhaSwaArgs& a, const Unit& x) {
+  return x.q0 + kBlockM < a.L ? unit_at(a, x.bh, x.q0 + kBlockM) : unit_at(a, x.bh + 1, 0);
 }
 
 // O_m *= f in tensor memory (the lazy rescale; rare, out of line).
@@ -143,7 +163,8 @@ __device__ __noinline__ void rotate_q_row(const float2* cs, int cs_stride, int L
 template <bool BF16>
 __global__ void __launch_bounds__(kFmhaThreads, 1)
     fmha_swa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ FmhaSwaArgs a) {
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const __grid_constant__ FmhaSwaArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~static_cast<uintptr_t>(1023));
@@ -183,7 +204,8 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         mbar_init(bar.s_full(m, b), 1);
         mbar_init(bar.p_full(m, b), 4);
       }
-      mbar_init(bar.pv_done(m), 1);
+      mbar_init(bar.pv_done(m, 0), 1);
+      mbar_init(bar.pv_done(m, 1), 1);
       mbar_init(bar.o_full(m), 1);
       mbar_init(bar.drain(m), 1);
     }
@@ -201,6 +223,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     tma_prefetch_desc(&tm_k);
   }
   if (warp == kTmaWarpV && lane == 0) tma_prefetch_desc(&tm_v);
+  if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_o);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -212,8 +235,8 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     int g = 0, issued = 0, q_issued = 0;
     bool ok = true;
-    for (int ui = 0; ok && ui < n_units; ++ui) {
-      const Unit x = unit_of(a, u_begin + ui);
+    Unit x = unit_of(a, u_begin);
+    for (int ui = 0; ok && ui < n_units; ++ui, x = next_unit(a, x)) {
       const int qb = ui & 1;
       // the buffer's previous unit (ui - 2) must be done with it (its S MMAs have completed)
       if (ui >= 2 && !pwait_w(bar.q_free(qb), ((ui >> 1) - 1) & 1, abort_flag, a.err, kErrProducer, tmo)) break;
@@ -245,8 +268,8 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     // ---------------------------------------------------------------- V producer
     int g = 0, issued = 0;
     bool ok = true;
-    for (int ui = 0; ok && ui < n_units; ++ui) {
-      const Unit x = unit_of(a, u_begin + ui);
+    Unit x = unit_of(a, u_begin);
+    for (int ui = 0; ok && ui < n_units; ++ui, x = next_unit(a, x)) {
       for (int t = 0; t < x.n_tiles; ++t, ++g) {
         const int st = g % kNS;
         if (!pwait_w(bar.v_empty(st), ((g / kNS) & 1) ^ 1, abort_flag, a.err, kErrProducer, tmo)) {
@@ -286,20 +309,21 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     };
     int g = 0;
     bool ok = true;
-    for (int ui = 0; ok && ui < n_units; ++ui) {
-      const Unit x = unit_of(a, u_begin + ui);
+    Unit x = unit_of(a, u_begin);
+    for (int ui = 0; ok && ui < n_units; ++ui, x = next_unit(a, x)) {
       const int qb = ui & 1;
       const uint64_t dq = dq0 + static_cast<uint64_t>(qb * (kQBuf >> 4));
       const int n = x.n_tiles;
       ok = pwait_w(bar.q_ready(qb, m), (ui >> 1) & 1, abort_flag, a.err, eb, tmo);
-      // both S buffers free: the previous unit's last P.V has read its P
-      if (ok && ui > 0) ok = pwait_w(bar.pv_done(m), (g - 1) & 1, abort_flag, a.err, eb, tmo);
+      // S(g) goes into the buffer of tile g - 2: after that tile's P.V has read its P
+      if (ok && g >= 2) ok = pwait_w(bar.pv_done(m, g & 1), ((g - 2) >> 1) & 1, abort_flag, a.err, eb, tmo);
       if (ok) ok = pwait_w(bar.k_full(g % kNS), (g / kNS) & 1, abort_flag, a.err, eb, tmo);
       if (!ok) break;
       tc_fence_after();
       issue_s(g, dq);
       if (n > 1) {
-        ok = pwait_w(bar.k_full((g + 1) % kNS), ((g + 1) / kNS) & 1, abort_flag, a.err, eb, tmo);
+        ok = (g < 1 || pwait_w(bar.pv_done(m, (g + 1) & 1), ((g - 1) >> 1) & 1, abort_flag, a.err, eb, tmo)) &&
+             pwait_w(bar.k_full((g + 1) % kNS), ((g + 1) / kNS) & 1, abort_flag, a.err, eb, tmo);
         if (!ok) break;
         tc_fence_after();
         issue_s(g + 1, dq);
@@ -318,7 +342,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           umma_ts_w(tmem + o_col(m), a_p + 8 * kk, dv + 128 * kk, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
-        umma_commit_w(bar.pv_done(m));
+        umma_commit_w(bar.pv_done(m, gg & 1));
         umma_commit_w(bar.v_empty(sv));
         if (t + 1 == n) {
           umma_commit_w(bar.o_full(m));
@@ -326,7 +350,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         }
         if (t + 2 < n) {
           // S(gg + 2) goes into the buffer P(gg) occupies: after P.V(gg) has read it
-          ok = pwait_w(bar.pv_done(m), gg & 1, abort_flag, a.err, eb, tmo) &&
+          ok = pwait_w(bar.pv_done(m, gg & 1), (gg >> 1) & 1, abort_flag, a.err, eb, tmo) &&
                pwait_w(bar.k_full((gg + 2) % kNS), ((gg + 2) / kNS) & 1, abort_flag, a.err, eb, tmo);
           if (!ok) break;
           tc_fence_after();
@@ -349,22 +373,26 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     const int w = a.window;
     // a per-call (cos, sin) table is the RoPE pass's output
     if (!a.cs_static) asm volatile("griddepcontrol.wait;" ::: "memory");
-    int g = 0;
-    bool ok = true;
-    for (int ui = 0; ok && ui < n_units; ++ui) {
-      const Unit x = unit_of(a, u_begin + ui);
+    // RoPE prologue of this row of unit ui's Q (in its buffer), then the unit's Q goes to the
+    // map's MMA issuer
+    auto q_prologue = [&](int ui, const Unit& y) {
       const int qb = ui & 1;
-      const int grow = x.q0 + r;
-      const int rows_lo = x.q0, rows_hi = x.q0 + kBlockM - 1;
-      // RoPE prologue of this row in the unit's Q buffer
-      ok = pwait(bar.q_full(qb), (ui >> 1) & 1, abort_flag, a.err, kErrSoftmax, tmo);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
+      bool good = pwait(bar.q_full(qb), (ui >> 1) & 1, abort_flag, a.err, kErrSoftmax, tmo);
+      good = __all_sync(0xffffffffu, good);
+      if (!good) return false;
       if (a.cs != nullptr)
-        rotate_q_row<BF16>(a.cs, a.cs_stride, L, grow, sQ + qb * kQBuf + m * kQTile + r * 128, r);
+        rotate_q_row<BF16>(a.cs, a.cs_stride, L, y.q0 + r, sQ + qb * kQBuf + m * kQTile + r * 128, r);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.q_ready(qb, m));
+      return true;
+    };
+    int g = 0;
+    Unit x = unit_of(a, u_begin);
+    bool ok = n_units > 0 ? q_prologue(0, x) : true;
+    for (int ui = 0; ok && ui < n_units; ++ui, x = next_unit(a, x)) {
+      const int grow = x.q0 + r;
+      const int rows_lo = x.q0, rows_hi = x.q0 + kBlockM - 1;
 
       float m_use = -INFINITY, l_sum = 0.0f;
       for (int t = 0; t < x.n_tiles; ++t) {
@@ -386,12 +414,19 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
           // covers the masked columns, so the row max is taken again over the masked row
           const int j_lo = grow - w - key0;
           const int j_hi = min(L - key0, grow + w + 1 - key0);
-          mt = -INFINITY;
 #pragma unroll
-          for (int j = 0; j < kBN; ++j) {
+          for (int j = 0; j < kBN; ++j)
             if (j < j_lo || j >= j_hi) sr[j] = __float_as_uint(-INFINITY);
-            mt = fmaxf(mt, __uint_as_float(sr[j]));
+          // 8 independent chains; chain q covers elements q, q + 8, ..., q + 56
+          float mx[8];
+#pragma unroll
+          for (int q = 0; q < 8; ++q) mx[q] = fmaxf(__uint_as_float(sr[q]), __uint_as_float(sr[q + 8]));
+#pragma unroll
+          for (int j = 16; j < kBN; j += 16) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) mx[q] = fmax3(mx[q], __uint_as_float(sr[j + q]), __uint_as_float(sr[j + 8 + q]));
           }
+          mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
         }
         float f = 1.0f;
         bool rescale = false;
@@ -423,7 +458,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         l_sum = fmaf(l_sum, f, sum.x + sum.y);
         if (rescale) {
           // O_m is still written by P.V of the previous tile until it is done
-          ok = pwait(bar.pv_done(m), (gg - 1) & 1, abort_flag, a.err, kErrSoftmax, tmo);
+          ok = pwait(bar.pv_done(m, (gg - 1) & 1), ((gg - 1) >> 1) & 1, abort_flag, a.err, kErrSoftmax, tmo);
           ok = __all_sync(0xffffffffu, ok);
           if (!ok) break;
           tc_fence_after();
@@ -437,6 +472,11 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         if (lane == 0) mbar_arrive(bar.p_full(m, b));
       }
       if (!ok) break;
+      // the next unit's Q now, so that its first S MMAs overlap this unit's last P.V and epilogue
+      if (ui + 1 < n_units && !q_prologue(ui + 1, next_unit(a, x))) {
+        ok = false;
+        break;
+      }
 
       // ---------------------------------------------------------------- epilogue of the unit
       ok = pwait(bar.o_full(0), ui & 1, abort_flag, a.err, kErrSoftmax, tmo);
@@ -455,9 +495,11 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       const float inv0 = l0 > 0.0f ? 1.0f / l0 : 0.0f;
       const float inv1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;
       const float lam = a.lambda[x.bh % a.H];
-      uint16_t* dst = static_cast<uint16_t*>(a.out) +
-                      (static_cast<size_t>(x.bh) * L + grow) * static_cast<size_t>(2 * kHeadDim) + 64 * m;
-      // warpgroup m writes output columns [64 m, 64 m + 64)
+      // warpgroup m writes output columns [64 m, 64 m + 64): this warp's 32 rows go through its
+      // staging block (128-byte swizzle: 16-byte chunk c of row i at c ^ (i & 7)) and one TMA store
+      const uint32_t stage = sb + kOffStage + warp * kStageWarp + lane * 128;
+      if (lane == 0) bulk_wait_read();   // the previous unit's store has read the block
+      __syncwarp();
 #pragma unroll
       for (int cc = 0; cc < 2; ++cc) {
         const uint32_t col = 64 * m + 32 * cc;
@@ -473,18 +515,26 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
           const float y1 = fmaf(-lam, __uint_as_float(o1[2 * j + 1]) * inv1, __uint_as_float(o0[2 * j + 1]) * inv0);
           pkd[j] = pack2<BF16>(y0, y1);
         }
-        if (grow < L) {
-          uint4* d4 = reinterpret_cast<uint4*>(dst + 32 * cc);
 #pragma unroll
-          for (int j = 0; j < 4; ++j) d4[j] = make_uint4(pkd[4 * j], pkd[4 * j + 1], pkd[4 * j + 2], pkd[4 * j + 3]);
-        }
+        for (int j = 0; j < 4; ++j)
+          st_shared_v4(stage + (((4 * cc + j) ^ (lane & 7)) << 4), pkd[4 * j], pkd[4 * j + 1], pkd[4 * j + 2],
+                       pkd[4 * j + 3]);
       }
       // O has been read: the next unit's first P.V may overwrite it
       tc_fence_before();
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar.o_free());
+      if (lane == 0) {
+        mbar_arrive(bar.o_free());
+        // rows past L are outside the tensor and not written
+        tma_store_3d(&tm_o, sb + kOffStage + warp * kStageWarp, 64 * m, x.q0 + 32 * quarter, x.bh);
+        bulk_commit();
+      }
       g += x.n_tiles;
     }
+    // the output stores complete before the CTA's shared memory goes away
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   // ---------------------------------------------------------------- teardown
@@ -497,8 +547,8 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
 }
 
 template <bool BF16>
-cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FmhaSwaArgs& a,
-                   int num_ctas, cudaStream_t stream) {
+cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
+                   const FmhaSwaArgs& a, int num_ctas, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(num_ctas));
   cfg.blockDim = dim3(kFmhaThreads);
@@ -509,7 +559,7 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fmha_swa_kernel<BF16>, tq, tk, tv, a);
+  return cudaLaunchKernelEx(&cfg, fmha_swa_kernel<BF16>, tq, tk, tv, to, a);
 }
 
 }  // namespace
@@ -531,8 +581,8 @@ bool fmha_swa_check() {
 }
 
 cudaError_t fmha_swa_launch(bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const FmhaSwaArgs& a, int num_ctas, cudaStream_t stream) {
-  return bf16 ? launch<true>(tq, tk, tv, a, num_ctas, stream) : launch<false>(tq, tk, tv, a, num_ctas, stream);
+                            const CUtensorMap& to, const FmhaSwaArgs& a, int num_ctas, cudaStream_t stream) {
+  return bf16 ? launch<true>(tq, tk, tv, to, a, num_ctas, stream) : launch<false>(tq, tk, tv, to, a, num_ctas, stream);
 }
 
 }  // namespace sa
