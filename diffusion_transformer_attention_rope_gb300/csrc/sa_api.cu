@@ -341,7 +341,7 @@ int side_sms(const sa_attn_s* h, long long ctas, long long k_bytes) {
 // rotated already when cs is nullptr).
 sa_status launch_attn_swa(const sa_attn_s* h, const void* q, const void* k_rot, const void* v, void* out, int B,
                           int H, int L, int window, const float* lambda, bool bf16, sa_stream_t stream,
-                          const void* cs, int cs_stride, bool cs_static) {
+                          const void* cs, int cs_stride, bool cs_static, const QkNorm* nrm) {
   const unsigned long long planes_qk = static_cast<unsigned long long>(B) * H * 2;
   const unsigned long long planes_v = static_cast<unsigned long long>(B) * H;
   CUtensorMap tm_q, tm_k, tm_v, tm_o;
@@ -369,6 +369,9 @@ sa_status launch_attn_swa(const sa_attn_s* h, const void* q, const void* k_rot, 
   fa.cs_stride = cs_stride > 0 ? cs_stride : L;
   fa.cs_static = cs_static;
   for (int i = 0; i < H; ++i) fa.lambda[i] = lambda[i];
+  fa.qk_norm = nrm != nullptr;   // (with cs: the prologue normalises each raw q row)
+  fa.eps = nrm ? nrm->eps : 0.0f;
+  for (int i = 0; i < sa::kHeadDim; ++i) fa.gamma_q[i] = nrm ? nrm->gamma_q[i] : 1.0f;
   const int ctas = static_cast<int>(std::min<long long>(fa.units, h->num_sms));
   const cudaError_t e =
       sa::fmha_swa_launch(bf16, tm_q, tm_k, tm_v, tm_o, fa, ctas, reinterpret_cast<cudaStream_t>(stream));
@@ -390,8 +393,9 @@ sa_status launch_attn(const sa_attn_s* h, const void* q_rot, const void* k_rot, 
   const unsigned long long planes_qk = static_cast<unsigned long long>(B) * H * (diff ? 2 : 1);
   const unsigned long long planes_v = static_cast<unsigned long long>(B) * H;
   const int wnd = (window < 0 || window >= L - 1) ? -1 : window;
-  if (diff && wnd >= 0 && wnd <= sa::kSwaMaxWindow && nrm == nullptr)
-    return launch_attn_swa(h, q_rot, k_rot, v, out, B, H, L, wnd, lambda, bf16, stream, cs, cs_stride, cs_static);
+  if (diff && wnd >= 0 && wnd <= sa::kSwaMaxWindow)
+    return launch_attn_swa(h, q_rot, k_rot, v, out, B, H, L, wnd, lambda, bf16, stream, cs, cs_stride, cs_static,
+                           nrm);
   CUtensorMap tm_q, tm_k, tm_v;
   if (!encode_map(h, &tm_q, q_rot, bf16, d, L, planes_qk) ||
       !encode_map(h, &tm_k, k_rot, bf16, d, L, planes_qk) ||

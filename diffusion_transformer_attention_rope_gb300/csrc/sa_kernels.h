@@ -151,7 +151,8 @@ cudaError_t fmha_tf32_launch(const CUtensorMap& tq, const CUtensorMap& tk, const
 // Differential attention with a narrow window (sa_swa.cu): one CTA per SM walks a contiguous
 // run of 128-row query blocks (units); raw q is rotated in its prologue with the (cos, sin) table
 // (or taken as rotated already).
-constexpr int kSwaMaxWindow = 64;     // windows up to this width take this kernel
+constexpr int kSwaMaxWindow = 256;    // windows up to this width take this kernel (measured faster
+                                      // than the general one at 17 and 256, slower without a window)
 struct FmhaSwaArgs {
   void* out;                  // [B, H, L, 128]
   int* err;
@@ -166,6 +167,10 @@ struct FmhaSwaArgs {
   int cs_stride;
   int cs_static;              // the handle's table (no wait for the RoPE pass)
   float lambda[kMaxDiffHeads];
+  // QK-RMSNorm of each raw q row in the prologue (cs != nullptr only)
+  int qk_norm;
+  float eps;
+  float gamma_q[kHeadDim];
 };
 
 cudaError_t fmha_swa_set_attributes();

@@ -3,8 +3,8 @@
 // "Three gotchas": a key tile much wider than the window is mostly masked-out waste, and the
 // kernel there is faster with small tiles).  Same result as the general attention kernel:
 //   out = softmax(q1' k1'^T / sqrt(d)) v - lambda_h * softmax(q2' k2'^T / sqrt(d)) v
-// over the keys |i - j| <= w, RoPE of q in the prologue (FP32, cast back), softmax in FP32, the
-// subtraction in FP32 on the FP32 accumulators.
+// over the keys |i - j| <= w, RoPE of q in the prologue (FP32, cast back; after the QK-RMSNorm
+// when one is asked for), softmax in FP32, the subtraction in FP32 on the FP32 accumulators.
 //
 // With a narrow window a query block touches only a few key tiles, so the general kernel's
 // fixed costs per CTA (setup, Q load and rotation, pipeline fill, drain, epilogue, relaunch)
@@ -129,9 +129,11 @@ __device__ __noinline__ void rescale_o128(uint32_t taddr, float f) {
 }
 
 // RoPE of this thread's raw Q row in shared memory (128-byte-swizzled), with the (cos, sin)
-// table of the RoPE pass and its arithmetic (rope_rotate8), so that q' has the pass's bits.
-template <bool BF16>
-__device__ __noinline__ void rotate_q_row(const float2* cs, int cs_stride, int L, int grow, uint32_t row, int r) {
+// table of the RoPE pass and its arithmetic (rope_rotate8), so that q' has the pass's bits; with
+// NORM the row is QK-RMS-normalised first, with the pass's sum order and scaling.
+template <bool BF16, bool NORM>
+__device__ __noinline__ void rotate_q_row(const float2* cs, int cs_stride, int L, int grow, uint32_t row, int r,
+                                          const float* gamma, float eps) {
   if (grow >= L) return;
   float4 t[16];
   const float4* cs4 = reinterpret_cast<const float4*>(cs) + grow;
@@ -142,6 +144,13 @@ __device__ __noinline__ void rotate_q_row(const float2* cs, int cs_stride, int L
   for (int g = 0; g < 4; ++g) {
     lo[g] = ld_shared_v4(row + ((g ^ (r & 7)) << 4));
     hi[g] = ld_shared_v4(row + (((g + 4) ^ (r & 7)) << 4));
+  }
+  float inv = 1.0f;
+  if (NORM) {
+    float tg[4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g) tg[g] = sumsq8<BF16>(lo[g]) + sumsq8<BF16>(hi[g]);
+    inv = qknorm_inv_rms((tg[0] + tg[1]) + (tg[2] + tg[3]), eps);
   }
 #pragma unroll
   for (int g = 0; g < 4; ++g) {
@@ -154,13 +163,24 @@ __device__ __noinline__ void rotate_q_row(const float2* cs, int cs_stride, int L
       sg[2 * i + 1] = t[4 * g + i].w;
     }
     uint4 olo, ohi;
-    rope_rotate8<BF16>(lo[g], hi[g], cg, sg, olo, ohi);
+    if (NORM) {
+      float sl[8], sh[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        sl[i] = __fmul_rn(inv, gamma[8 * g + i]);
+        sh[i] = __fmul_rn(inv, gamma[32 + 8 * g + i]);
+      }
+      rope_rotate8_scaled<BF16>(lo[g], hi[g], cg, sg, sl, sh, olo, ohi);
+    } else {
+      rope_rotate8<BF16>(lo[g], hi[g], cg, sg, olo, ohi);
+    }
     st_shared_v4(row + ((g ^ (r & 7)) << 4), olo.x, olo.y, olo.z, olo.w);
     st_shared_v4(row + (((g + 4) ^ (r & 7)) << 4), ohi.x, ohi.y, ohi.z, ohi.w);
   }
 }
 
-template <bool BF16>
+// NORM: the QK-RMSNorm form (a kernel of its own, so that the plain one carries none of its code)
+template <bool BF16, bool NORM>
 __global__ void __launch_bounds__(kFmhaThreads, 1)
     fmha_swa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -381,7 +401,8 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       good = __all_sync(0xffffffffu, good);
       if (!good) return false;
       if (a.cs != nullptr)
-        rotate_q_row<BF16>(a.cs, a.cs_stride, L, y.q0 + r, sQ + qb * kQBuf + m * kQTile + r * 128, r);
+        rotate_q_row<BF16, NORM>(a.cs, a.cs_stride, L, y.q0 + r, sQ + qb * kQBuf + m * kQTile + r * 128, r,
+                                 a.gamma_q, a.eps);
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) mbar_arrive(bar.q_ready(qb, m));
@@ -546,7 +567,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
   }
 }
 
-template <bool BF16>
+template <bool BF16, bool NORM>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& to,
                    const FmhaSwaArgs& a, int num_ctas, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -559,21 +580,25 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, fmha_swa_kernel<BF16>, tq, tk, tv, to, a);
+  return cudaLaunchKernelEx(&cfg, fmha_swa_kernel<BF16, NORM>, tq, tk, tv, to, a);
 }
 
 }  // namespace
 
+const void* const kSwaKernels[4] = {
+    reinterpret_cast<const void*>(fmha_swa_kernel<false, false>), reinterpret_cast<const void*>(fmha_swa_kernel<true, false>),
+    reinterpret_cast<const void*>(fmha_swa_kernel<false, true>), reinterpret_cast<const void*>(fmha_swa_kernel<true, true>)};
+
 cudaError_t fmha_swa_set_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(fmha_swa_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(fmha_swa_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
-  return e;
+  for (const void* f : kSwaKernels) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 bool fmha_swa_check() {
-  for (const void* f : {reinterpret_cast<const void*>(fmha_swa_kernel<false>),
-                        reinterpret_cast<const void*>(fmha_swa_kernel<true>)}) {
+  for (const void* f : kSwaKernels) {
     cudaFuncAttributes attr;
     if (cudaFuncGetAttributes(&attr, f) != cudaSuccess || attr.binaryVersion != 103) return false;
   }
@@ -582,7 +607,11 @@ bool fmha_swa_check() {
 
 cudaError_t fmha_swa_launch(bool bf16, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& to, const FmhaSwaArgs& a, int num_ctas, cudaStream_t stream) {
-  return bf16 ? launch<true>(tq, tk, tv, to, a, num_ctas, stream) : launch<false>(tq, tk, tv, to, a, num_ctas, stream);
+  if (a.qk_norm)
+    return bf16 ? launch<true, true>(tq, tk, tv, to, a, num_ctas, stream)
+                : launch<false, true>(tq, tk, tv, to, a, num_ctas, stream);
+  return bf16 ? launch<true, false>(tq, tk, tv, to, a, num_ctas, stream)
+              : launch<false, false>(tq, tk, tv, to, a, num_ctas, stream);
 }
 
 }  // namespace sa
