@@ -90,25 +90,39 @@ def load_peaks():
         return {"hbm_gbs": 6800.0, "tflops": 1900.0, "tflops_sustained": 1700.0, "source": "fallback"}
 
 
-def kernel_sha() -> str:
-    """Hash of the attention kernel's source with comments and blank lines removed, so that the
-    stored ncu counters stay valid across comment-only edits and no others."""
+# Differential windows up to this width run the narrow-window kernel (the library's rule).
+SWA_MAX_WINDOW = 256
+
+
+def kernel_source(w=None) -> str:
+    """Source file of the attention kernel a workload runs: the FP32-input (TF32) kernel, the
+    narrow-window differential kernel, or the general one."""
+    if w is not None and w.dtype == "fp32":
+        return "sa_tf32.cu"
+    if w is not None and w.nmaps == 2 and 0 <= w.window <= SWA_MAX_WINDOW and w.window < w.L - 1:
+        return "sa_swa.cu"
+    return "sa_fmha.cu"
+
+
+def kernel_sha(w=None) -> str:
+    """Hash of the workload's attention kernel source with comments and blank lines removed, so
+    that the stored ncu counters stay valid across comment-only edits and no others."""
     import hashlib
     import re
 
-    path = os.path.join(ROOT, "diffusion_transformer_attention_rope_gb300", "csrc", "sa_fmha.cu")
+    path = os.path.join(ROOT, "diffusion_transformer_attention_rope_gb300", "csrc", kernel_source(w))
     code = [re.sub(r"\s*//.*$", "", ln).rstrip() for ln in open(path).read().splitlines()]
     return hashlib.sha256("\n".join(ln for ln in code if ln).encode()).hexdigest()[:16]
 
 
-def load_traffic(workload: str):
+def load_traffic(w):
     """DRAM bytes per attention launch from the committed ncu summary, or None when no
     capture exists for this workload or the kernel source changed since it was taken."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            t = json.load(f).get(workload)
-        if t and t.get("kernel_sha") == kernel_sha():
+            t = json.load(f).get(w.name)
+        if t and t.get("kernel_sha") == kernel_sha(w):
             return t["bytes"]
     except Exception:
         pass
@@ -568,11 +582,11 @@ def measure(args, w, dist, world, rank, local, device, cpu_budget):
         "frac_of_peak": value / world / peaks["tflops"],
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["tflops"],
-                     "traffic": load_traffic(w.name) if nrm is None else None,
+                     "traffic": load_traffic(w) if nrm is None else None,
                      "kernel": ("attention, TF32 (sa_attn_fwd_f32 on sa_rope_qkv_f32 output)" if fp32 else
                                 "attention (sa_attn_fwd_rope_q)" if nrm is None else
                                 "attention (sa_attn_fwd on sa_qknorm_rope_qk output)"),
-                     "kernel_sha": kernel_sha(),
+                     "kernel_source": kernel_source(w), "kernel_sha": kernel_sha(w),
                      "peak_source": peaks["source"] if fp32 else peaks["source"] + " bf16 burst",
                      "avg_ms": attn_avg_s * 1e3,
                      # the same launch against the HBM roof: algorithmic bytes (q', k', v read once,

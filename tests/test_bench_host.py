@@ -58,11 +58,23 @@ def test_traffic_is_reported_only_for_the_captured_kernel(tmp_path, monkeypatch)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     stored = json.load(open(tmp_path / "profiles" / "traffic.json"))
     entry = stored["dit_l1292"]
-    monkeypatch.setattr(bench, "kernel_sha", lambda: entry["kernel_sha"])
-    assert bench.load_traffic("dit_l1292") == entry["bytes"]
-    assert bench.load_traffic("no_such_workload") is None
-    monkeypatch.setattr(bench, "kernel_sha", lambda: "0" * 16)
-    assert bench.load_traffic("dit_l1292") is None
+    monkeypatch.setattr(bench, "kernel_sha", lambda w=None: entry["kernel_sha"])
+    assert bench.load_traffic(W["dit_l1292"]) == entry["bytes"]
+    assert bench.load_traffic(W["tiny"]) is None
+    monkeypatch.setattr(bench, "kernel_sha", lambda w=None: "0" * 16)
+    assert bench.load_traffic(W["dit_l1292"]) is None
+
+
+def test_kernel_source_follows_the_library_routing():
+    # the FP32-input form runs the TF32 kernel; differential windows up to 256 the narrow-window
+    # kernel; everything else the general kernel
+    assert bench.kernel_source(W["swa_diff_l8192_fp32"]) == "sa_tf32.cu"
+    assert bench.kernel_source(W["swa_diff_l8192"]) == "sa_swa.cu"
+    assert bench.kernel_source(W["swa17_diff_l8192"]) == "sa_swa.cu"
+    assert bench.kernel_source(W["diff_l4096"]) == "sa_fmha.cu"
+    assert bench.kernel_source(W["dit_l4096_outliers"]) == "sa_fmha.cu"
+    src = open(os.path.join(bench.ROOT, "diffusion_transformer_attention_rope_gb300", "csrc", "sa_kernels.h")).read()
+    assert f"constexpr int kSwaMaxWindow = {bench.SWA_MAX_WINDOW};" in src
 
 
 def test_committed_traffic_is_at_least_the_compulsory_reads():
@@ -73,7 +85,8 @@ def test_committed_traffic_is_at_least_the_compulsory_reads():
         assert len(entry["kernel_sha"]) == 16, name
         w = W[name]
         n = w.B * w.H * w.L
-        compulsory = 2 * (n * w.nmaps * w.d * 2 + n * w.dv)
+        elem = 4 if w.dtype == "fp32" else 2
+        compulsory = elem * (n * w.nmaps * w.d * 2 + n * w.dv)
         assert entry["bytes"] >= 0.99 * compulsory, name
 
 
