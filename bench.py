@@ -104,15 +104,31 @@ def kernel_source(w=None) -> str:
     return "sa_fmha.cu"
 
 
-def kernel_sha(w=None) -> str:
-    """Hash of the workload's attention kernel source with comments and blank lines removed, so
-    that the stored ncu counters stay valid across comment-only edits and no others."""
+def kernel_sha(w=None, read=None) -> str:
+    """Hash of the workload's attention kernel source and of the device headers it includes
+    (sa_*.cuh, transitively), with comments and blank lines removed, so that the stored ncu
+    counters stay valid across comment-only edits and no others.  `read(name)` returns a source
+    file's text (default: the file in the package's csrc)."""
     import hashlib
     import re
 
-    path = os.path.join(ROOT, "diffusion_transformer_attention_rope_gb300", "csrc", kernel_source(w))
-    code = [re.sub(r"\s*//.*$", "", ln).rstrip() for ln in open(path).read().splitlines()]
-    return hashlib.sha256("\n".join(ln for ln in code if ln).encode()).hexdigest()[:16]
+    csrc = os.path.join(ROOT, "diffusion_transformer_attention_rope_gb300", "csrc")
+    if read is None:
+        def read(name):
+            with open(os.path.join(csrc, name)) as f:
+                return f.read()
+    names, todo = [], [kernel_source(w)]
+    while todo:
+        name = todo.pop(0)
+        if name in names:
+            continue
+        names.append(name)
+        todo += re.findall(r'^#include "(sa_\w+\.cuh)"', read(name), flags=re.M)
+    h = hashlib.sha256()
+    for name in [names[0]] + sorted(names[1:]):
+        code = [re.sub(r"\s*//.*$", "", ln).rstrip() for ln in read(name).splitlines()]
+        h.update(("\n".join(ln for ln in code if ln) + "\n").encode())
+    return h.hexdigest()[:16]
 
 
 def load_traffic(w):

@@ -33,10 +33,12 @@ def test_algorithmic_bytes():
 
 def _copy_tree(tmp_path):
     # the files bench reads for its bookkeeping, under a scratch root
-    src = os.path.join(bench.ROOT, "diffusion_transformer_attention_rope_gb300", "csrc", "sa_fmha.cu")
+    src_dir = os.path.join(bench.ROOT, "diffusion_transformer_attention_rope_gb300", "csrc")
     dst_dir = tmp_path / "diffusion_transformer_attention_rope_gb300" / "csrc"
     dst_dir.mkdir(parents=True)
-    shutil.copy(src, dst_dir / "sa_fmha.cu")
+    for name in os.listdir(src_dir):
+        if name.endswith((".cu", ".cuh", ".h")):
+            shutil.copy(os.path.join(src_dir, name), dst_dir / name)
     (tmp_path / "profiles").mkdir()
     shutil.copy(os.path.join(bench.ROOT, "profiles", "traffic.json"), tmp_path / "profiles" / "traffic.json")
     return dst_dir / "sa_fmha.cu"
@@ -51,6 +53,22 @@ def test_kernel_sha_ignores_comments_but_not_code(tmp_path, monkeypatch):
     assert bench.kernel_sha() == base
     src.write_text(text + "\nstatic int sa_unused_marker = 1;\n")
     assert bench.kernel_sha() != base
+
+
+def test_kernel_sha_covers_the_device_headers_a_kernel_includes(tmp_path, monkeypatch):
+    src = _copy_tree(tmp_path)
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    base = bench.kernel_sha()
+    hdr = src.parent / "sa_ptx.cuh"      # included through sa_pipe.cuh as well as directly
+    text = hdr.read_text()
+    hdr.write_text(text + "\n// a comment only\n")
+    assert bench.kernel_sha() == base
+    hdr.write_text(text + "\nstatic int sa_unused_marker = 1;\n")
+    assert bench.kernel_sha() != base
+    # a header no attention kernel includes does not count
+    hdr.write_text(text)
+    (src.parent / "sa_unrelated.cuh").write_text("static int sa_other = 2;\n")
+    assert bench.kernel_sha() == base
 
 
 def test_traffic_is_reported_only_for_the_captured_kernel(tmp_path, monkeypatch):
