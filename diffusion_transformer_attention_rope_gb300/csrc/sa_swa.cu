@@ -18,14 +18,19 @@
 //   - the rings, S buffers and their barriers run on across units with a CTA-wide tile count
 //     (the P.V completion is tracked per S buffer, so an S MMA waits only for the P.V that read
 //     its buffer); the first P.V of a unit (which overwrites O) waits until the previous
-//     epilogue has read O.
-// Warp roles as in the general kernel: warps 0-3 / 4-7 softmax of map 0 / 1 (thread = query row
-// = TMEM lane), warp 8 TMA of Q and the K ring, warp 9 TMEM allocation and MMA issuer of map 0,
-// warp 10 MMA issuer of map 1, warp 11 TMA of the V ring.
+//     epilogue has read O;
+//   - the RoPE of each unit's Q and each unit's epilogue run on a warpgroup of their own (the
+//     output warps), so the softmax warps go from one unit's last key tile straight to the next
+//     unit's first: the output warps rotate unit u + 1's Q while the softmax warps work on unit
+//     u, and write unit u's output while they work on unit u + 1.
+// Warp roles (512 threads): warps 0-3 / 4-7 softmax of map 0 / 1 (thread = query row = TMEM
+// lane), warp 8 TMA of Q and the K ring, warp 9 TMEM allocation and MMA issuer of map 0, warp 10
+// MMA issuer of map 1, warp 11 TMA of the V ring, warps 12-15 the output warps (thread = query
+// row of both maps).
 // Tensor memory (512 columns): map m at 256 m: S buffer 0 | S buffer 1 | O = 64 | 64 | 128.
-// Shared memory: Q 2 x 32 KB, K ring 3 x 16 KB, V ring 3 x 16 KB, output staging 32 KB (the
-// epilogue writes each warp's 32 x 64 block of the output with one TMA store, not as scattered
-// 16-byte stores of rows 256 bytes apart).  Every wait is bounded.
+// Shared memory: Q 2 x 32 KB, K ring 3 x 16 KB, V ring 3 x 16 KB, output staging 32 KB (each
+// output warp writes its 32 rows x 128 values with two TMA stores, not as scattered 16-byte
+// stores of rows 256 bytes apart).  Every wait is bounded.
 #include <cuda.h>
 
 #include "sa_kernels.h"
@@ -35,6 +40,8 @@
 namespace sa {
 namespace {
 
+constexpr int kSwaThreads = 512;               // 4 warpgroups: 2 softmax, control, output
+constexpr int kOutWarp = 12;                   // first output warp
 constexpr int kBN = 64;                        // keys per tile
 constexpr int kQTile = kBlockM * kHeadDim * 2; // one map's 128 x 64 Q tile (16 KB, one atom)
 constexpr int kKMap = kBN * kHeadDim * 2;      // one map's 64 x 64 K tile (8 KB)
@@ -46,13 +53,16 @@ constexpr int kVAtom = kVStage / 2;
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + 2 * kQBuf;
 constexpr int kOffV = kOffK + kNS * kKStage;
-// output staging for the epilogue's TMA stores: per softmax warp 32 rows x 64 values (4 KB)
-constexpr int kStageWarp = 32 * 128;
+// output staging for the epilogue's TMA stores: per output warp 32 rows x 128 values as two
+// 32 x 64 boxes of 4 KB
+constexpr int kStageBox = 32 * 128;
+constexpr int kStageWarp = 2 * kStageBox;
 constexpr int kOffStage = kOffV + kNS * kVStage;
-// barriers: q_full[2], q_ready[2][2], q_free[2], k_full[4], k_empty[4], v_full[4], v_empty[4],
-//           s_full[2][2], p_full[2][2], pv_done[2][2], o_full[2], o_free, drain[2], l_ready
-constexpr int kNBar = 2 + 4 + 2 + 4 * kNS + 4 + 4 + 4 + 2 + 1 + 2 + 1;
-constexpr int kOffBar = kOffStage + 8 * kStageWarp;
+// barriers: q_full[2], q_ready[2][2], q_free[2], k_full[kNS], k_empty[kNS], v_full[kNS],
+//           v_empty[kNS], s_full[2][2], p_full[2][2], pv_done[2][2], o_full[2], o_free, drain[2],
+//           l_ready[2], l_free[2]
+constexpr int kNBar = 2 + 4 + 2 + 4 * kNS + 4 + 4 + 4 + 2 + 1 + 2 + 2 + 2;
+constexpr int kOffBar = kOffStage + 4 * kStageWarp;
 constexpr int kOffMisc = kOffBar + 8 * kNBar;  // tmem base, abort flag
 constexpr int kOffLsum = kOffMisc + 16;        // float [2 units][2 maps][128]
 constexpr int kSmemUsed = kOffLsum + 2 * 2 * kBlockM * 4;
@@ -76,11 +86,12 @@ struct Bars {
   __device__ uint32_t o_full(int m) const { return base + 160 + 32 * kNS + 8 * m; }
   __device__ uint32_t o_free() const { return base + 176 + 32 * kNS; }
   __device__ uint32_t drain(int m) const { return base + 184 + 32 * kNS + 8 * m; }
-  // the epilogue's exchange of row sums between the two maps' warpgroups (an mbarrier, so that
-  // its wait is bounded like every other)
-  __device__ uint32_t l_ready() const { return base + 200 + 32 * kNS; }
+  // the row sums of the units of parity b: written by the softmax warps (l_ready), read by the
+  // output warps (l_free)
+  __device__ uint32_t l_ready(int b) const { return base + 200 + 32 * kNS + 8 * b; }
+  __device__ uint32_t l_free(int b) const { return base + 216 + 32 * kNS + 8 * b; }
 };
-static_assert(208 + 32 * kNS == 8 * kNBar, "barrier layout");
+static_assert(232 + 32 * kNS == 8 * kNBar, "barrier layout");
 
 __device__ __forceinline__ uint32_t s_col(int m, int b) { return 256 * m + 64 * b; }
 __device__ __forceinline__ uint32_t o_col(int m) { return 256 * m + 128; }
@@ -128,39 +139,26 @@ __device__ __noinline__ void rescale_o128(uint32_t taddr, float f) {
   }
 }
 
-// RoPE of this thread's raw Q row in shared memory (128-byte-swizzled), with the (cos, sin)
-// table of the RoPE pass and its arithmetic (rope_rotate8), so that q' has the pass's bits; with
-// NORM the row is QK-RMS-normalised first, with the pass's sum order and scaling.
+// RoPE of this thread's raw Q rows of both maps in shared memory (128-byte-swizzled; the rows
+// share the position), with the (cos, sin) table of the RoPE pass and its arithmetic
+// (rope_rotate8), so that q' has the pass's bits; with NORM each row is QK-RMS-normalised first,
+// with the pass's sum order and scaling.  Each table entry is loaded once for both rows: all 16
+// up front, or (NORM, which needs the registers for its scales) one group of 4 at a time.
 template <bool BF16, bool NORM>
-__device__ __noinline__ void rotate_q_row(const float2* cs, int cs_stride, int L, int grow, uint32_t row, int r,
-                                          const float* gamma, float eps) {
+__device__ __noinline__ void rotate_q_rows(const float2* cs, int cs_stride, int L, int grow, uint32_t row0,
+                                           uint32_t row1, int r, const float* gamma, float eps) {
   if (grow >= L) return;
-  float4 t[16];
   const float4* cs4 = reinterpret_cast<const float4*>(cs) + grow;
-#pragma unroll
-  for (int m = 0; m < 16; ++m) t[m] = __ldg(cs4 + static_cast<size_t>(m) * cs_stride);
-  uint4 lo[4], hi[4];
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
-    lo[g] = ld_shared_v4(row + ((g ^ (r & 7)) << 4));
-    hi[g] = ld_shared_v4(row + (((g + 4) ^ (r & 7)) << 4));
-  }
-  float inv = 1.0f;
-  if (NORM) {
-    float tg[4];
-#pragma unroll
-    for (int g = 0; g < 4; ++g) tg[g] = sumsq8<BF16>(lo[g]) + sumsq8<BF16>(hi[g]);
-    inv = qknorm_inv_rms((tg[0] + tg[1]) + (tg[2] + tg[3]), eps);
-  }
-#pragma unroll
-  for (int g = 0; g < 4; ++g) {
+  auto rotate_group = [&](uint32_t row, int g, const float4 (&t)[4], float inv) {
+    const uint4 lo = ld_shared_v4(row + ((g ^ (r & 7)) << 4));
+    const uint4 hi = ld_shared_v4(row + (((g + 4) ^ (r & 7)) << 4));
     float cg[8], sg[8];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      cg[2 * i] = t[4 * g + i].x;
-      sg[2 * i] = t[4 * g + i].y;
-      cg[2 * i + 1] = t[4 * g + i].z;
-      sg[2 * i + 1] = t[4 * g + i].w;
+      cg[2 * i] = t[i].x;
+      sg[2 * i] = t[i].y;
+      cg[2 * i + 1] = t[i].z;
+      sg[2 * i + 1] = t[i].w;
     }
     uint4 olo, ohi;
     if (NORM) {
@@ -170,18 +168,51 @@ __device__ __noinline__ void rotate_q_row(const float2* cs, int cs_stride, int L
         sl[i] = __fmul_rn(inv, gamma[8 * g + i]);
         sh[i] = __fmul_rn(inv, gamma[32 + 8 * g + i]);
       }
-      rope_rotate8_scaled<BF16>(lo[g], hi[g], cg, sg, sl, sh, olo, ohi);
+      rope_rotate8_scaled<BF16>(lo, hi, cg, sg, sl, sh, olo, ohi);
     } else {
-      rope_rotate8<BF16>(lo[g], hi[g], cg, sg, olo, ohi);
+      rope_rotate8<BF16>(lo, hi, cg, sg, olo, ohi);
     }
     st_shared_v4(row + ((g ^ (r & 7)) << 4), olo.x, olo.y, olo.z, olo.w);
     st_shared_v4(row + (((g + 4) ^ (r & 7)) << 4), ohi.x, ohi.y, ohi.z, ohi.w);
+  };
+  if (NORM) {
+    // each row's 1 / rms from its raw values, then the rotation group by group
+    float inv[2];
+#pragma unroll
+    for (int mm = 0; mm < 2; ++mm) {
+      const uint32_t row = mm ? row1 : row0;
+      float tg[4];
+#pragma unroll
+      for (int g = 0; g < 4; ++g)
+        tg[g] = sumsq8<BF16>(ld_shared_v4(row + ((g ^ (r & 7)) << 4))) +
+                sumsq8<BF16>(ld_shared_v4(row + (((g + 4) ^ (r & 7)) << 4)));
+      inv[mm] = qknorm_inv_rms((tg[0] + tg[1]) + (tg[2] + tg[3]), eps);
+    }
+#pragma unroll 1
+    for (int g = 0; g < 4; ++g) {
+      float4 t[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) t[i] = __ldg(cs4 + static_cast<size_t>(4 * g + i) * cs_stride);
+      rotate_group(row0, g, t, inv[0]);
+      rotate_group(row1, g, t, inv[1]);
+    }
+  } else {
+    float4 t[4][4];
+#pragma unroll
+    for (int g = 0; g < 4; ++g)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) t[g][i] = __ldg(cs4 + static_cast<size_t>(4 * g + i) * cs_stride);
+#pragma unroll 1
+    for (int mm = 0; mm < 2; ++mm) {
+#pragma unroll
+      for (int g = 0; g < 4; ++g) rotate_group(mm ? row1 : row0, g, t[g], 1.0f);
+    }
   }
 }
 
 // NORM: the QK-RMSNorm form (a kernel of its own, so that the plain one carries none of its code)
 template <bool BF16, bool NORM>
-__global__ void __launch_bounds__(kFmhaThreads, 1)
+__global__ void __launch_bounds__(kSwaThreads, 1)
     fmha_swa_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                     const __grid_constant__ FmhaSwaArgs a) {
@@ -229,8 +260,11 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       mbar_init(bar.o_full(m), 1);
       mbar_init(bar.drain(m), 1);
     }
-    mbar_init(bar.o_free(), 8);          // every softmax warp, after the epilogue read O
-    mbar_init(bar.l_ready(), 8);         // every softmax warp, after writing its row sums
+    mbar_init(bar.o_free(), 4);          // every output warp, after the epilogue read O
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar.l_ready(b), 8);      // every softmax warp, after writing its row sums
+      mbar_init(bar.l_free(b), 4);       // every output warp, after reading them
+    }
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -243,7 +277,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     tma_prefetch_desc(&tm_k);
   }
   if (warp == kTmaWarpV && lane == 0) tma_prefetch_desc(&tm_v);
-  if (warp == 0 && lane == 0) tma_prefetch_desc(&tm_o);
+  if (warp == kOutWarp && lane == 0) tma_prefetch_desc(&tm_o);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -327,27 +361,36 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       umma_commit_w(bar.s_full(m, gg & 1));
       umma_commit_w(bar.k_empty(st));
     };
+    // S MMAs run ahead of the P.V MMAs by two tiles across unit boundaries: S(j) is issued as soon
+    // as its buffer (that of tile j - 2) has been read by P.V(j - 2), whichever unit tile j belongs
+    // to, so the softmax warps find the next unit's first S ready when they finish a unit.
+    Unit sx = unit_of(a, u_begin);   // unit of the next S to issue
+    int s_ui = 0, s_t = 0, s_g = 0;  // its index in the run, its tile in the unit, its tile in the run
+    auto issue_next_s = [&]() {
+      if (s_ui >= n_units) return true;
+      const int qb = s_ui & 1;
+      // a unit's first S: its Q has been rotated
+      if (s_t == 0 && !pwait_w(bar.q_ready(qb, m), (s_ui >> 1) & 1, abort_flag, a.err, eb, tmo)) return false;
+      // S(j) goes into the buffer of tile j - 2: after that tile's P.V has read its P
+      if (s_g >= 2 && !pwait_w(bar.pv_done(m, s_g & 1), ((s_g - 2) >> 1) & 1, abort_flag, a.err, eb, tmo))
+        return false;
+      if (!pwait_w(bar.k_full(s_g % kNS), (s_g / kNS) & 1, abort_flag, a.err, eb, tmo)) return false;
+      tc_fence_after();
+      issue_s(s_g, dq0 + static_cast<uint64_t>(qb * (kQBuf >> 4)));
+      ++s_g;
+      if (++s_t == sx.n_tiles) {
+        s_t = 0;
+        ++s_ui;
+        sx = next_unit(a, sx);
+      }
+      return true;
+    };
+    bool ok = issue_next_s() && issue_next_s();
     int g = 0;
-    bool ok = true;
     Unit x = unit_of(a, u_begin);
     for (int ui = 0; ok && ui < n_units; ++ui, x = next_unit(a, x)) {
       const int qb = ui & 1;
-      const uint64_t dq = dq0 + static_cast<uint64_t>(qb * (kQBuf >> 4));
       const int n = x.n_tiles;
-      ok = pwait_w(bar.q_ready(qb, m), (ui >> 1) & 1, abort_flag, a.err, eb, tmo);
-      // S(g) goes into the buffer of tile g - 2: after that tile's P.V has read its P
-      if (ok && g >= 2) ok = pwait_w(bar.pv_done(m, g & 1), ((g - 2) >> 1) & 1, abort_flag, a.err, eb, tmo);
-      if (ok) ok = pwait_w(bar.k_full(g % kNS), (g / kNS) & 1, abort_flag, a.err, eb, tmo);
-      if (!ok) break;
-      tc_fence_after();
-      issue_s(g, dq);
-      if (n > 1) {
-        ok = (g < 1 || pwait_w(bar.pv_done(m, (g + 1) & 1), ((g - 1) >> 1) & 1, abort_flag, a.err, eb, tmo)) &&
-             pwait_w(bar.k_full((g + 1) % kNS), ((g + 1) / kNS) & 1, abort_flag, a.err, eb, tmo);
-        if (!ok) break;
-        tc_fence_after();
-        issue_s(g + 1, dq);
-      }
       for (int t = 0; t < n; ++t) {
         const int gg = g + t;
         const int sv = gg % kNS;
@@ -368,14 +411,9 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
           umma_commit_w(bar.o_full(m));
           umma_commit_w(bar.q_free(qb));
         }
-        if (t + 2 < n) {
-          // S(gg + 2) goes into the buffer P(gg) occupies: after P.V(gg) has read it
-          ok = pwait_w(bar.pv_done(m, gg & 1), (gg >> 1) & 1, abort_flag, a.err, eb, tmo) &&
-               pwait_w(bar.k_full((gg + 2) % kNS), ((gg + 2) / kNS) & 1, abort_flag, a.err, eb, tmo);
-          if (!ok) break;
-          tc_fence_after();
-          issue_s(gg + 2, dq);
-        }
+        // S(gg + 2), of this unit or of the next ones
+        ok = issue_next_s();
+        if (!ok) break;
       }
       g += n;
     }
@@ -391,26 +429,9 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     const float c = a.scale_log2;
     const float tau = 8.0f / c;
     const int w = a.window;
-    // a per-call (cos, sin) table is the RoPE pass's output
-    if (!a.cs_static) asm volatile("griddepcontrol.wait;" ::: "memory");
-    // RoPE prologue of this row of unit ui's Q (in its buffer), then the unit's Q goes to the
-    // map's MMA issuer
-    auto q_prologue = [&](int ui, const Unit& y) {
-      const int qb = ui & 1;
-      bool good = pwait(bar.q_full(qb), (ui >> 1) & 1, abort_flag, a.err, kErrSoftmax, tmo);
-      good = __all_sync(0xffffffffu, good);
-      if (!good) return false;
-      if (a.cs != nullptr)
-        rotate_q_row<BF16, NORM>(a.cs, a.cs_stride, L, y.q0 + r, sQ + qb * kQBuf + m * kQTile + r * 128, r,
-                                 a.gamma_q, a.eps);
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar.q_ready(qb, m));
-      return true;
-    };
     int g = 0;
+    bool ok = true;
     Unit x = unit_of(a, u_begin);
-    bool ok = n_units > 0 ? q_prologue(0, x) : true;
     for (int ui = 0; ok && ui < n_units; ++ui, x = next_unit(a, x)) {
       const int grow = x.q0 + r;
       const int rows_lo = x.q0, rows_hi = x.q0 + kBlockM - 1;
@@ -493,40 +514,77 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         if (lane == 0) mbar_arrive(bar.p_full(m, b));
       }
       if (!ok) break;
-      // the next unit's Q now, so that its first S MMAs overlap this unit's last P.V and epilogue
+      // the unit's row sums go to the output warps (the buffer of this parity is free once they
+      // have read the sums of unit ui - 2)
+      if (ui >= 2) {
+        ok = pwait(bar.l_free(ui & 1), ((ui >> 1) - 1) & 1, abort_flag, a.err, kErrSoftmax, tmo);
+        ok = __all_sync(0xffffffffu, ok);
+        if (!ok) break;
+      }
+      lsum[(ui & 1) * 2 * kBlockM + m * kBlockM + r] = l_sum;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.l_ready(ui & 1));
+      g += x.n_tiles;
+    }
+  } else if (warp >= kOutWarp) {
+    // ---------------------------------------------------------------- output warps
+    // Thread = query row r of both maps.  Per unit: the RoPE of the next unit's Q (both maps),
+    // then this unit's epilogue, out = O_0 / l_0 - lambda_h O_1 / l_1 in FP32, one RNE cast.
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t stage = sb + kOffStage + (warp - kOutWarp) * kStageWarp;
+    // a per-call (cos, sin) table is the RoPE pass's output
+    if (!a.cs_static) asm volatile("griddepcontrol.wait;" ::: "memory");
+    // RoPE of row r of unit ui's Q (both maps, in its buffer), then the Q goes to the issuers
+    auto q_prologue = [&](int ui, const Unit& y) {
+      const int qb = ui & 1;
+      bool good = pwait(bar.q_full(qb), (ui >> 1) & 1, abort_flag, a.err, kErrSoftmax, tmo);
+      good = __all_sync(0xffffffffu, good);
+      if (!good) return false;
+      if (a.cs != nullptr)
+        rotate_q_rows<BF16, NORM>(a.cs, a.cs_stride, L, y.q0 + r, sQ + qb * kQBuf + r * 128,
+                                  sQ + qb * kQBuf + kQTile + r * 128, r, a.gamma_q, a.eps);
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(bar.q_ready(qb, 0));
+        mbar_arrive(bar.q_ready(qb, 1));
+      }
+      return true;
+    };
+    Unit x = unit_of(a, u_begin);
+    bool ok = n_units > 0 ? q_prologue(0, x) : true;
+    for (int ui = 0; ok && ui < n_units; ++ui, x = next_unit(a, x)) {
+      // the next unit's Q first: its S MMAs then start as soon as this unit's last tiles free
+      // the S buffers
       if (ui + 1 < n_units && !q_prologue(ui + 1, next_unit(a, x))) {
         ok = false;
         break;
       }
-
-      // ---------------------------------------------------------------- epilogue of the unit
-      ok = pwait(bar.o_full(0), ui & 1, abort_flag, a.err, kErrSoftmax, tmo);
+      // ---------------------------------------------------------------- epilogue of unit ui
+      ok = pwait(bar.l_ready(ui & 1), (ui >> 1) & 1, abort_flag, a.err, kErrSoftmax, tmo);
+      if (ok) ok = pwait(bar.o_full(0), ui & 1, abort_flag, a.err, kErrSoftmax, tmo);
       if (ok) ok = pwait(bar.o_full(1), ui & 1, abort_flag, a.err, kErrSoftmax, tmo);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      float* ls = lsum + (ui & 1) * 2 * kBlockM;
-      ls[m * kBlockM + r] = l_sum;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar.l_ready());
-      ok = pwait(bar.l_ready(), ui & 1, abort_flag, a.err, kErrSoftmax, tmo);
-      ok = __all_sync(0xffffffffu, ok);
-      if (!ok) break;
+      const float* ls = lsum + (ui & 1) * 2 * kBlockM;
       const float l0 = ls[r], l1 = ls[kBlockM + r];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar.l_free(ui & 1));
       const float inv0 = l0 > 0.0f ? 1.0f / l0 : 0.0f;
       const float inv1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;
       const float lam = a.lambda[x.bh % a.H];
-      // warpgroup m writes output columns [64 m, 64 m + 64): this warp's 32 rows go through its
-      // staging block (128-byte swizzle: 16-byte chunk c of row i at c ^ (i & 7)) and one TMA store
-      const uint32_t stage = sb + kOffStage + warp * kStageWarp + lane * 128;
-      if (lane == 0) bulk_wait_read();   // the previous unit's store has read the block
+      // this warp's 32 rows x 128 values go through its staging block (two 32 x 64 boxes,
+      // 128-byte swizzle: 16-byte chunk c of row i at c ^ (i & 7)) and two TMA stores
+      if (lane == 0) bulk_wait_read();   // the previous unit's stores have read the block
       __syncwarp();
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const uint32_t col = 64 * m + 32 * cc;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
         uint32_t o0[32], o1[32];
-        tmem_ld32_nowait(tmem + o_col(0) + lane_off + col, o0);
-        tmem_ld32_nowait(tmem + o_col(1) + lane_off + col, o1);
+        tmem_ld32_nowait(tmem + o_col(0) + lane_off + 32 * cc, o0);
+        tmem_ld32_nowait(tmem + o_col(1) + lane_off + 32 * cc, o1);
         tmem_wait_ld_32(o0);
         tmem_wait_ld_32(o1);
         uint32_t pkd[16];
@@ -536,9 +594,10 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
           const float y1 = fmaf(-lam, __uint_as_float(o1[2 * j + 1]) * inv1, __uint_as_float(o0[2 * j + 1]) * inv0);
           pkd[j] = pack2<BF16>(y0, y1);
         }
+        const uint32_t row = stage + (cc >> 1) * kStageBox + lane * 128;
 #pragma unroll
         for (int j = 0; j < 4; ++j)
-          st_shared_v4(stage + (((4 * cc + j) ^ (lane & 7)) << 4), pkd[4 * j], pkd[4 * j + 1], pkd[4 * j + 2],
+          st_shared_v4(row + (((4 * (cc & 1) + j) ^ (lane & 7)) << 4), pkd[4 * j], pkd[4 * j + 1], pkd[4 * j + 2],
                        pkd[4 * j + 3]);
       }
       // O has been read: the next unit's first P.V may overwrite it
@@ -548,10 +607,10 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       if (lane == 0) {
         mbar_arrive(bar.o_free());
         // rows past L are outside the tensor and not written
-        tma_store_3d(&tm_o, sb + kOffStage + warp * kStageWarp, 64 * m, x.q0 + 32 * quarter, x.bh);
+        tma_store_3d(&tm_o, stage, 0, x.q0 + 32 * quarter, x.bh);
+        tma_store_3d(&tm_o, stage + kStageBox, 64, x.q0 + 32 * quarter, x.bh);
         bulk_commit();
       }
-      g += x.n_tiles;
     }
     // the output stores complete before the CTA's shared memory goes away
     if (lane == 0) bulk_wait_all();
@@ -572,7 +631,7 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
                    const FmhaSwaArgs& a, int num_ctas, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(num_ctas));
-  cfg.blockDim = dim3(kFmhaThreads);
+  cfg.blockDim = dim3(kSwaThreads);
   cfg.dynamicSmemBytes = kSmemAlloc;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
