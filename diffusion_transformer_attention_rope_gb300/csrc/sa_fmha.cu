@@ -448,7 +448,8 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
   // run warp-uniform code: every lane waits on the barriers and one lane, elected inside each
   // issuing instruction, issues the copies / MMAs / commits (the operands stay warp-uniform,
   // which keeps the issue of each tcgen05.mma short).
-  regs_dec<kControlRegs>();
+  // the standard kernel's register split (the differential kernel runs without one)
+  if (!DIFF) regs_dec<kControlRegs>();
   if (warp == kTmaWarp) {
     // ------------------------------------------------------------------ K producer (+ Q)
     // This grid may have been started early (programmatic dependent launch) while the kernel
@@ -603,7 +604,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
   }
   } else {
     // ------------------------------------------------------------------ softmax warpgroups
-    regs_inc<kSoftmaxRegs>();
+    if (!DIFF) regs_inc<kSoftmaxRegs>();
     const int s = warp >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;                     // TMEM lane = tile row

@@ -476,9 +476,11 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
           m_use = mt;
         } else if (__any_sync(0xffffffffu, mt > m_use + tau)) {
           const float m_new = fmaxf(m_use, mt);
-          f = (m_new == m_use) ? 1.0f : ex2_approx((m_use - m_new) * c);
+          // a row whose running max is still -inf has had P = 0 on every tile so far: its O row
+          // and row sum are exactly 0 and need no rescale (nor the wait for the last P.V)
+          f = (m_new == m_use || m_use == -INFINITY) ? 1.0f : ex2_approx((m_use - m_new) * c);
           m_use = m_new;
-          rescale = true;
+          rescale = __any_sync(0xffffffffu, f != 1.0f);
         }
         const float mb = (m_use == -INFINITY) ? 0.0f : m_use * c;
         const float2 c2 = make_float2(c, c), nmb2 = make_float2(-mb, -mb);
