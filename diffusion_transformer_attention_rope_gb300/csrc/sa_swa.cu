@@ -285,19 +285,31 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
 
   if (warp == kTmaWarp) {
     // ---------------------------------------------------------------- Q and K producer
-    // raw q is the caller's; k' is the RoPE pass's output (programmatic dependent launch)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     int g = 0, issued = 0, q_issued = 0;
     bool ok = true;
     Unit x = unit_of(a, u_begin);
+    auto load_q = [&](int ui, const Unit& y) {
+      const int qb = ui & 1;
+      mbar_arrive_expect_tx_w(bar.q_full(qb), kQBuf);
+      tma_load_3d_w(sQ + qb * kQBuf, &tm_q, bar.q_full(qb), 0, y.q0, 2 * y.bh);
+      tma_load_3d_w(sQ + qb * kQBuf + kQTile, &tm_q, bar.q_full(qb), 0, y.q0, 2 * y.bh + 1);
+      q_issued = ui + 1;
+    };
+    // Raw q is the caller's: the first two units' Q are copied before the wait for the RoPE
+    // pass, whose output (k', or q' as well when cs is nullptr) the rest waits for
+    // (programmatic dependent launch).
+    if (a.cs != nullptr && n_units > 0) {
+      load_q(0, x);
+      if (n_units > 1) load_q(1, next_unit(a, x));
+    }
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     for (int ui = 0; ok && ui < n_units; ++ui, x = next_unit(a, x)) {
       const int qb = ui & 1;
       // the buffer's previous unit (ui - 2) must be done with it (its S MMAs have completed)
-      if (ui >= 2 && !pwait_w(bar.q_free(qb), ((ui >> 1) - 1) & 1, abort_flag, a.err, kErrProducer, tmo)) break;
-      q_issued = ui + 1;
-      mbar_arrive_expect_tx_w(bar.q_full(qb), kQBuf);
-      tma_load_3d_w(sQ + qb * kQBuf, &tm_q, bar.q_full(qb), 0, x.q0, 2 * x.bh);
-      tma_load_3d_w(sQ + qb * kQBuf + kQTile, &tm_q, bar.q_full(qb), 0, x.q0, 2 * x.bh + 1);
+      if (ui >= q_issued) {
+        if (ui >= 2 && !pwait_w(bar.q_free(qb), ((ui >> 1) - 1) & 1, abort_flag, a.err, kErrProducer, tmo)) break;
+        load_q(ui, x);
+      }
       for (int t = 0; t < x.n_tiles; ++t, ++g) {
         const int st = g % kNS;
         if (!pwait_w(bar.k_empty(st), ((g / kNS) & 1) ^ 1, abort_flag, a.err, kErrProducer, tmo)) {
@@ -321,7 +333,9 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
   } else if (warp == kTmaWarpV) {
     // ---------------------------------------------------------------- V producer
     int g = 0, issued = 0;
-    bool ok = true;
+    // V is first read by the first P.V, well after the first Q: its copies start once that Q
+    // has landed, so that the Q copies at the start of the kernel do not share HBM with them
+    bool ok = n_units == 0 || pwait_w(bar.q_full(0), 0, abort_flag, a.err, kErrProducer, tmo);
     Unit x = unit_of(a, u_begin);
     for (int ui = 0; ok && ui < n_units; ++ui, x = next_unit(a, x)) {
       for (int t = 0; t < x.n_tiles; ++t, ++g) {
@@ -541,6 +555,13 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
     // RoPE of row r of unit ui's Q (both maps, in its buffer), then the Q goes to the issuers
     auto q_prologue = [&](int ui, const Unit& y) {
       const int qb = ui & 1;
+      if (a.cs != nullptr && y.q0 + r < L) {
+        // the row's 16 table entries into L2 while the Q copy is in flight
+        const float4* cs4 = reinterpret_cast<const float4*>(a.cs) + y.q0 + r;
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          asm volatile("prefetch.global.L2 [%0];" ::"l"(cs4 + static_cast<size_t>(i) * a.cs_stride));
+      }
       bool good = pwait(bar.q_full(qb), (ui >> 1) & 1, abort_flag, a.err, kErrSoftmax, tmo);
       good = __all_sync(0xffffffffu, good);
       if (!good) return false;

@@ -174,12 +174,19 @@ def test_q_rope_prologue_matches_prepass(attn, diff, dtype, window):
     (1, 2, 900, False, "fp16", 129, False),
     (1, 2, 300, False, "bf16", 0, True),
     (1, 3, 129, True, "fp16", 1, False),       # ragged tail tile
+    # the narrow-window kernel: windows 0 and 256, units of one key tile (L <= 64), runs of
+    # several units per CTA, a ragged tail
+    (1, 5, 50, True, "bf16", 0, False),
+    (2, 3, 64, True, "fp16", 5, True),
+    (2, 16, 1292, True, "bf16", 17, True),     # 352 units on the SMs
+    (1, 4, 2000, True, "bf16", 256, False),
+    (1, 2, 1111, True, "fp16", 256, True),
 ])
 def test_rope_attn_matches_two_pass_bits(attn, B, H, L, diff, dtype, window, explicit):
     # the public call (K pass with the (cos, sin) table, q rotated in the attention kernel's
-    # prologue, workspace-backed last-wave pieces) has the bits of the two-pass path
-    # (sa_rope_qk, then sa_attn_fwd on q') across grid sizes and windows, with and without
-    # positions.
+    # prologue, workspace-backed last-wave pieces; the narrow-window kernel for differential
+    # windows up to 256) has the bits of the two-pass path (sa_rope_qk, then sa_attn_fwd on q',
+    # k') across grid sizes and windows, with and without positions.
     w = small("twopass", B=B, H=H, L=L, window=window, nmaps=2 if diff else 1, dv=128 if diff else 64,
               dtype=dtype, seed=77 + L, lam=("uniform", 0.2, 0.8) if diff else None)
     x = synth.make_inputs(w)
@@ -550,7 +557,7 @@ def test_qknorm_prepass_matches_oracle(attn, dtype):
         assert (got == oracle.round_to(exact, dtype)).mean() > 0.95
 
 
-@pytest.mark.parametrize("diff,dtype,window", [(False, "fp16", -1), (True, "bf16", 129)])
+@pytest.mark.parametrize("diff,dtype,window", [(False, "fp16", -1), (True, "bf16", 129), (True, "fp16", 17)])
 def test_qknorm_prologue_matches_prepass(attn, diff, dtype, window):
     # the fused path (K pass with the norm, q normalised in the attention kernel's prologue)
     # has the bits of sa_qknorm_rope_qk followed by sa_attn_fwd
