@@ -71,70 +71,96 @@ __device__ __forceinline__ void rope_rotate8_f32(float (&lo)[8], float (&hi)[8],
   }
 }
 
-// v^T of 32 keys of every plane of the block's slice: v [L][128] rows read as float4 per lane,
-// staged in shared memory, written as 128 rows of 32 keys (TF32) of v^T [128][L_pad].
-__device__ __forceinline__ void transpose_v_item(const RopeF32Args& a, float (*tile)[kRopeF32Rows + 1]) {
-  const int l0 = blockIdx.x * kRopeF32Rows;
+// v^T of keys [l0, l0 + 32) of v plane pl: the rows v[l][0 .. 128) read as float4 per lane,
+// staged in shared memory, written as 128 rows of 32 keys (TF32) of v^T [128][L_pad] (keys past
+// L as zeros).  Every thread of the block takes part (two block barriers).
+__device__ __forceinline__ void transpose_v_item(const RopeF32Args& a, int l0, long long pl,
+                                                 float (*tile)[kRopeF32Rows + 1]) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (long long pl = blockIdx.y; pl < a.planes_v; pl += gridDim.y) {
-    const float* src = a.v + static_cast<size_t>(pl) * a.L * (2 * kHeadDim);
-    float* dst = a.v_t + static_cast<size_t>(pl) * (2 * kHeadDim) * a.L_pad;
-    // row l0 + 4 j + warp: each lane loads 4 consecutive values of the row's 128
+  const float* src = a.v + static_cast<size_t>(pl) * a.L * (2 * kHeadDim);
+  float* dst = a.v_t + static_cast<size_t>(pl) * (2 * kHeadDim) * a.L_pad;
+  // row l0 + 4 j + warp: each lane loads 4 consecutive values of the row's 128 (all 8 loads
+  // issued before the first use)
+  float4 x[kRopeF32Rows / 4];
 #pragma unroll
-    for (int j = 0; j < kRopeF32Rows / 4; ++j) {
-      const int rr = 4 * j + warp;
-      const int l = l0 + rr;
-      float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (l < a.L) x = ld_stream_f4(src + static_cast<size_t>(l) * (2 * kHeadDim) + 4 * lane);
-      tile[4 * lane + 0][rr] = x.x;
-      tile[4 * lane + 1][rr] = x.y;
-      tile[4 * lane + 2][rr] = x.z;
-      tile[4 * lane + 3][rr] = x.w;
-    }
-    __syncthreads();
-    // v^T row c = 4 i + warp: each lane writes key l0 + lane of it (keys past L as zeros)
-#pragma unroll 4
-    for (int i = 0; i < (2 * kHeadDim) / 4; ++i) {
-      const int c = 4 * i + warp;
-      const int l = l0 + lane;
-      if (l < a.L_pad) dst[static_cast<size_t>(c) * a.L_pad + l] = l < a.L ? round_tf32(tile[c][lane]) : 0.0f;
-    }
-    __syncthreads();
+  for (int j = 0; j < kRopeF32Rows / 4; ++j) {
+    const int l = l0 + 4 * j + warp;
+    x[j] = l < a.L ? ld_stream_f4(src + static_cast<size_t>(l) * (2 * kHeadDim) + 4 * lane)
+                   : make_float4(0.f, 0.f, 0.f, 0.f);
   }
+#pragma unroll
+  for (int j = 0; j < kRopeF32Rows / 4; ++j) {
+    const int rr = 4 * j + warp;
+    tile[4 * lane + 0][rr] = x[j].x;
+    tile[4 * lane + 1][rr] = x[j].y;
+    tile[4 * lane + 2][rr] = x[j].z;
+    tile[4 * lane + 3][rr] = x[j].w;
+  }
+  __syncthreads();
+  // v^T row c = 4 i + warp: each lane writes key l0 + lane of it
+  const int l = l0 + lane;
+#pragma unroll 8
+  for (int i = 0; i < (2 * kHeadDim) / 4; ++i) {
+    const int c = 4 * i + warp;
+    if (l < a.L_pad) dst[static_cast<size_t>(c) * a.L_pad + l] = l < a.L ? round_tf32(tile[c][lane]) : 0.0f;
+  }
+  __syncthreads();
 }
 
+// The FP32 pre-pass as a grid of resident blocks, each walking a contiguous chunk of items:
+// first the RoPE items (positions [32 pb, 32 pb + 32) of one plane of q and of k; the thread of
+// position row r and pair group g computes its 8 (cos, sin) once per position block), then the
+// transpose items (32 keys of one v plane).
 __global__ void __launch_bounds__(kRopeF32Threads) rope_f32_kernel(RopeF32Args a) {
   // the attention grid may be scheduled now; it waits for this grid before reading its output
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-  if (blockIdx.z == 1 || a.q == nullptr) {
-    __shared__ float tile[2 * kHeadDim][kRopeF32Rows + 1];
-    transpose_v_item(a, tile);
-    return;
-  }
+  __shared__ float tile[2 * kHeadDim][kRopeF32Rows + 1];
+  const long long n_pb = (a.L + kRopeF32Rows - 1) / kRopeF32Rows;
+  const long long n_rope = a.q ? n_pb * a.planes : 0;
+  const long long n_items = n_rope + (a.v ? n_pb * a.planes_v : 0);
+  const long long per = (n_items + gridDim.x - 1) / gridDim.x;
+  const long long i0 = static_cast<long long>(blockIdx.x) * per;
+  const long long i1 = i0 + per < n_items ? i0 + per : n_items;
   const int r = threadIdx.x >> 2;
   const int g = threadIdx.x & 3;   // pairs [8g, 8g + 8)
-  const int l = blockIdx.x * kRopeF32Rows + r;
-  if (l >= a.L) return;
-  const int p = a.positions ? a.positions[l] : l;
-  const float pf = static_cast<float>(p);
-  float c[8], s[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const float theta = __fmul_rn(pf, a.inv_freq[8 * g + i]);
-    sincosf(theta, &s[i], &c[i]);
-  }
-  const size_t base = static_cast<size_t>(l) * kHeadDim + 8 * g;
   const size_t plane_stride = static_cast<size_t>(a.L) * kHeadDim;
-  for (long long pl = blockIdx.y; pl < a.planes; pl += gridDim.y) {
-    const size_t off = static_cast<size_t>(pl) * plane_stride + base;
+  long long cur_pb = -1;
+  float c[8], s[8];
+  for (long long it = i0; it < i1; ++it) {
+    if (it >= n_rope) {
+      const long long j = it - n_rope;
+      transpose_v_item(a, static_cast<int>(j / a.planes_v) * kRopeF32Rows, j % a.planes_v, tile);
+      continue;
+    }
+    const long long pb = it / a.planes, pl = it % a.planes;
+    const int l = static_cast<int>(pb) * kRopeF32Rows + r;
+    if (l >= a.L) continue;
+    const size_t off = static_cast<size_t>(pl) * plane_stride + static_cast<size_t>(l) * kHeadDim + 8 * g;
+    // q and k of this row and pair group: all 8 loads before the first use
+    float4 v4[2][4];
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
       const float* src = t == 0 ? a.q : a.k;
+      v4[t][0] = ld_stream_f4(src + off);
+      v4[t][1] = ld_stream_f4(src + off + 4);
+      v4[t][2] = ld_stream_f4(src + off + 32);
+      v4[t][3] = ld_stream_f4(src + off + 36);
+    }
+    if (pb != cur_pb) {
+      cur_pb = pb;
+      const int p = a.positions ? a.positions[l] : l;
+      const float pf = static_cast<float>(p);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float theta = __fmul_rn(pf, a.inv_freq[8 * g + i]);
+        sincosf(theta, &s[i], &c[i]);
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
       float* dst = t == 0 ? a.q_out : a.k_out;
-      const float4 l0 = ld_stream_f4(src + off), l1 = ld_stream_f4(src + off + 4);
-      const float4 h0 = ld_stream_f4(src + off + 32), h1 = ld_stream_f4(src + off + 36);
-      float lo[8] = {l0.x, l0.y, l0.z, l0.w, l1.x, l1.y, l1.z, l1.w};
-      float hi[8] = {h0.x, h0.y, h0.z, h0.w, h1.x, h1.y, h1.z, h1.w};
+      float lo[8] = {v4[t][0].x, v4[t][0].y, v4[t][0].z, v4[t][0].w, v4[t][1].x, v4[t][1].y, v4[t][1].z, v4[t][1].w};
+      float hi[8] = {v4[t][2].x, v4[t][2].y, v4[t][2].z, v4[t][2].w, v4[t][3].x, v4[t][3].y, v4[t][3].z, v4[t][3].w};
       rope_rotate8_f32(lo, hi, c, s);
       st_f4(dst + off, make_float4(lo[0], lo[1], lo[2], lo[3]));
       st_f4(dst + off + 4, make_float4(lo[4], lo[5], lo[6], lo[7]));
@@ -521,15 +547,19 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
 }  // namespace
 
 cudaError_t rope_f32_launch(const RopeF32Args& a, int num_sms, cudaStream_t stream) {
-  const unsigned gx = static_cast<unsigned>((a.L + kRopeF32Rows - 1) / kRopeF32Rows);
-  // about 8 resident blocks per SM over the whole grid; every block walks planes by the grid's y
-  long long gy = (static_cast<long long>(num_sms) * 8 + gx - 1) / gx;
-  const long long planes = a.q ? a.planes : a.planes_v;
-  if (gy > planes) gy = planes;
-  if (gy < 1) gy = 1;
-  if (gy > 65535) gy = 65535;
-  // z = 0: RoPE of q and k (when given); z = 1 (or the only z without q): the v transpose
-  rope_f32_kernel<<<dim3(gx, static_cast<unsigned>(gy), (a.q && a.v) ? 2u : 1u), kRopeF32Threads, 0, stream>>>(a);
+  // one block per resident slot (the occupancy calculator's count, looked up once)
+  static const int per_sm = [] {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, rope_f32_kernel, kRopeF32Threads, 0) != cudaSuccess || n < 1)
+      n = 1;
+    return n;
+  }();
+  const long long n_pb = (a.L + kRopeF32Rows - 1) / kRopeF32Rows;
+  const long long items = n_pb * ((a.q ? a.planes : 0) + (a.v ? a.planes_v : 0));
+  long long grid = static_cast<long long>(per_sm) * num_sms;
+  if (grid > items) grid = items;
+  if (grid < 1) grid = 1;
+  rope_f32_kernel<<<static_cast<unsigned>(grid), kRopeF32Threads, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
