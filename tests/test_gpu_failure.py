@@ -17,35 +17,45 @@ import synth
 
 pytestmark = pytest.mark.gpu
 
-TDT = {"fp16": torch.float16, "bf16": torch.bfloat16}
+TDT = {"fp16": torch.float16, "bf16": torch.bfloat16, "fp32": torch.float32}
+SA_DT = {"fp16": sa.SA_FP16, "bf16": sa.SA_BF16, "fp32": sa.SA_FP32}
 
 
 def _dev(bits, dtype):
-    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(TDT[dtype])
+    raw = np.ascontiguousarray(bits).view(np.int32 if dtype == "fp32" else np.int16)
+    return torch.from_numpy(raw).cuda().view(TDT[dtype])
 
 
 def _run(h, x, stream):
     w = x["workload"]
     q, k, v = _dev(x["q"], w.dtype), _dev(x["k"], w.dtype), _dev(x["v"], w.dtype)
     out = torch.zeros((w.B, w.H, w.L, w.dv), dtype=TDT[w.dtype], device="cuda")
-    nbytes = sa.sa_rope_attn_workspace_size(w.B, w.H, w.L, w.d, w.differential)
+    nbytes = sa.sa_rope_attn_workspace_bytes(w.B, w.H, w.L, w.d, w.differential, SA_DT[w.dtype])
     ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     lam = None if x["lam"] is None else [float(t) for t in x["lam"]]
     sa.sa_rope_attn(h, q.data_ptr(), k.data_ptr(), v.data_ptr(), None, out.data_ptr(), w.B, w.H, w.L,
-                    w.d, w.window, lam, sa.SA_FP16 if w.dtype == "fp16" else sa.SA_BF16,
-                    ws.data_ptr(), nbytes, stream)
+                    w.d, w.window, lam, SA_DT[w.dtype], ws.data_ptr(), nbytes, stream)
     torch.cuda.synchronize()
     return out
 
 
-@pytest.mark.parametrize("variant", ["standard", "differential"])
+# one shape per attention kernel: the general kernel (standard and differential), the
+# narrow-window kernel (differential, window 17: persistent CTAs, output warps) and the TF32
+# kernel (FP32 inputs)
+@pytest.mark.parametrize("variant", ["standard", "differential", "narrow_window", "fp32"])
 def test_pipeline_timeout_is_reported_and_recoverable(variant):
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
     if variant == "standard":
         w = synth.Workload("fail_std", B=1, H=8, L=2048, seed=41)
-    else:
+    elif variant == "differential":
         w = synth.Workload("fail_diff", B=1, H=4, L=2048, nmaps=2, dv=128, dtype="bf16", seed=42,
+                           lam=("uniform", 0.2, 0.8))
+    elif variant == "narrow_window":
+        w = synth.Workload("fail_swa", B=1, H=8, L=4096, nmaps=2, dv=128, dtype="bf16", window=17, seed=44,
+                           lam=("uniform", 0.2, 0.8))
+    else:
+        w = synth.Workload("fail_f32", B=1, H=4, L=2048, nmaps=2, dv=128, dtype="fp32", window=256, seed=45,
                            lam=("uniform", 0.2, 0.8))
     x = synth.make_inputs(w)
     stream = torch.cuda.current_stream().cuda_stream
