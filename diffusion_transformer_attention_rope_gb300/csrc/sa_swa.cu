@@ -12,12 +12,13 @@
 //   - 64-key tiles (the span of a 128-row block at +-17 is 162 keys: 3 tiles of 64 instead of 2
 //     of 128), S double-buffered per map in tensor memory and P (fp16/bf16) written over its S
 //     buffer, the A operand of a TS P.V MMA, so P never goes through shared memory;
-//   - Q double-buffered in shared memory: the next unit's raw Q arrives while this one runs,
-//     and the softmax warps rotate it right after this unit's last key tile, before this unit's
-//     epilogue, so the next unit's first S MMAs run while this unit's last P.V and epilogue do;
+//   - Q double-buffered in shared memory: the next unit's raw Q arrives while this one runs
+//     (the first two units' Q are copied before the wait for the K pass; the V ring starts
+//     once the first Q has landed);
 //   - the rings, S buffers and their barriers run on across units with a CTA-wide tile count
 //     (the P.V completion is tracked per S buffer, so an S MMA waits only for the P.V that read
-//     its buffer); the first P.V of a unit (which overwrites O) waits until the previous
+//     its buffer), and the issuers run the S MMAs two tiles ahead of the P.V MMAs across unit
+//     boundaries; the first P.V of a unit (which overwrites O) waits until the previous
 //     epilogue has read O;
 //   - the RoPE of each unit's Q and each unit's epilogue run on a warpgroup of their own (the
 //     output warps), so the softmax warps go from one unit's last key tile straight to the next
