@@ -111,7 +111,7 @@ __device__ __forceinline__ void transpose_v_item(const RopeF32Args& a, int l0, l
 // first the RoPE items (positions [32 pb, 32 pb + 32) of one plane of q and of k; the thread of
 // position row r and pair group g computes its 8 (cos, sin) once per position block), then the
 // transpose items (32 keys of one v plane).
-__global__ void __launch_bounds__(kRopeF32Threads) rope_f32_kernel(RopeF32Args a) {
+__global__ void __launch_bounds__(kRopeF32Threads, 8) rope_f32_kernel(RopeF32Args a) {
   // the attention grid may be scheduled now; it waits for this grid before reading its output
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   __shared__ float tile[2 * kHeadDim][kRopeF32Rows + 1];
