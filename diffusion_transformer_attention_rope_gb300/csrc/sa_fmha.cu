@@ -12,9 +12,10 @@
 //   warps 0-3, 4-7  softmax warpgroups, one per tile / map (stream s): thread = query row =
 //                   TMEM lane; with a raw q they first rotate their Q row in shared memory
 //                   (RoPE prologue, from the RoPE pass's FP32 (cos, sin) table).
-//   warp 8          TMA producer of Q and of the K ring (128 keys per stage).
-//   warp 9          TMEM allocator and the MMA issuer of stream 0.
-//   warp 10         the MMA issuer of stream 1.
+//   warp 8          TMA producer of Q and of the K ring (128 keys per stage); in the standard
+//                   kernel also the issuer of both streams' S MMAs.
+//   warp 9          TMEM allocator and the MMA issuer of stream 0 (P.V only, standard kernel).
+//   warp 10         the MMA issuer of stream 1 (likewise).
 //   warp 11         TMA producer of the V ring.
 // Per K/V tile and stream s:
 //   S_s = Q_s K^T      tcgen05.mma, A and B from 128B-swizzled smem, fp32 into TMEM
@@ -69,8 +70,8 @@ struct Cfg {
   static constexpr int OFF_P = OFF_V + NSV * V_STAGE;
   static constexpr int OFF_BAR = OFF_P + P_BYTES;
   // barriers: q_full, q_ready[2], k_full[NSK], k_empty[NSK], v_full[NSV], v_empty[NSV], s_full[2],
-  //           p_full[2], pv_done[2], s_free[2], o_full[2], drain[2], turn[2][4]
-  static constexpr int NBAR = 1 + 2 + 2 * NSK + 2 * NSV + 2 + 2 + 2 + 2 + 2 + 2 + 8;
+  //           p_full[2], pv_done[2], s_free[2], o_full[2], drain[2], turn[2][4], drain_k
+  static constexpr int NBAR = 1 + 2 + 2 * NSK + 2 * NSV + 2 + 2 + 2 + 2 + 2 + 2 + 8 + 1;
   static constexpr int OFF_MISC = OFF_BAR + 8 * NBAR;           // tmem base, abort flag, ticket
   static constexpr int OFF_LSUM = OFF_MISC + 16;                // float [2][128]
   static constexpr int SMEM_USED = OFF_LSUM + 2 * kBlockM * 4;
@@ -87,6 +88,8 @@ static_assert(Cfg<false>::SMEM_USED > 114 * 1024, "one CTA per SM keeps TMEM all
 struct Barriers {
   uint32_t q_full, q_ready0, k_full0, k_empty0, v_full0, v_empty0, s_full0, p_full0, pv_done0, s_free0, o_full0,
       drain0, turn0;
+  // the S MMAs of the standard kernel's K producer warp have completed (before TMEM is released)
+  uint32_t drain_k;
   __device__ uint32_t q_ready(int s) const { return q_ready0 + 8 * s; }
   __device__ uint32_t k_full(int i) const { return k_full0 + 8 * i; }
   __device__ uint32_t k_empty(int i) const { return k_empty0 + 8 * i; }
@@ -366,6 +369,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
   bar.o_full0 = bar.s_free0 + 16;
   bar.drain0 = bar.o_full0 + 16;
   bar.turn0 = bar.drain0 + 16;
+  bar.drain_k = bar.turn0 + 64;
 
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
@@ -411,7 +415,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     for (int s = 0; s < 2; ++s) mbar_init(bar.q_ready(s), 4);   // one arrival per softmax warp
     for (int i = 0; i < C::NSK; ++i) {
       mbar_init(bar.k_full(i), 1);
-      mbar_init(bar.k_empty(i), 2);    // one commit from each MMA issuer
+      mbar_init(bar.k_empty(i), 2);    // one commit per stream's S MMAs
     }
     for (int i = 0; i < C::NSV; ++i) {
       mbar_init(bar.v_full(i), 1);
@@ -426,6 +430,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       mbar_init(bar.drain(s), 1);
       for (int q = 0; q < 4; ++q) mbar_init(bar.turn(s, q), 1);
     }
+    mbar_init(bar.drain_k, 1);
     *abort_flag = 0;
     mbar_fence_init();
   }
@@ -480,10 +485,10 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       asm volatile("griddepcontrol.wait;" ::: "memory");
     }
     int issued = 0;
-    for (int it = 0; it < n_tiles; ++it) {
+    auto load_k = [&](int it) {
       const int st = it % C::NSK;
       if (!pwait_w(bar.k_empty(st), ((it / C::NSK) & 1) ^ 1, abort_flag, a.err, kErrProducer, tmo))
-        break;
+        return false;
       const int key0 = k_first + (t_lo + it) * kBlockN;
       const uint32_t k_dst = sK + st * C::K_STAGE;
       mbar_arrive_expect_tx_w(bar.k_full(st), C::K_STAGE);
@@ -494,6 +499,49 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         tma_load_3d_w(k_dst, &tm_k, bar.k_full(st), 0, key0, bh);
       }
       issued = it + 1;
+      return true;
+    };
+    if constexpr (DIFF) {
+      for (int it = 0; it < n_tiles; ++it)
+        if (!load_k(it)) break;
+    } else {
+      // The standard kernel's K producer also issues both streams' S MMAs (the MMA issuers keep
+      // the P.V MMAs): each SM sub-partition that hosts an issuing warp gives some of its issue
+      // slots to it, and its softmax warps then finish their tiles last, so the issue work is
+      // spread over three sub-partitions instead of two.  Per tile: S_0(j) and S_1(j), each once
+      // the softmax warps hold S_s(j - 1) in registers (S is single-buffered per stream), then
+      // K(j + NSK - 1) into the stage that S(j - 1) has released.
+      constexpr uint32_t idesc_s = make_idesc_f16(kBlockM, kBlockN, BF16, false);
+      const uint64_t dq0 = smem_desc_sw128(sQ, 16, 1024);
+      const uint64_t dq1 = smem_desc_sw128(sQ + kTile, 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(sK, 16, 1024);
+      const uint32_t q_bar0 = raw_q ? bar.q_ready(0) : bar.q_full;
+      const uint32_t q_bar1 = raw_q ? bar.q_ready(1) : bar.q_full;
+      constexpr int eb = kErrMma;
+      bool ok = true;
+      for (int it = 0; ok && it < C::NSK - 1 && it < n_tiles; ++it) ok = load_k(it);
+      for (int j = 0; ok && j < n_tiles; ++j) {
+        const int st = j % C::NSK;
+        const uint64_t dk = dk0 + static_cast<uint64_t>(st * (C::K_STAGE >> 4));
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          ok = pwait_w(j == 0 ? (s == 0 ? q_bar0 : q_bar1) : bar.s_free(s), j == 0 ? 0u : static_cast<uint32_t>((j - 1) & 1),
+                       abort_flag, a.err, eb, tmo) &&
+               pwait_w(bar.k_full(st), (j / C::NSK) & 1, abort_flag, a.err, eb, tmo);
+          if (!ok) break;
+          tc_fence_after();
+          const uint64_t dq = s == 0 ? dq0 : dq1;
+#pragma unroll
+          for (int kk = 0; kk < kHeadDim / 16; ++kk)
+            umma_ss_w(tmem + C::s_col(s), dq + 2 * kk, dk + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
+          umma_commit_w(bar.s_full(s));
+          umma_commit_w(bar.k_empty(st));
+        }
+        if (ok && j + C::NSK - 1 < n_tiles) ok = load_k(j + C::NSK - 1);
+      }
+      // no S MMA of this warp may still be running when TMEM is released
+      umma_commit_w(bar.drain_k);
+      mbar_wait_limit(bar.drain_k, 0, drain_tmo);
     }
     // Let the copies already issued land before the CTA's shared memory goes away (after a
     // normal run these phases have completed and the waits return at once).
@@ -522,10 +570,12 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ MMA issuers
-    // One issuing warp per stream s (query tile s, or map s).  After the prologue each issues,
-    // per tile, one block: P.V_s(i) as soon as P_s(i) is ready, then S_s(i + 2) (it overwrites
-    // S_s(i + 1), which the softmax warps load right after P_s(i)).  The stream index is a
-    // compile-time constant in each instance so that every operand is warp-uniform.
+    // One issuing warp per stream s (query tile s, or map s).  Differential kernel: after the
+    // prologue each issues, per tile, one block: P.V_s(i) as soon as P_s(i) is ready, then
+    // S_s(i + 2) (it overwrites S_s(i + 1), which the softmax warps load right after P_s(i)).
+    // Standard kernel: P.V_s(i) only (the K producer issues the S MMAs; P has TMEM columns of
+    // its own, so no S MMA can overwrite a P that a P.V MMA has yet to read).  The stream index
+    // is a compile-time constant in each instance so that every operand is warp-uniform.
     auto issuer = [&](auto stream) {
       constexpr int s = decltype(stream)::value;
       constexpr uint32_t idesc_s = make_idesc_f16(kBlockM, kBlockN, BF16, false);
@@ -553,12 +603,15 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       };
       // Q tile s as the MMA reads it: straight from the TMA, or after the softmax warps' RoPE
       const uint32_t q_bar = a.cs != nullptr ? bar.q_ready(s) : bar.q_full;
-      bool ok = pwait_w(q_bar, 0, abort_flag, a.err, eb, tmo) && wait_k(0);
-      if (ok) {
-        tc_fence_after();
-        issue_s(0);
+      bool ok = true;
+      if constexpr (DIFF) {
+        ok = pwait_w(q_bar, 0, abort_flag, a.err, eb, tmo) && wait_k(0);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+        }
       }
-      if (ok && n_tiles > 1) {
+      if (DIFF && ok && n_tiles > 1) {
         // S_s(1) once the softmax warps hold S_s(0) in registers
         ok = pwait_w(bar.s_free(s), 0, abort_flag, a.err, eb, tmo) && wait_k(1);
         if (ok) {
@@ -585,7 +638,7 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
         umma_commit_w(bar.pv_done(s));
         umma_commit_w(bar.v_empty(sv));
         if (it + 1 == n_tiles) umma_commit_w(bar.o_full(s));
-        if (it + 2 < n_tiles) {
+        if (DIFF && it + 2 < n_tiles) {
           ok = pwait_w(bar.s_free(s), (it + 1) & 1, abort_flag, a.err, eb, tmo) && wait_k(it + 2);
           if (!ok) break;
           tc_fence_after();
