@@ -580,6 +580,8 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
     Unit x = unit_of(a, u_begin);
     bool ok = n_units > 0 ? q_prologue(0, x) : true;
     for (int ui = 0; ok && ui < n_units; ++ui, x = next_unit(a, x)) {
+      // lambda_h now: its load latency then stays off the path from O ready to O released
+      const float lam = a.lambda[x.bh % a.H];
       // the next unit's Q first: its S MMAs then start as soon as this unit's last tiles free
       // the S buffers
       if (ui + 1 < n_units && !q_prologue(ui + 1, next_unit(a, x))) {
@@ -599,7 +601,10 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
       if (lane == 0) mbar_arrive(bar.l_free(ui & 1));
       const float inv0 = l0 > 0.0f ? 1.0f / l0 : 0.0f;
       const float inv1 = l1 > 0.0f ? 1.0f / l1 : 0.0f;
-      const float lam = a.lambda[x.bh % a.H];
+      // out = O_0 inv0 + O_1 (-lambda_h inv1), two elements per paired FP32 multiply and fma
+      const float2 a2 = make_float2(inv0, inv0);
+      const float nb = -lam * inv1;
+      const float2 b2 = make_float2(nb, nb);
       // this warp's 32 rows x 128 values go through its staging block (two 32 x 64 boxes,
       // 128-byte swizzle: 16-byte chunk c of row i at c ^ (i & 7)) and two TMA stores
       if (lane == 0) bulk_wait_read();   // the previous unit's stores have read the block
@@ -611,12 +616,18 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
         tmem_ld32_nowait(tmem + o_col(1) + lane_off + 32 * cc, o1);
         tmem_wait_ld_32(o0);
         tmem_wait_ld_32(o1);
+        if (cc == 3) {
+          // O has been read: the next unit's first P.V may overwrite it
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar.o_free());
+        }
         uint32_t pkd[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
-          const float y0 = fmaf(-lam, __uint_as_float(o1[2 * j]) * inv1, __uint_as_float(o0[2 * j]) * inv0);
-          const float y1 = fmaf(-lam, __uint_as_float(o1[2 * j + 1]) * inv1, __uint_as_float(o0[2 * j + 1]) * inv0);
-          pkd[j] = pack2<BF16>(y0, y1);
+          const float2 y = ffma2(make_float2(__uint_as_float(o1[2 * j]), __uint_as_float(o1[2 * j + 1])), b2,
+                                 fmul2(make_float2(__uint_as_float(o0[2 * j]), __uint_as_float(o0[2 * j + 1])), a2));
+          pkd[j] = pack2<BF16>(y.x, y.y);
         }
         const uint32_t row = stage + (cc >> 1) * kStageBox + lane * 128;
 #pragma unroll
@@ -624,12 +635,10 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
           st_shared_v4(row + (((4 * (cc & 1) + j) ^ (lane & 7)) << 4), pkd[4 * j], pkd[4 * j + 1], pkd[4 * j + 2],
                        pkd[4 * j + 3]);
       }
-      // O has been read: the next unit's first P.V may overwrite it
-      tc_fence_before();
+      // the staging block is complete: the TMA stores may read it
       asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
       __syncwarp();
       if (lane == 0) {
-        mbar_arrive(bar.o_free());
         // rows past L are outside the tensor and not written
         tma_store_3d(&tm_o, stage, 0, x.q0 + 32 * quarter, x.bh);
         tma_store_3d(&tm_o, stage + kStageBox, 64, x.q0 + 32 * quarter, x.bh);
