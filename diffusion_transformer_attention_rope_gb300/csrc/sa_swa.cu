@@ -460,17 +460,33 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
         if (!ok) break;
         tc_fence_after();
         const uint32_t sa = tmem + s_col(m, b) + lane_off;
+        const int key0 = x.k_first + t * kBN;
+        const bool need_mask = (key0 + kBN > L) || !(key0 >= rows_hi - w && key0 + kBN - 1 <= rows_lo + w);
+        // this row's keys are columns [j_lo, j_hi) of the tile
+        const int j_lo = grow - w - key0;
+        const int j_hi = min(L - key0, grow + w + 1 - key0);
+        if (need_mask && __all_sync(0xffffffffu, max(j_lo, 0) >= min(j_hi, kBN))) {
+          // No row of this warp has a key in this tile (the band of 32 rows misses it): P = 0,
+          // and the rows' max and sum stay as they are (exactly what the masked path gives).
+          // The warp goes straight on to its next tile, so on a narrow band the warps whose
+          // rows miss a unit's first or last tile run ahead of the others.
+          uint32_t z[kBN / 2];
+#pragma unroll
+          for (int j = 0; j < kBN / 2; ++j) z[j] = 0u;
+          tmem_st32(sa, z);
+          tmem_wait_st();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar.p_full(m, b));
+          continue;
+        }
         uint32_t sr[kBN];
         float mt;
         tmem_ld64_max_nowait(sa, sr, mt);
         tmem_wait_ld_64_max(sr, mt);
-        const int key0 = x.k_first + t * kBN;
-        const bool need_mask = (key0 + kBN > L) || !(key0 >= rows_hi - w && key0 + kBN - 1 <= rows_lo + w);
         if (need_mask) {
-          // this row's keys are columns [j_lo, j_hi) of the tile; the loaded maximum also
-          // covers the masked columns, so the row max is taken again over the masked row
-          const int j_lo = grow - w - key0;
-          const int j_hi = min(L - key0, grow + w + 1 - key0);
+          // the loaded maximum also covers the masked columns, so the row max is taken again
+          // over the masked row
 #pragma unroll
           for (int j = 0; j < kBN; ++j)
             if (j < j_lo || j >= j_hi) sr[j] = __float_as_uint(-INFINITY);
