@@ -392,6 +392,9 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
       if (!pwait_w(bar.k_full(s_g % kNS), (s_g / kNS) & 1, abort_flag, a.err, eb, tmo)) return false;
       tc_fence_after();
       issue_s(s_g, dq0 + static_cast<uint64_t>(qb * (kQBuf >> 4)));
+      // the unit's last S MMA is the last reader of its Q buffer: the next Q may land there once
+      // it has completed
+      if (s_t + 1 == sx.n_tiles) umma_commit_w(bar.q_free(qb));
       ++s_g;
       if (++s_t == sx.n_tiles) {
         s_t = 0;
@@ -404,7 +407,6 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
     int g = 0;
     Unit x = unit_of(a, u_begin);
     for (int ui = 0; ok && ui < n_units; ++ui, x = next_unit(a, x)) {
-      const int qb = ui & 1;
       const int n = x.n_tiles;
       for (int t = 0; t < n; ++t) {
         const int gg = g + t;
@@ -422,10 +424,7 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
           umma_ts_w(tmem + o_col(m), a_p + 8 * kk, dv + 128 * kk, idesc_o, (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit_w(bar.pv_done(m, gg & 1));
         umma_commit_w(bar.v_empty(sv));
-        if (t + 1 == n) {
-          umma_commit_w(bar.o_full(m));
-          umma_commit_w(bar.q_free(qb));
-        }
+        if (t + 1 == n) umma_commit_w(bar.o_full(m));
         // S(gg + 2), of this unit or of the next ones
         ok = issue_next_s();
         if (!ok) break;
