@@ -317,6 +317,13 @@ __device__ __forceinline__ float round_tf32(float x) {
   return __uint_as_float(r);
 }
 
+// a + b clamped to [0, 1] (FMA pipe)
+__device__ __forceinline__ float sat_add(float a, float b) {
+  float d;
+  asm("add.rn.sat.f32 %0, %1, %2;" : "=f"(d) : "f"(a), "f"(b));
+  return d;
+}
+
 // max(a, b, c) in one instruction (sm_100+).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;

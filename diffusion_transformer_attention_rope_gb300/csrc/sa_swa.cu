@@ -484,11 +484,23 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
         tmem_ld64_max_nowait(sa, sr, mt);
         tmem_wait_ld_64_max(sr, mt);
         if (need_mask) {
-          // the loaded maximum also covers the masked columns, so the row max is taken again
-          // over the masked row
+          // The loaded maximum also covers the masked columns, so the row max is taken again
+          // over the masked row.  The mask runs on the FMA pipe (the ALU pipe, half as wide, is
+          // the one the compares and selects would load): a_j = sat(1 - j_lo + j) and
+          // b_j = sat(j_hi - j) are both 1 exactly on the row's keys, and s_j + (a_j b_j - 1) 2^100
+          // leaves those scores exact and puts every other one far below any score (its
+          // exponential is 0, as for -inf); a row with no key here gets -inf as its max.
+          const float fa = static_cast<float>(1 - j_lo), fb = static_cast<float>(j_hi);
 #pragma unroll
-          for (int j = 0; j < kBN; ++j)
-            if (j < j_lo || j >= j_hi) sr[j] = __float_as_uint(-INFINITY);
+          for (int j = 0; j < kBN; j += 2) {
+            const float2 a2 = make_float2(sat_add(fa, static_cast<float>(j)), sat_add(fa, static_cast<float>(j + 1)));
+            const float2 b2 = make_float2(sat_add(fb, -static_cast<float>(j)), sat_add(fb, -static_cast<float>(j + 1)));
+            const float2 w2 = ffma2(a2, b2, make_float2(-1.0f, -1.0f));
+            const float2 s2 = ffma2(w2, make_float2(0x1p100f, 0x1p100f),
+                                    make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])));
+            sr[j] = __float_as_uint(s2.x);
+            sr[j + 1] = __float_as_uint(s2.y);
+          }
           // 8 independent chains; chain q covers elements q, q + 8, ..., q + 56
           float mx[8];
 #pragma unroll
@@ -499,6 +511,7 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
             for (int q = 0; q < 8; ++q) mx[q] = fmax3(mx[q], __uint_as_float(sr[j + q]), __uint_as_float(sr[j + 8 + q]));
           }
           mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+          if (mt < -0x1p99f) mt = -INFINITY;
         }
         float f = 1.0f;
         bool rescale = false;
