@@ -431,23 +431,57 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const uint32_t sa = tmem + s_col(m, b) + lane_off;
+      const int key0 = k_first + it * kBN;
+      const bool need_mask = (key0 + kBN > L) || (w >= 0 && !(key0 >= rows_hi - w && key0 + kBN - 1 <= rows_lo + w));
+      // this row's keys are columns [j_lo, j_hi) of the tile
+      const int j_lo = w >= 0 ? grow - w - key0 : 0;
+      const int j_hi = w >= 0 ? min(L - key0, grow + w + 1 - key0) : L - key0;
+      if (need_mask && __all_sync(0xffffffffu, max(j_lo, 0) >= min(j_hi, kBN))) {
+        // No row of this warp has a key in this tile: P = 0, and the rows' max and sum stay as
+        // they are (exactly what the masked path gives); the warp goes on to its next tile.
+        uint32_t z[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) z[j] = 0u;
+        tmem_st32(sa, z);
+        tmem_st32(sa + 32, z);
+        tmem_wait_st();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar.p_full(m, b));
+        continue;
+      }
       uint32_t sr[kBN];
       float mt;
       tmem_ld64_max_nowait(sa, sr, mt);
       tmem_wait_ld_64_max(sr, mt);
-      const int key0 = k_first + it * kBN;
-      const bool need_mask = (key0 + kBN > L) || (w >= 0 && !(key0 >= rows_hi - w && key0 + kBN - 1 <= rows_lo + w));
       if (need_mask) {
-        // this row's keys are columns [j_lo, j_hi) of the tile; the loaded maximum also covers
-        // the masked columns, so the row max is taken again over the masked row
-        const int j_lo = w >= 0 ? grow - w - key0 : 0;
-        const int j_hi = w >= 0 ? min(L - key0, grow + w + 1 - key0) : L - key0;
-        mt = -INFINITY;
+        // The loaded maximum also covers the masked columns, so the row max is taken again over
+        // the masked row.  The mask runs on the FMA pipe: a_j = sat(1 - j_lo + j) and
+        // b_j = sat(j_hi - j) are both 1 exactly on the row's keys, and s_j + (a_j b_j - 1) 2^100
+        // leaves those scores exact and puts every other one far below any score (its
+        // exponential is 0, as for -inf); a row with no key here gets -inf as its max.
+        const float fa = static_cast<float>(1 - j_lo), fb = static_cast<float>(j_hi);
 #pragma unroll
-        for (int j = 0; j < kBN; ++j) {
-          if (j < j_lo || j >= j_hi) sr[j] = __float_as_uint(-INFINITY);
-          mt = fmaxf(mt, __uint_as_float(sr[j]));
+        for (int j = 0; j < kBN; j += 2) {
+          const float2 a2 = make_float2(sat_add(fa, static_cast<float>(j)), sat_add(fa, static_cast<float>(j + 1)));
+          const float2 b2 = make_float2(sat_add(fb, -static_cast<float>(j)), sat_add(fb, -static_cast<float>(j + 1)));
+          const float2 w2 = ffma2(a2, b2, make_float2(-1.0f, -1.0f));
+          const float2 s2 = ffma2(w2, make_float2(0x1p100f, 0x1p100f),
+                                  make_float2(__uint_as_float(sr[j]), __uint_as_float(sr[j + 1])));
+          sr[j] = __float_as_uint(s2.x);
+          sr[j + 1] = __float_as_uint(s2.y);
         }
+        // 8 independent chains; chain q covers elements q, q + 8, ..., q + 56
+        float mx[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) mx[q] = fmaxf(__uint_as_float(sr[q]), __uint_as_float(sr[q + 8]));
+#pragma unroll
+        for (int j = 16; j < kBN; j += 16) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q) mx[q] = fmax3(mx[q], __uint_as_float(sr[j + q]), __uint_as_float(sr[j + 8 + q]));
+        }
+        mt = fmax3(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], mx[5]), fmaxf(mx[6], mx[7]));
+        if (mt < -0x1p99f) mt = -INFINITY;
       }
       float f = 1.0f;
       bool rescale = false;
