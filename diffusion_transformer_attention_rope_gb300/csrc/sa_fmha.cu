@@ -172,8 +172,8 @@ __device__ __noinline__ bool q_rope_prologue(const float2* cs, int cs_stride, bo
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         cg[2 * i] = t[4 * g + i].x;
-        sg[2 * i] = t[4 * g + i].y;
-        cg[2 * i + 1] = t[4 * g + i].z;
+        cg[2 * i + 1] = t[4 * g + i].y;
+        sg[2 * i] = t[4 * g + i].z;
         sg[2 * i + 1] = t[4 * g + i].w;
       }
       uint4 olo, ohi;

@@ -452,6 +452,18 @@ __device__ __forceinline__ void tmem_wait_ld_64_max(uint32_t* r, float& mx) {
 // RoPE of 8 rotate-half pairs in FP32, cast back: lo = x[8g .. 8g+8), hi = x[32+8g .. 32+8g+8)
 // (8 fp16/bf16 values each), c/s the pairs' cos/sin.  The pre-pass and the attention kernel's
 // Q prologue both use this, so a row rotated by either has the same bits.
+// Two rotation pairs at once, in paired FP32 operations with each element's own rounding steps:
+// x' = fma(x, cos, -(y sin)) and y' = fma(y, cos, x sin) for a = (x_i, x_{i+1}),
+// b = (x_{i+32}, x_{i+33}), then the RNE cast.
+template <bool BF16>
+__device__ __forceinline__ void rope_pair2(float2 a, float2 b, float2 c2, float2 s2, uint32_t& lo, uint32_t& hi) {
+  const float2 nbs = fmul2(b, fmul2(s2, make_float2(-1.0f, -1.0f)));   // -(y sin), exactly
+  const float2 x = ffma2(a, c2, nbs);
+  const float2 y = ffma2(b, c2, fmul2(a, s2));
+  lo = pack2<BF16>(x.x, x.y);
+  hi = pack2<BF16>(y.x, y.y);
+}
+
 template <bool BF16>
 __device__ __forceinline__ void rope_rotate8(const uint4& lo, const uint4& hi, const float (&c)[8],
                                        const float (&s)[8], uint4& out_lo, uint4& out_hi) {
@@ -462,9 +474,7 @@ __device__ __forceinline__ void rope_rotate8(const uint4& lo, const uint4& hi, c
   for (int j = 0; j < 4; ++j) {
     const float2 a = unpack2<BF16>(lw[j]);  // x_i, x_{i+1}
     const float2 b = unpack2<BF16>(hw[j]);  // x_{i+32}, x_{i+33}
-    const int i0 = 2 * j, i1 = 2 * j + 1;
-    ol[j] = pack2<BF16>(fmaf(a.x, c[i0], -(b.x * s[i0])), fmaf(a.y, c[i1], -(b.y * s[i1])));
-    oh[j] = pack2<BF16>(fmaf(b.x, c[i0], a.x * s[i0]), fmaf(b.y, c[i1], a.y * s[i1]));
+    rope_pair2<BF16>(a, b, make_float2(c[2 * j], c[2 * j + 1]), make_float2(s[2 * j], s[2 * j + 1]), ol[j], oh[j]);
   }
   out_lo = make_uint4(ol[0], ol[1], ol[2], ol[3]);
   out_hi = make_uint4(oh[0], oh[1], oh[2], oh[3]);
@@ -512,8 +522,7 @@ __device__ __forceinline__ void rope_rotate8_scaled(const uint4& lo, const uint4
     a.y = __fmul_rn(a.y, glo[i1]);
     b.x = __fmul_rn(b.x, ghi[i0]);
     b.y = __fmul_rn(b.y, ghi[i1]);
-    ol[j] = pack2<BF16>(fmaf(a.x, c[i0], -(b.x * s[i0])), fmaf(a.y, c[i1], -(b.y * s[i1])));
-    oh[j] = pack2<BF16>(fmaf(b.x, c[i0], a.x * s[i0]), fmaf(b.y, c[i1], a.y * s[i1]));
+    rope_pair2<BF16>(a, b, make_float2(c[i0], c[i1]), make_float2(s[i0], s[i1]), ol[j], oh[j]);
   }
   out_lo = make_uint4(ol[0], ol[1], ol[2], ol[3]);
   out_hi = make_uint4(oh[0], oh[1], oh[2], oh[3]);

@@ -115,12 +115,13 @@ __device__ __forceinline__ void rope_item(const RopeArgs& a, const float (*s_gam
       have_cs = true;
       if (a.cs != nullptr && by == 0) {
         // this position's pairs [8g, 8g + 8) of the (cos, sin) table for the Q prologue; the
-        // table is [16][L] float4 (pairs 2m and 2m + 1 of position l at [m][l]), so that the
-        // prologue's loads of consecutive rows are contiguous
+        // table is [16][L] float4 (cos_2m, cos_2m+1, sin_2m, sin_2m+1 of position l at [m][l]), so
+        // that the prologue's loads of consecutive rows are contiguous and each (cos, cos) and
+        // (sin, sin) pair is one 64-bit operand of the paired FP32 rotation
         float4* t = reinterpret_cast<float4*>(a.cs);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          t[static_cast<size_t>(4 * g + i) * a.L + l] = make_float4(c[2 * i], s[2 * i], c[2 * i + 1], s[2 * i + 1]);
+          t[static_cast<size_t>(4 * g + i) * a.L + l] = make_float4(c[2 * i], c[2 * i + 1], s[2 * i], s[2 * i + 1]);
       }
     }
 #pragma unroll
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(kRopeThreads) rope_table_kernel(const __grid_c
   float4* t = reinterpret_cast<float4*>(a.cs);
 #pragma unroll
   for (int i = 0; i < 4; ++i)
-    t[static_cast<size_t>(4 * g + i) * a.L + l] = make_float4(c[2 * i], s[2 * i], c[2 * i + 1], s[2 * i + 1]);
+    t[static_cast<size_t>(4 * g + i) * a.L + l] = make_float4(c[2 * i], c[2 * i + 1], s[2 * i], s[2 * i + 1]);
 }
 
 // Resident blocks per SM of one variant (the fewer of its fp16 and bf16 forms).

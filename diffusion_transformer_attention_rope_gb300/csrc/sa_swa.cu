@@ -157,8 +157,8 @@ __device__ __noinline__ void rotate_q_rows(const float2* cs, int cs_stride, int 
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       cg[2 * i] = t[i].x;
-      sg[2 * i] = t[i].y;
-      cg[2 * i + 1] = t[i].z;
+      cg[2 * i + 1] = t[i].y;
+      sg[2 * i] = t[i].z;
       sg[2 * i + 1] = t[i].w;
     }
     uint4 olo, ohi;

@@ -298,8 +298,8 @@ SA_API sa_status sa_qknorm_rope_qk(sa_attn_t handle,
  *   (256 * L); 0 for invalid L.
  * sa_rope_k: k_rot = cast(RoPE_fp32(k)) (the layout of k) and the table of
  *   (cos, sin) of the FP32 angle fl(fl(p_l) * inv_freq[i]), i < 32,
- *   p_l = positions[l] or l, as float4 cs_table[m][l] = (cos_2m, sin_2m,
- *   cos_2m+1, sin_2m+1), m < 16 (rows of one pair-pair contiguous).
+ *   p_l = positions[l] or l, as float4 cs_table[m][l] = (cos_2m, cos_2m+1,
+ *   sin_2m, sin_2m+1), m < 16 (rows of one pair-pair contiguous).
  *   cs_table: device, 16-byte aligned.
  * sa_attn_fwd_rope_q: attention (as sa_attn_fwd) on the raw q, rotated in the
  *   kernel's prologue with cs_table in the pre-pass's arithmetic, so the output

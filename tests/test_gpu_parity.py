@@ -151,8 +151,8 @@ def test_q_rope_prologue_matches_prepass(attn, diff, dtype, window):
     # the table: cos and sin of the FP32 angle fl(fl(p) * inv_freq_i), to a few ulp
     inv = (10000.0 ** (-2.0 * np.arange(32) / 64.0)).astype(np.float32)
     ang = (pos.cpu().numpy().astype(np.float32)[:, None] * inv[None, :]).astype(np.float64)
-    # [16][L] float4 (cos_2m, sin_2m, cos_2m+1, sin_2m+1) -> [L][32][2]
-    t = cs.cpu().numpy().reshape(16, L, 2, 2).transpose(1, 0, 2, 3).reshape(L, 32, 2).astype(np.float64)
+    # [16][L] float4 (cos_2m, cos_2m+1, sin_2m, sin_2m+1) -> [L][32][2]
+    t = cs.cpu().numpy().reshape(16, L, 2, 2).transpose(1, 0, 3, 2).reshape(L, 32, 2).astype(np.float64)
     assert np.abs(t[..., 0] - np.cos(ang)).max() < 1e-6
     assert np.abs(t[..., 1] - np.sin(ang)).max() < 1e-6
     x["positions"] = pos.cpu().numpy()
