@@ -448,7 +448,9 @@ __global__ void __launch_bounds__(kSwaThreads, 1)
     Unit x = unit_of(a, u_begin);
     for (int ui = 0; ok && ui < n_units; ++ui, x = next_unit(a, x)) {
       const int grow = x.q0 + r;
-      const int rows_lo = x.q0, rows_hi = x.q0 + kBlockM - 1;
+      // this warp's 32 rows: a tile needs the element mask only if it is not wholly inside each
+      // of their windows
+      const int rows_lo = x.q0 + 32 * quarter, rows_hi = rows_lo + 31;
 
       float m_use = -INFINITY, l_sum = 0.0f;
       for (int t = 0; t < x.n_tiles; ++t) {

@@ -421,7 +421,9 @@ __global__ void __launch_bounds__(kFmhaThreads, 1)
     const int grow = q0 + r;
     const float c = a.scale_log2;
     const float tau = 8.0f / c;
-    const int rows_lo = q0, rows_hi = q0 + kBlockM - 1;
+    // this warp's 32 rows: a tile needs the element mask only if it is not wholly inside each of
+    // their windows
+    const int rows_lo = q0 + 32 * quarter, rows_hi = rows_lo + 31;
     float m_use = -INFINITY, l_sum = 0.0f;
     bool ok = true;
     for (int it = 0; it < n_tiles; ++it) {
